@@ -1,0 +1,65 @@
+"""Glue between the seeded workloads and the float64 oracle (test side only)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from paged_split_kv_gather_gb300.workloads import Workload, q_token_stride, storage_view
+
+
+def np_storage(t: torch.Tensor):
+    """(uint16 numpy array over t's whole CPU storage, element offset)."""
+    flat, off, _ = storage_view(t)
+    return flat.view(torch.int16).numpy().view(np.uint16), off
+
+
+def oracle_pool(t: torch.Tensor) -> oracle.Pool:
+    arr, off = np_storage(t)
+    return oracle.Pool(arr, off, t.shape[0], t.stride(0), t.stride(1), t.stride(2))
+
+
+def oracle_run(w: Workload, rows=None, n_threads: int = 0, seq_lens=None):
+    """Oracle (out, lse) for a CPU workload."""
+    assert w.q.device.type == "cpu"
+    q_arr, q_off = np_storage(w.q)
+    lens = w.seq_lens if seq_lens is None else seq_lens
+    return oracle.paged_attention(
+        q_arr, q_off, q_token_stride(w.q), w.q.stride(2), oracle_pool(w.k), oracle_pool(w.v),
+        w.page_table, lens, q_len=w.q_len, num_qo_heads=w.num_qo_heads,
+        num_kv_heads=w.num_kv_heads, head_dim=w.head_dim, page_size=w.page_size,
+        is_bf16=(w.dtype == "bf16"), causal=w.causal, scale=w.scale, rows=rows,
+        n_threads=n_threads)
+
+
+def gather_tokens(w: Workload, pool: torch.Tensor, b: int, kvh: int, n: int) -> np.ndarray:
+    """float64 rows pool[table[b][t//P], kvh, t%P, :] for t < n (test-side gather)."""
+    t = np.arange(n)
+    pages = torch.as_tensor(w.page_table[b, t // w.page_size].astype(np.int64))
+    slots = torch.as_tensor((t % w.page_size).astype(np.int64))
+    return pool[pages, kvh, slots].double().numpy()
+
+
+def visible(w: Workload, b: int, i: int) -> int:
+    L = int(w.seq_lens[b])
+    if not w.causal:
+        return L
+    return max(0, min(L, L - w.q_len + i + 1))
+
+
+def row_rel_err(got: np.ndarray, ref: np.ndarray) -> float:
+    """max over rows of ||got - ref||_inf / ||ref||_inf (rows = leading dims, last = D)."""
+    got = np.asarray(got, dtype=np.float64).reshape(-1, ref.shape[-1])
+    ref = np.asarray(ref, dtype=np.float64).reshape(-1, ref.shape[-1])
+    num = np.max(np.abs(got - ref), axis=1)
+    den = np.max(np.abs(ref), axis=1)
+    den = np.where(den == 0, 1.0, den)
+    return float(np.max(num / den)) if num.size else 0.0
+
+
+def lse_abs_err(got, ref) -> float:
+    got = np.asarray(got, dtype=np.float64).reshape(-1)
+    ref = np.asarray(ref, dtype=np.float64).reshape(-1)
+    both_inf = np.isneginf(got) & np.isneginf(ref)
+    d = np.where(both_inf, 0.0, np.abs(got - ref))
+    return float(np.max(d)) if d.size else 0.0
