@@ -1,0 +1,428 @@
+"""Benchmark: paged split-KV decode, µs/call and achieved HBM GB/s against the measured peak.
+
+One step = one fdec_run over the workload (split kernel over the gathered
+pages + the log-sum-exp reduction), with every input resident in HBM.  The
+headline workload is the long-context decode at 262144 tokens (batch 1,
+32 query / 4 KV heads, head_dim 128, bf16, page 64, 537 MB of K/V per call,
+more than the 129 MB L2, so consecutive steps do not hit in L2).  The same line
+carries the whole long-context sweep (1900 ... 262144 tokens), each point
+timed per call with an L2 flush before it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fdec|reference]
+
+--impl reference times the float64 CPU oracle on the same workload (a bounded
+sample per step) on this host's cores.  With --gpus N > 1 (torchrun), every
+rank runs its own replica of the workload: the path has no exchange step, so
+there is no collective on the data path (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged split-KV decode: µs/call and achieved HBM GB/s vs GB300 peak, per KV length"
+HEADLINE_LENGTH = 262144
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "paged_split_kv_gather_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_from_profile(workload: str):
+    """DRAM bytes per launch of the split kernel from the committed ncu summary,
+    only while the kernel sources are the ones that summary was taken from."""
+    path = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    entry = d.get(workload)
+    if not entry or entry.get("kernel_source_hash") != _kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fdec_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _make_inputs(length, device):
+    from paged_split_kv_gather_gb300 import workloads as W
+
+    return W.long_context(length, device=device)
+
+
+def _run_fdec(args):
+    import torch
+    import torch.distributed as dist
+
+    import paged_split_kv_gather_gb300 as fd
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    from paged_split_kv_gather_gb300 import workloads as W
+
+    w_host = _make_inputs(HEADLINE_LENGTH, "cpu")  # the same draws the CPU baseline reads
+    w = w_host.to(dev)
+    table = torch.as_tensor(w.page_table, device=dev)
+    lens = torch.as_tensor(w.seq_lens, device=dev)
+    out = torch.empty((1, 1, w.num_qo_heads, w.head_dim), device=dev)
+    lse = torch.empty((1, 1, w.num_qo_heads), device=dev)
+    pd = fd.PagedDecode(w.seq_lens, 1, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
+                        device=dev)
+    info = pd.info
+    kv_bytes = w.kv_bytes
+
+    def step():
+        pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps, barrier + synchronize on both sides
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for ev in starts + mids + ends:  # create the CUDA events before the timed region
+        ev.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            starts[i].record(stream)
+            fd.fdec_plan_set_split_event(pd.plan, mids[i])
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    fd.fdec_plan_set_split_event(pd.plan, None)
+    if world > 1:
+        dist.barrier()
+    total_ms = starts[0].elapsed_time(ends[-1])
+    split_ms = float(np.mean([s.elapsed_time(m) for s, m in zip(starts, mids)]))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    assert pd.device_errors() == 0, "device-side check fired during the benchmark"
+
+    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+    achieved = kv_bytes / (split_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API from pinned host buffers
+    h_q = w.q.cpu().pin_memory()
+    h_table = torch.as_tensor(w.page_table).pin_memory()
+    h_lens = torch.as_tensor(w.seq_lens).pin_memory()
+    h_out = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    d_q = torch.empty_like(w.q)
+    e2e_steps = max(10, min(args.steps, 2000))
+    for i in range(args.warmup + e2e_steps):
+        if i == args.warmup:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+        d_q.copy_(h_q, non_blocking=True)
+        table.copy_(h_table, non_blocking=True)
+        lens.copy_(h_lens, non_blocking=True)
+        pd.run(d_q, w.k, w.v, table, lens, out, lse, scale=w.scale)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    h2d = h_q.numel() * 2 + h_table.numel() * 4 + h_lens.numel() * 4
+    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+
+    # ---- the long-context sweep: per-call time with an L2 flush before each call
+    sweep = []
+    if not args.no_sweep:
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        for length in W.LONG_CONTEXT_LENGTHS:
+            ws = w if length == HEADLINE_LENGTH else _make_inputs(length, dev)
+            pds = pd if length == HEADLINE_LENGTH else fd.PagedDecode(
+                ws.seq_lens, 1, ws.page_size, ws.num_qo_heads, ws.num_kv_heads, ws.head_dim, ws.dtype, device=dev)
+            tb = torch.as_tensor(ws.page_table, device=dev)
+            ln = torch.as_tensor(ws.seq_lens, device=dev)
+            for _ in range(3):
+                pds.run(ws.q, ws.k, ws.v, tb, ln, out, lse, scale=ws.scale)
+            times = []
+            for _ in range(args.sweep_calls):
+                flush.zero_()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record()
+                pds.run(ws.q, ws.k, ws.v, tb, ln, out, lse, scale=ws.scale)
+                b.record()
+                b.synchronize()
+                times.append(a.elapsed_time(b) * 1e3)
+            us = float(np.median(times))
+            gbs = ws.kv_bytes / (us * 1e-6) / 1e9
+            sweep.append({"kv_len": length, "us_per_call": round(us, 2), "us_min": round(min(times), 2),
+                          "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                          "splits": int(pds.info["max_splits"]), "launches": int(pds.info["launches"])})
+            if ws is not w:
+                del pds, ws
+        del flush
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = _cpu_baseline(w_host, kv_bytes, args.cpu_seconds)
+
+    if rank == 0:
+        traffic = _traffic_from_profile("long_context_decode_L262144")
+        line = {
+            "metric": METRIC,
+            "value": round(value, 1),
+            "unit": "GB/s",
+            "us_per_call": round(ms_per_step * 1e3, 2),
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded normal q/K/V, 1% spiked keys, shuffled pages)",
+            "config": {"workload": "long_context_decode_L262144", "batch": 1, "q_len": 1, "num_qo_heads": 32,
+                       "num_kv_heads": 4, "head_dim": 128, "page_size": 64, "kv_len": HEADLINE_LENGTH,
+                       "kv_bytes_per_call": kv_bytes, "out": "fp32 out + lse",
+                       "l2": "inputs larger than L2 (537 MB of K/V per step vs 129 MB L2); sweep points flush L2",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "plan": {k: info[k] for k in ("blocks_per_split", "num_split_ctas", "max_splits",
+                                                      "reduce_passes", "launches")}},
+            "roofline": {"bound": "hbm", "kernel": f"split_kernel<128,{info['rows_per_group']},bf16>", "achieved": round(achieved, 1),
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes,
+                         "split_kernel_us": round(split_ms * 1e3, 2)},
+            "e2e": {"value": round(kv_bytes / e2e_s / 1e9, 1), "unit": "GB/s", "us_per_call": round(e2e_s * 1e6, 2),
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "note": "per step: pinned H2D of q, page table and seq_lens, fdec_run, D2H of out and lse, "
+                            "stream sync; the K/V cache stays resident (decode state)"},
+            "gpu_launches": int(info["launches"]) * args.steps,
+            "clocks": clocks.summary(),
+            "cpu_baseline": cpu,
+            "sweep": sweep,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _cpu_baseline(c, kv_bytes, seconds):
+    """Time the float64 oracle as it stands on this host's cores, over passes of
+    the full headline workload (all 32 query rows), until `seconds` have elapsed."""
+    import oracle  # test-infrastructure oracle: the reported CPU baseline
+
+    from paged_split_kv_gather_gb300.workloads import q_token_stride, storage_view
+
+    def pool(t):
+        base, off, _ = storage_view(t)
+        return oracle.Pool(base.view(__import__("torch").int16).numpy().view(np.uint16), off, t.shape[0],
+                           t.stride(0), t.stride(1), t.stride(2))
+
+    qb, qoff, _ = storage_view(c.q)
+    q_arr = qb.view(__import__("torch").int16).numpy().view(np.uint16)
+    kp, vp = pool(c.k), pool(c.v)
+    cores = os.cpu_count() or 1
+
+    def one():
+        oracle.paged_attention(q_arr, qoff, q_token_stride(c.q), c.q.stride(2), kp, vp, c.page_table, c.seq_lens,
+                               q_len=1, num_qo_heads=c.num_qo_heads, num_kv_heads=c.num_kv_heads,
+                               head_dim=c.head_dim, page_size=c.page_size, is_bf16=True, causal=False,
+                               scale=c.scale, n_threads=cores)
+
+    one()  # warm (page in)
+    passes = 0
+    t0 = time.perf_counter()
+    while True:
+        one()
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or passes >= 1000:
+            break
+    per = el / passes
+    return {"value": round(kv_bytes / per / 1e9, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "ms_per_call": round(per * 1e3, 2),
+            "sample": f"{passes} full passes (all 32 query rows x 262144 tokens) of the headline workload in "
+                      f"{el:.1f} s, float64, OpenMP over rows"}
+
+
+def _run_reference(args):
+    """The reference arm: the float64 CPU oracle, as it stands, on the same workload."""
+    world, rank, local = _dist()
+    if rank != 0:
+        return
+    import torch
+
+    import oracle
+    from paged_split_kv_gather_gb300.workloads import q_token_stride, storage_view
+
+    c = _make_inputs(HEADLINE_LENGTH, "cpu")
+    kv_bytes = c.kv_bytes
+
+    def arr(t):
+        base, off, _ = storage_view(t)
+        return base.view(torch.int16).numpy().view(np.uint16), off
+
+    def pool(t):
+        a, off = arr(t)
+        return oracle.Pool(a, off, t.shape[0], t.stride(0), t.stride(1), t.stride(2))
+
+    q_arr, q_off = arr(c.q)
+    kp, vp = pool(c.k), pool(c.v)
+    cores = os.cpu_count() or 1
+    # a bounded sample per step: 8 of the 32 query rows (two per KV head), full length
+    rows = np.array([h for h in range(32) if h % 4 == 0], dtype=np.int64)
+    frac = len(rows) / 32.0
+
+    def step():
+        oracle.paged_attention(q_arr, q_off, q_token_stride(c.q), c.q.stride(2), kp, vp, c.page_table,
+                               c.seq_lens, q_len=1, num_qo_heads=32, num_kv_heads=4, head_dim=128, page_size=64,
+                               is_bf16=True, causal=False, scale=c.scale, rows=rows, n_threads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    steps = 0
+    for _ in range(args.steps):
+        step()
+        steps += 1
+        if time.perf_counter() - t0 > args.reference_seconds:
+            break  # bounded: the reference arm must finish within minutes
+    el = time.perf_counter() - t0
+    args.steps = steps
+    per_row_sample = el / steps
+    per_call = per_row_sample / frac  # the whole call's rows at the sampled rate
+    value = kv_bytes / per_call / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "us_per_call": round(per_call * 1e6, 1), "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(per_row_sample * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded normal q/K/V, 1% spiked keys, shuffled pages)",
+        "config": {"workload": "long_context_decode_L262144", "batch": 1, "q_len": 1, "num_qo_heads": 32,
+                   "num_kv_heads": 4, "head_dim": 128, "page_size": 64, "kv_len": HEADLINE_LENGTH,
+                   "kv_bytes_per_call": kv_bytes},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step {len(rows)} of 32 query rows over all 262144 tokens; "
+                                   f"value scaled to the whole call"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["fdec", "reference"], default="fdec")
+    ap.add_argument("--sweep-calls", type=int, default=50)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-seconds", type=float, default=120.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        _run_reference(args)
+    else:
+        _run_fdec(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,608 @@
+// fdec_api.cu -- the C ABI: planning, validation, upload, launch and errors.
+//
+// Planning follows the dispatch lesson of the HRX decode-split issue: the
+// split path must be chosen at every context length (its matcher once stopped
+// at a capacity of 2048 = 32 blocks x 64 tokens and handed longer contexts to
+// a serial fallback, -32% at depth 2100).  Here every sequence is cut into
+// splits of whole 64-token blocks, the split count follows the machine (SM
+// count) and the batch, and the reduction takes as many passes as needed.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <functional>
+#include <new>
+#include <queue>
+#include <string>
+#include <vector>
+
+#include "../../include/fdec.h"
+#include "fdec_internal.h"
+#include "split_kernel.cuh"
+
+using namespace fdec;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+fdec_status fail(fdec_status st, const std::string& msg) {
+    g_last_error = msg;
+    return st;
+}
+
+fdec_status fail_cuda(cudaError_t e, const char* what) {
+    g_last_error = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    return FDEC_ERR_CUDA;
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int ilog2_exact(int x) {
+    int s = 0;
+    while ((1 << s) < x) ++s;
+    return (1 << s) == x ? s : -1;
+}
+
+int next_pow2(int x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+bool head_dim_supported(int d) { return d == 64 || d == 128 || d == 192 || d == 256 || d == 512; }
+
+template <int D>
+size_t smem_for_rc(int rc) {
+    switch (rc) {
+        case 1: return SplitLayout<D, 1>::SMEM;
+        case 2: return SplitLayout<D, 2>::SMEM;
+        case 4: return SplitLayout<D, 4>::SMEM;
+        case 8:
+            if constexpr (SplitShape<D>::RCMAX >= 8) return SplitLayout<D, 8>::SMEM;
+            return 0;
+        case 16:
+            if constexpr (SplitShape<D>::RCMAX >= 16) return SplitLayout<D, 16>::SMEM;
+            return 0;
+        default: return 0;
+    }
+}
+
+}  // namespace
+
+namespace fdec {
+
+size_t split_smem_bytes(int d, int rc) {
+    switch (d) {
+        case 64: return smem_for_rc<64>(rc);
+        case 128: return smem_for_rc<128>(rc);
+        case 192: return smem_for_rc<192>(rc);
+        case 256: return smem_for_rc<256>(rc);
+        case 512: return smem_for_rc<512>(rc);
+        default: return 0;
+    }
+}
+
+int split_threads(int d) {
+    switch (d) {
+        case 64: return (SplitShape<64>::NW + 1) * 32;
+        case 128: return (SplitShape<128>::NW + 1) * 32;
+        case 192: return (SplitShape<192>::NW + 1) * 32;
+        case 256: return (SplitShape<256>::NW + 1) * 32;
+        case 512: return (SplitShape<512>::NW + 1) * 32;
+        default: return 0;
+    }
+}
+
+int split_max_rc(int d) {
+    switch (d) {
+        case 64: return SplitShape<64>::RCMAX;
+        case 128: return SplitShape<128>::RCMAX;
+        case 192: return SplitShape<192>::RCMAX;
+        case 256: return SplitShape<256>::RCMAX;
+        case 512: return SplitShape<512>::RCMAX;
+        default: return 0;
+    }
+}
+
+}  // namespace fdec
+
+struct fdec_plan_s {
+    int batch = 0, q_len = 1, page_size = 1, page_shift = 0;
+    int hq = 0, hk = 0, head_dim = 0, group = 1, rows = 1;
+    fdec_dtype dtype = FDEC_BF16;
+    int causal = 0;
+    int path = FDEC_PATH_SIMT;
+    int rc = 1, row_groups = 1;
+    int blocks_per_split = 1, fanin = 64, num_sms = 0, ctas_per_sm = 1;
+    int max_pages_needed = 0;  // max_b ceil(capacity_b / page_size)
+    std::vector<int32_t> capacity;
+    std::vector<int32_t> splits;  // per sequence
+    std::vector<WorkItem> items;
+    std::vector<std::vector<ReduceTask>> passes;
+    // workspace layout
+    size_t off_err = 0, off_cap = 0, off_items = 0;
+    std::vector<size_t> off_tasks;
+    size_t off_a_o = 0, off_a_ml = 0, off_b_o = 0, off_b_ml = 0;
+    size_t slots_a = 0, slots_b = 0;
+    size_t meta_bytes = 0, ws_bytes = 0;
+    std::vector<uint8_t> meta;  // host image of [0, meta_bytes)
+    void* uploaded = nullptr;
+    cudaEvent_t split_event = nullptr;
+};
+
+namespace {
+
+// Longest-processing-time makespan of `sizes` (each repeated `copies` times)
+// on `slots` identical CTA slots, plus a fixed cost per item.
+double lpt_makespan(std::vector<int> sizes, int copies, int slots, double per_item) {
+    std::sort(sizes.begin(), sizes.end(), std::greater<int>());
+    std::priority_queue<double, std::vector<double>, std::greater<double>> load;
+    for (int i = 0; i < slots; ++i) load.push(0.0);
+    double worst = 0.0;
+    for (int s : sizes) {
+        for (int c = 0; c < copies; ++c) {
+            double l = load.top();
+            load.pop();
+            l += s + per_item;
+            worst = std::max(worst, l);
+            load.push(l);
+        }
+    }
+    return worst;
+}
+
+std::vector<int> item_sizes(const std::vector<int>& nblocks, int C) {
+    std::vector<int> out;
+    for (int nb : nblocks) {
+        int left = nb;
+        do {
+            out.push_back(std::min(C, std::max(left, 0)));
+            left -= C;
+        } while (left > 0);
+    }
+    return out;
+}
+
+int choose_blocks_per_split(const std::vector<int>& nblocks, int copies, int slots) {
+    const int max_nb = std::max(1, *std::max_element(nblocks.begin(), nblocks.end()));
+    long long total = 0;
+    for (int nb : nblocks) total += std::max(nb, 1);
+    // Cost model in units of one 64-token block streamed by one CTA slot: the
+    // LPT makespan of the items, a fixed start-up cost per item, and the extra
+    // reduction launch when any sequence is split.
+    const double per_item = 2.0;
+    const double reduce_cost = 4.0;
+    std::vector<int> cands;
+    const long long lo = std::max<long long>(1, (total * copies) / (8LL * slots));
+    if (max_nb - lo <= 512) {
+        for (long long c = lo; c <= max_nb; ++c) cands.push_back(static_cast<int>(c));
+    } else {
+        for (double c = static_cast<double>(lo); c < max_nb; c *= 1.02) cands.push_back(static_cast<int>(c));
+        cands.push_back(max_nb);
+    }
+    int best = max_nb;
+    double best_cost = 1e300;
+    for (int C : cands) {
+        const std::vector<int> sizes = item_sizes(nblocks, C);
+        const bool split = sizes.size() > nblocks.size();
+        const double cost = lpt_makespan(sizes, copies, slots, per_item) + (split ? reduce_cost : 0.0);
+        if (cost < best_cost - 1e-9 || (std::fabs(cost - best_cost) <= 1e-9 && C > best)) {
+            best_cost = cost;
+            best = C;
+        }
+    }
+    return best;
+}
+
+cudaError_t dispatch_split(const fdec_plan_s* p, const SplitParams& sp, dim3 grid, cudaStream_t stream, bool launch) {
+    const bool bf16 = p->dtype == FDEC_BF16;
+    switch (p->head_dim) {
+        case 64: return launch_split_d64(sp, p->rc, bf16, grid, stream, launch);
+        case 128: return launch_split_d128(sp, p->rc, bf16, grid, stream, launch);
+        case 192: return launch_split_d192(sp, p->rc, bf16, grid, stream, launch);
+        case 256: return launch_split_d256(sp, p->rc, bf16, grid, stream, launch);
+        case 512: return launch_split_d512(sp, p->rc, bf16, grid, stream, launch);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+void log_plan(const fdec_plan_s* p) {
+    const char* env = std::getenv("FDEC_LOG");
+    if (env == nullptr || env[0] == '0') return;
+    int max_s = 0;
+    for (int s : p->splits) max_s = std::max(max_s, s);
+    std::fprintf(stderr,
+                 "[fdec] plan: batch=%d q_len=%d Hq=%d Hk=%d D=%d P=%d rows=%d path=%s rc=%d row_groups=%d "
+                 "blocks_per_split=%d items=%zu max_splits=%d reduce_passes=%zu sms=%d ctas/sm=%d "
+                 "workspace=%zu B\n",
+                 p->batch, p->q_len, p->hq, p->hk, p->head_dim, p->page_size, p->rows,
+                 p->path == FDEC_PATH_MMA ? "mma" : "simt", p->rc, p->row_groups, p->blocks_per_split,
+                 p->items.size(), max_s, p->passes.size(), p->num_sms, p->ctas_per_sm, p->ws_bytes);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fdec_last_error(void) { return g_last_error.c_str(); }
+
+const char* fdec_version(void) { return "fdec 0.1.0 (sm_103a)"; }
+
+fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int page_size, int num_qo_heads,
+                      int num_kv_heads, int head_dim, fdec_dtype dtype, int causal, const fdec_plan_opts* opts,
+                      fdec_plan_t* out_plan, size_t* workspace_bytes) {
+    g_last_error.clear();
+    if (out_plan == nullptr || workspace_bytes == nullptr) return fail(FDEC_ERR_INVALID_ARG, "null output pointer");
+    *out_plan = nullptr;
+    *workspace_bytes = 0;
+    if (batch < 1 || seq_lens_host == nullptr) return fail(FDEC_ERR_INVALID_ARG, "batch must be >= 1 with seq_lens");
+    if (q_len < 1) return fail(FDEC_ERR_INVALID_ARG, "q_len must be >= 1");
+    if (num_qo_heads < 1 || num_kv_heads < 1 || num_qo_heads % num_kv_heads != 0)
+        return fail(FDEC_ERR_INVALID_ARG, "num_qo_heads must be a positive multiple of num_kv_heads");
+    if (dtype != FDEC_F16 && dtype != FDEC_BF16) return fail(FDEC_ERR_INVALID_ARG, "dtype must be FDEC_F16 or FDEC_BF16");
+    if (!head_dim_supported(head_dim))
+        return fail(FDEC_ERR_UNSUPPORTED, "head_dim must be one of 64, 128, 192, 256, 512");
+    const int pshift = ilog2_exact(page_size);
+    if (page_size < 1 || page_size > 256 || pshift < 0)
+        return fail(FDEC_ERR_UNSUPPORTED, "page_size must be a power of two in [1, 256]");
+    fdec_plan_opts o{};
+    if (opts != nullptr) o = *opts;
+    if (o.blocks_per_split < 0 || o.reducer_fanin < 0 || o.num_sms < 0 || (o.reducer_fanin == 1))
+        return fail(FDEC_ERR_INVALID_ARG, "invalid plan options");
+    if (o.path != FDEC_PATH_AUTO && o.path != FDEC_PATH_SIMT && o.path != FDEC_PATH_MMA)
+        return fail(FDEC_ERR_INVALID_ARG, "invalid path option");
+    if (o.path == FDEC_PATH_MMA) return fail(FDEC_ERR_UNSUPPORTED, "the tensor-core path is not built in this version");
+    const long long rows_ll = static_cast<long long>(q_len) * (num_qo_heads / num_kv_heads);
+    if (rows_ll > (1 << 24)) return fail(FDEC_ERR_UNSUPPORTED, "q_len x group too large");
+    for (int b = 0; b < batch; ++b)
+        if (seq_lens_host[b] < 0) return fail(FDEC_ERR_INVALID_ARG, "negative sequence capacity");
+
+    int num_sms = o.num_sms;
+    if (num_sms == 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail_cuda(e, "querying the SM count (pass opts.num_sms to plan without a device)");
+        }
+    }
+
+    fdec_plan_s* p = new (std::nothrow) fdec_plan_s();
+    if (p == nullptr) return fail(FDEC_ERR_INVALID_ARG, "out of host memory");
+    p->batch = batch;
+    p->q_len = q_len;
+    p->page_size = page_size;
+    p->page_shift = pshift;
+    p->hq = num_qo_heads;
+    p->hk = num_kv_heads;
+    p->head_dim = head_dim;
+    p->group = num_qo_heads / num_kv_heads;
+    p->rows = static_cast<int>(rows_ll);
+    p->dtype = dtype;
+    p->causal = (causal != 0 && q_len > 1) ? 1 : 0;
+    p->path = FDEC_PATH_SIMT;
+    p->num_sms = num_sms;
+    p->fanin = o.reducer_fanin > 0 ? o.reducer_fanin : 64;
+    p->rc = std::min(next_pow2(p->rows), split_max_rc(head_dim));
+    p->row_groups = (p->rows + p->rc - 1) / p->rc;
+    const size_t smem = split_smem_bytes(head_dim, p->rc);
+    const int threads = split_threads(head_dim);
+    p->ctas_per_sm = std::max(1, std::min(static_cast<int>(233472 / (smem + 1024)), 2048 / threads));
+
+    p->capacity.assign(seq_lens_host, seq_lens_host + batch);
+    std::vector<int> nblocks(batch);
+    for (int b = 0; b < batch; ++b) {
+        nblocks[b] = std::max(1, (p->capacity[b] + kBlockTokens - 1) / kBlockTokens);
+        p->max_pages_needed = std::max(p->max_pages_needed, (p->capacity[b] + page_size - 1) / page_size);
+    }
+    const int copies = p->hk * p->row_groups;
+    const int slots = num_sms * p->ctas_per_sm;
+    p->blocks_per_split = o.blocks_per_split > 0 ? o.blocks_per_split : choose_blocks_per_split(nblocks, copies, slots);
+    const int C = p->blocks_per_split;
+
+    // Work items and level-0 partial slots.
+    p->splits.resize(batch);
+    std::vector<int> slot_base(batch, -1);
+    size_t next_slot = 0;
+    for (int b = 0; b < batch; ++b) {
+        const int ns = (nblocks[b] + C - 1) / C;
+        p->splits[b] = ns;
+        if (ns > 1) {
+            slot_base[b] = static_cast<int>(next_slot);
+            next_slot += ns;
+        }
+        for (int k = 0; k < ns; ++k) {
+            WorkItem it;
+            it.seq = b;
+            it.block_begin = k * C;
+            it.block_end = std::min((k + 1) * C, nblocks[b]);
+            it.slot = ns > 1 ? slot_base[b] + k : -1;
+            p->items.push_back(it);
+        }
+    }
+    // Longest items first: the hardware hands out CTAs roughly in index order.
+    std::stable_sort(p->items.begin(), p->items.end(), [](const WorkItem& a, const WorkItem& b) {
+        return (a.block_end - a.block_begin) > (b.block_end - b.block_begin);
+    });
+    p->slots_a = next_slot;
+
+    // Reduction passes: level l merges groups of `fanin` slots; levels alternate
+    // between region A (even) and region B (odd).
+    std::vector<int> n_cur(batch), base_cur(slot_base);
+    for (int b = 0; b < batch; ++b) n_cur[b] = p->splits[b] > 1 ? p->splits[b] : 1;
+    size_t max_b = 0;
+    for (int level = 0;; ++level) {
+        std::vector<ReduceTask> tasks;
+        size_t next_base = 0;
+        std::vector<int> n_next(batch, 1), base_next(batch, -1);
+        for (int b = 0; b < batch; ++b) {
+            if (n_cur[b] <= 1) continue;
+            const int groups = (n_cur[b] + p->fanin - 1) / p->fanin;
+            if (groups > 1) {
+                base_next[b] = static_cast<int>(next_base);
+                next_base += groups;
+            }
+            n_next[b] = groups;
+            for (int gi = 0; gi < groups; ++gi) {
+                ReduceTask t;
+                t.seq = b;
+                t.src = base_cur[b] + gi * p->fanin;
+                t.count = std::min(p->fanin, n_cur[b] - gi * p->fanin);
+                t.dst = groups > 1 ? base_next[b] + gi : -1;
+                tasks.push_back(t);
+            }
+        }
+        if (tasks.empty()) break;
+        if (level % 2 == 0)
+            max_b = std::max(max_b, next_base);
+        else
+            p->slots_a = std::max(p->slots_a, next_base);
+        p->passes.push_back(std::move(tasks));
+        n_cur = n_next;
+        base_cur = base_next;
+    }
+    p->slots_b = max_b;
+
+    // Workspace layout: metadata first (uploaded), partial regions after.
+    size_t off = 0;
+    p->off_err = off;
+    off = align_up(off + sizeof(uint32_t));
+    p->off_cap = off;
+    off = align_up(off + sizeof(int32_t) * batch);
+    p->off_items = off;
+    off = align_up(off + sizeof(WorkItem) * p->items.size());
+    for (const auto& t : p->passes) {
+        p->off_tasks.push_back(off);
+        off = align_up(off + sizeof(ReduceTask) * t.size());
+    }
+    p->meta_bytes = off;
+    const size_t per_slot_o = static_cast<size_t>(p->hk) * p->rows * head_dim * sizeof(float);
+    const size_t per_slot_ml = static_cast<size_t>(p->hk) * p->rows * sizeof(float2);
+    p->off_a_o = off;
+    off = align_up(off + per_slot_o * p->slots_a);
+    p->off_a_ml = off;
+    off = align_up(off + per_slot_ml * p->slots_a);
+    p->off_b_o = off;
+    off = align_up(off + per_slot_o * p->slots_b);
+    p->off_b_ml = off;
+    off = align_up(off + per_slot_ml * p->slots_b);
+    p->ws_bytes = off;
+
+    p->meta.assign(p->meta_bytes, 0);
+    std::memcpy(p->meta.data() + p->off_cap, p->capacity.data(), sizeof(int32_t) * batch);
+    std::memcpy(p->meta.data() + p->off_items, p->items.data(), sizeof(WorkItem) * p->items.size());
+    for (size_t i = 0; i < p->passes.size(); ++i)
+        std::memcpy(p->meta.data() + p->off_tasks[i], p->passes[i].data(), sizeof(ReduceTask) * p->passes[i].size());
+
+    log_plan(p);
+    *out_plan = p;
+    *workspace_bytes = p->ws_bytes;
+    return FDEC_OK;
+}
+
+fdec_status fdec_plan_destroy(fdec_plan_t plan) {
+    delete plan;
+    return FDEC_OK;
+}
+
+fdec_status fdec_plan_get_info(fdec_plan_t p, fdec_plan_info* info) {
+    if (p == nullptr || info == nullptr) return fail(FDEC_ERR_INVALID_ARG, "null argument");
+    std::memset(info, 0, sizeof(*info));
+    info->path = p->path;
+    info->blocks_per_split = p->blocks_per_split;
+    info->num_items = static_cast<int>(p->items.size());
+    info->num_split_ctas = static_cast<int>(p->items.size()) * p->hk * p->row_groups;
+    info->row_groups = p->row_groups;
+    info->rows_per_group = p->rc;
+    for (int s : p->splits) info->max_splits = std::max(info->max_splits, s);
+    info->reduce_passes = static_cast<int>(p->passes.size());
+    info->launches = 1 + static_cast<int>(p->passes.size());
+    info->num_sms = p->num_sms;
+    info->workspace_bytes = p->ws_bytes;
+    return FDEC_OK;
+}
+
+fdec_status fdec_plan_get_splits(fdec_plan_t p, int32_t* splits, int batch) {
+    if (p == nullptr || splits == nullptr || batch != p->batch) return fail(FDEC_ERR_INVALID_ARG, "bad arguments");
+    std::memcpy(splits, p->splits.data(), sizeof(int32_t) * batch);
+    return FDEC_OK;
+}
+
+fdec_status fdec_plan_set_split_event(fdec_plan_t p, cudaEvent_t event) {
+    if (p == nullptr) return fail(FDEC_ERR_INVALID_ARG, "null plan");
+    p->split_event = event;
+    return FDEC_OK;
+}
+
+fdec_status fdec_plan_upload(fdec_plan_t p, void* workspace, cudaStream_t stream) {
+    g_last_error.clear();
+    if (p == nullptr || workspace == nullptr) return fail(FDEC_ERR_INVALID_ARG, "null plan or workspace");
+    if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0)
+        return fail(FDEC_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
+    if (cap != cudaStreamCaptureStatusNone)
+        return fail(FDEC_ERR_CAPTURING, "fdec_plan_upload must not run while the stream is capturing");
+    // Set the split kernel's shared-memory attribute here, outside any capture.
+    SplitParams none{};
+    e = dispatch_split(p, none, dim3(1, 1, 1), stream, false);
+    if (e != cudaSuccess) return fail_cuda(e, "preparing the split kernel");
+    e = cudaMemcpyAsync(workspace, p->meta.data(), p->meta_bytes, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "uploading the plan");
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail_cuda(e, "uploading the plan");
+    p->uploaded = workspace;
+    return FDEC_OK;
+}
+
+fdec_status fdec_read_device_errors(fdec_plan_t p, void* workspace, uint32_t* flags, int clear, cudaStream_t stream) {
+    if (p == nullptr || workspace == nullptr || flags == nullptr) return fail(FDEC_ERR_INVALID_ARG, "null argument");
+    uint32_t v = 0;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaError_t e = cudaMemcpyAsync(&v, ws + p->off_err, sizeof(v), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess && clear) e = cudaMemsetAsync(ws + p->off_err, 0, sizeof(v), stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail_cuda(e, "reading the device error word");
+    *flags = v;
+    return FDEC_OK;
+}
+
+fdec_status fdec_run(fdec_plan_t p, const void* q, int64_t q_stride_tok, int64_t q_stride_head, fdec_kv_desc k,
+                     fdec_kv_desc v, const int32_t* page_table, int64_t page_table_stride,
+                     const int32_t* seq_lens_dev, float scale, float* out, float* lse, void* workspace,
+                     cudaStream_t stream) {
+    if (p == nullptr) return fail(FDEC_ERR_INVALID_ARG, "null plan");
+    if (q == nullptr || k.base == nullptr || v.base == nullptr || page_table == nullptr || seq_lens_dev == nullptr ||
+        out == nullptr)
+        return fail(FDEC_ERR_INVALID_ARG, "null q, K, V, page_table, seq_lens or out");
+    if (k.num_pages < 1 || v.num_pages < 1) return fail(FDEC_ERR_INVALID_ARG, "K and V pools need at least one page");
+    if (k.num_pages > INT32_MAX || v.num_pages > INT32_MAX) return fail(FDEC_ERR_INVALID_ARG, "too many pages");
+    if (page_table_stride < p->max_pages_needed)
+        return fail(FDEC_ERR_CAPACITY, "page_table_stride is smaller than ceil(capacity / page_size)");
+    if (!std::isfinite(scale)) return fail(FDEC_ERR_INVALID_ARG, "scale must be finite");
+    const fdec_kv_desc* descs[2] = {&k, &v};
+    for (const fdec_kv_desc* d : descs) {
+        if (reinterpret_cast<uintptr_t>(d->base) % 16 != 0)
+            return fail(FDEC_ERR_LAYOUT, "K/V base must be 16-byte aligned");
+        if (d->stride_page % 8 != 0 || d->stride_head % 8 != 0 || d->stride_token % 8 != 0)
+            return fail(FDEC_ERR_LAYOUT, "K/V strides must be multiples of 8 elements (16 bytes)");
+        if (d->stride_page < 0 || d->stride_head < 0 || d->stride_token < 0)
+            return fail(FDEC_ERR_LAYOUT, "negative K/V stride");
+    }
+    if (reinterpret_cast<uintptr_t>(q) % 2 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0 ||
+        (lse != nullptr && reinterpret_cast<uintptr_t>(lse) % 4 != 0))
+        return fail(FDEC_ERR_LAYOUT, "misaligned q, out or lse");
+    if (workspace == nullptr || workspace != p->uploaded)
+        return fail(FDEC_ERR_WORKSPACE, "workspace is not the buffer this plan was uploaded to");
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    SplitParams sp;
+    sp.q = static_cast<const uint16_t*>(q);
+    sp.q_stride_tok = q_stride_tok;
+    sp.q_stride_head = q_stride_head;
+    sp.k_base = static_cast<const uint8_t*>(k.base);
+    sp.k_pages = k.num_pages;
+    sp.k_sp = k.stride_page * 2;
+    sp.k_sh = k.stride_head * 2;
+    sp.k_st = k.stride_token * 2;
+    sp.v_base = static_cast<const uint8_t*>(v.base);
+    sp.v_pages = v.num_pages;
+    sp.v_sp = v.stride_page * 2;
+    sp.v_sh = v.stride_head * 2;
+    sp.v_st = v.stride_token * 2;
+    sp.page_table = page_table;
+    sp.pt_stride = page_table_stride;
+    sp.seq_lens = seq_lens_dev;
+    sp.capacity = reinterpret_cast<const int32_t*>(ws + p->off_cap);
+    sp.items = reinterpret_cast<const WorkItem*>(ws + p->off_items);
+    sp.part_o = reinterpret_cast<float*>(ws + p->off_a_o);
+    sp.part_ml = reinterpret_cast<float2*>(ws + p->off_a_ml);
+    sp.out = out;
+    sp.lse = lse;
+    sp.err = reinterpret_cast<unsigned*>(ws + p->off_err);
+    sp.q_len = p->q_len;
+    sp.hq = p->hq;
+    sp.hk = p->hk;
+    sp.group = p->group;
+    sp.rows = p->rows;
+    sp.page_shift = p->page_shift;
+    sp.causal = p->causal;
+    sp.scale_log2 = scale * 1.4426950408889634074f;
+
+    const dim3 grid(static_cast<unsigned>(p->items.size()), static_cast<unsigned>(p->hk),
+                    static_cast<unsigned>(p->row_groups));
+    cudaError_t e = dispatch_split(p, sp, grid, stream, true);
+    if (e != cudaSuccess) return fail_cuda(e, "launching the split kernel");
+    if (p->split_event != nullptr) {
+        e = cudaEventRecord(p->split_event, stream);
+        if (e != cudaSuccess) return fail_cuda(e, "recording the split event");
+    }
+
+    for (size_t level = 0; level < p->passes.size(); ++level) {
+        ReduceParams rp;
+        const bool from_a = (level % 2 == 0);
+        rp.tasks = reinterpret_cast<const ReduceTask*>(ws + p->off_tasks[level]);
+        rp.src_o = reinterpret_cast<const float*>(ws + (from_a ? p->off_a_o : p->off_b_o));
+        rp.src_ml = reinterpret_cast<const float2*>(ws + (from_a ? p->off_a_ml : p->off_b_ml));
+        rp.src_lse = nullptr;
+        rp.dst_o = reinterpret_cast<float*>(ws + (from_a ? p->off_b_o : p->off_a_o));
+        rp.dst_ml = reinterpret_cast<float2*>(ws + (from_a ? p->off_b_ml : p->off_a_ml));
+        rp.out = out;
+        rp.lse = lse;
+        rp.hk = p->hk;
+        rp.rows = p->rows;
+        rp.group = p->group;
+        rp.q_len = p->q_len;
+        rp.hq = p->hq;
+        rp.head_dim = p->head_dim;
+        rp.normalized_input = 0;
+        rp.src_rows_stride = p->rows;
+        e = launch_reduce(rp, static_cast<int>(p->passes[level].size()), stream);
+        if (e != cudaSuccess) return fail_cuda(e, "launching the reduction");
+    }
+    return FDEC_OK;
+}
+
+fdec_status fdec_merge_states(const float* o, const float* lse, int n_states, int rows, int head_dim, float* o_out,
+                              float* lse_out, cudaStream_t stream) {
+    if (o == nullptr || lse == nullptr || o_out == nullptr) return fail(FDEC_ERR_INVALID_ARG, "null pointer");
+    if (n_states < 1 || rows < 1 || head_dim < 1 || head_dim > 512)
+        return fail(FDEC_ERR_INVALID_ARG, "need n_states >= 1, rows >= 1, 1 <= head_dim <= 512");
+    if (reinterpret_cast<uintptr_t>(o) % 4 != 0 || reinterpret_cast<uintptr_t>(lse) % 4 != 0 ||
+        reinterpret_cast<uintptr_t>(o_out) % 4 != 0 || (lse_out != nullptr && reinterpret_cast<uintptr_t>(lse_out) % 4 != 0))
+        return fail(FDEC_ERR_LAYOUT, "misaligned float arrays");
+    // One task over all states; the rows are one "KV head" of `rows` rows, and
+    // row r is written to output row r (group = rows, q_len = 1, Hq = rows).
+    ReduceParams rp;
+    rp.tasks = nullptr;
+    rp.src_o = o;
+    rp.src_ml = nullptr;
+    rp.src_lse = lse;
+    rp.dst_o = nullptr;
+    rp.dst_ml = nullptr;
+    rp.out = o_out;
+    rp.lse = lse_out;
+    rp.hk = 1;
+    rp.rows = rows;
+    rp.group = rows;
+    rp.q_len = 1;
+    rp.hq = rows;
+    rp.head_dim = head_dim;
+    rp.normalized_input = 1;
+    rp.src_rows_stride = rows;
+    ReduceTask single;
+    single.seq = 0;
+    single.src = 0;
+    single.count = n_states;
+    single.dst = -1;
+    cudaError_t e = launch_reduce_single(rp, single, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "launching the merge");
+    return FDEC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,91 @@
+// fdec_internal.h -- kernel parameter blocks and launcher declarations shared by
+// the C-ABI layer (fdec_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace fdec {
+
+// The split granularity: every split is a run of whole 64-token blocks (the HRX
+// decode_split producer runs one workgroup per 64-token KV block).
+constexpr int kBlockTokens = 64;
+// One pipeline stage carries 32 consecutive tokens of K and V (one per lane).
+constexpr int kStageTokens = 32;
+
+// Work item of the split kernel: sequence, [block_begin, block_end) in 64-token
+// blocks, and the partial slot (-1: the item covers its whole sequence and
+// writes out/lse directly).
+struct WorkItem {
+    int32_t seq;
+    int32_t block_begin;
+    int32_t block_end;
+    int32_t slot;
+};
+
+// Reduction task: merge partial slots [src, src + count) of one sequence into
+// slot dst of the next level, or into out/lse when dst < 0.
+struct ReduceTask {
+    int32_t seq;
+    int32_t src;
+    int32_t count;
+    int32_t dst;
+};
+
+struct SplitParams {
+    const uint16_t* q;
+    int64_t q_stride_tok;
+    int64_t q_stride_head;
+    const uint8_t* k_base;   // byte strides below
+    int64_t k_pages, k_sp, k_sh, k_st;
+    const uint8_t* v_base;
+    int64_t v_pages, v_sp, v_sh, v_st;
+    const int32_t* page_table;
+    int64_t pt_stride;
+    const int32_t* seq_lens;
+    const int32_t* capacity;   // planned capacity per sequence (workspace copy)
+    const WorkItem* items;
+    float* part_o;             // [slot][Hk][rows][D]
+    float2* part_ml;           // [slot][Hk][rows]  (m in log2 units, l)
+    float* out;                // [B*Q*Hq][D]
+    float* lse;                // [B*Q*Hq] or null
+    unsigned* err;
+    int q_len, hq, hk, group, rows, page_shift, causal;
+    float scale_log2;          // scale * log2(e): logits are kept in log2 units
+};
+
+struct ReduceParams {
+    const ReduceTask* tasks;
+    const float* src_o;        // [slot][Hk][rows][D]
+    const float2* src_ml;      // (m in log2 units, l) per source row
+    const float* src_lse;      // natural-log lse per source row when normalized_input
+    float* dst_o;
+    float2* dst_ml;
+    float* out;                // final: [B*Q*Hq][D]
+    float* lse;                // final: [B*Q*Hq] or null
+    int hk, rows, group, q_len, hq, head_dim;
+    int normalized_input;      // 1: sources are normalised (o, lse) states (merge_states)
+    int src_rows_stride;       // rows per (slot, kv head) in the source arrays
+};
+
+// Launch the split kernel for head_dim D (defined in split_d<D>.cu); rc is the
+// compile-time query-row group.  With launch == false only the kernel's
+// shared-memory attribute is set (done at upload, outside any capture).
+cudaError_t launch_split_d64(const SplitParams& p, int rc, bool bf16, dim3 grid, cudaStream_t s, bool launch);
+cudaError_t launch_split_d128(const SplitParams& p, int rc, bool bf16, dim3 grid, cudaStream_t s, bool launch);
+cudaError_t launch_split_d192(const SplitParams& p, int rc, bool bf16, dim3 grid, cudaStream_t s, bool launch);
+cudaError_t launch_split_d256(const SplitParams& p, int rc, bool bf16, dim3 grid, cudaStream_t s, bool launch);
+cudaError_t launch_split_d512(const SplitParams& p, int rc, bool bf16, dim3 grid, cudaStream_t s, bool launch);
+
+// Shared-memory bytes and threads of the split kernel for (D, RC); 0 if not built.
+size_t split_smem_bytes(int head_dim, int rc);
+int split_threads(int head_dim);
+int split_max_rc(int head_dim);
+
+cudaError_t launch_reduce(const ReduceParams& p, int num_tasks, cudaStream_t s);
+// One task given by value (p.tasks must be null): used by fdec_merge_states.
+cudaError_t launch_reduce_single(const ReduceParams& p, ReduceTask task, cudaStream_t s);
+
+}  // namespace fdec

@@ -1,0 +1,11 @@
+// split_d192.cu -- split-kernel instantiations for head_dim 192.
+#include "split_kernel.cuh"
+
+namespace fdec {
+
+cudaError_t launch_split_d192(const SplitParams& p, int rc, bool bf16, dim3 grid, cudaStream_t s,
+                              bool launch) {
+    return launch_split_d<192>(p, rc, bf16, grid, s, launch);
+}
+
+}  // namespace fdec

@@ -1,0 +1,11 @@
+// split_d512.cu -- split-kernel instantiations for head_dim 512.
+#include "split_kernel.cuh"
+
+namespace fdec {
+
+cudaError_t launch_split_d512(const SplitParams& p, int rc, bool bf16, dim3 grid, cudaStream_t s,
+                              bool launch) {
+    return launch_split_d<512>(p, rc, bf16, grid, s, launch);
+}
+
+}  // namespace fdec

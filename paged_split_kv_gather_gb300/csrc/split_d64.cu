@@ -1,0 +1,11 @@
+// split_d64.cu -- split-kernel instantiations for head_dim 64.
+#include "split_kernel.cuh"
+
+namespace fdec {
+
+cudaError_t launch_split_d64(const SplitParams& p, int rc, bool bf16, dim3 grid, cudaStream_t s,
+                              bool launch) {
+    return launch_split_d<64>(p, rc, bf16, grid, s, launch);
+}
+
+}  // namespace fdec

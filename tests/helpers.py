@@ -63,3 +63,37 @@ def lse_abs_err(got, ref) -> float:
     both_inf = np.isneginf(got) & np.isneginf(ref)
     d = np.where(both_inf, 0.0, np.abs(got - ref))
     return float(np.max(d)) if d.size else 0.0
+
+
+# ---------------------------------------------------------------------------
+# running the CUDA library on a workload (GPU tests only)
+# ---------------------------------------------------------------------------
+
+OUT_TOL = 2e-3   # max over rows of ||out - ref||_inf / ||ref||_inf
+LSE_TOL = 1e-4   # max |lse - ref|
+
+
+def gpu_run(w: Workload, capacities=None, seq_lens=None, stream=None, **plan_opts):
+    """Plan, upload and run the library on a CUDA workload; returns (out, lse, PagedDecode)."""
+    import paged_split_kv_gather_gb300 as fd
+
+    dev = w.q.device
+    caps = w.seq_lens if capacities is None else capacities
+    pd = fd.PagedDecode(caps, w.q_len, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
+                        w.causal, device=dev, stream=stream, **plan_opts)
+    out = torch.full((w.batch, w.q_len, w.num_qo_heads, w.head_dim), float("nan"), device=dev)
+    lse = torch.full((w.batch, w.q_len, w.num_qo_heads), float("nan"), device=dev)
+    table = torch.as_tensor(w.page_table, device=dev)
+    lens = torch.as_tensor(w.seq_lens if seq_lens is None else seq_lens, dtype=torch.int32, device=dev)
+    pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale, stream=stream)
+    return out, lse, pd
+
+
+def assert_parity(out, lse, ref_out, ref_lse, what=""):
+    o = out.detach().cpu().double().numpy() if hasattr(out, "detach") else np.asarray(out)
+    l = lse.detach().cpu().double().numpy() if hasattr(lse, "detach") else np.asarray(lse)
+    e_out = row_rel_err(o, ref_out)
+    e_lse = lse_abs_err(l, ref_lse)
+    assert np.isfinite(o).all(), f"{what}: non-finite output"
+    assert e_out <= OUT_TOL and e_lse <= LSE_TOL, f"{what}: out rel {e_out:.3g}, lse abs {e_lse:.3g}"
+    return e_out, e_lse

@@ -1,0 +1,197 @@
+"""Host-side tests of the C ABI (no GPU): symbols, planning, argument checks."""
+import ctypes
+import json
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import paged_split_kv_gather_gb300 as fd
+from paged_split_kv_gather_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fdec.h")
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    if not os.path.exists(fd.library_path()):
+        _build.build()
+    return fd.library_path()
+
+
+def declared_entry_points():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fdec_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declarations_match_binding_list():
+    assert declared_entry_points() == sorted(fd.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(fd.library_path())
+    for name in declared_entry_points():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", fd.library_path()], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (fdec_\w+)", out))
+    assert set(declared_entry_points()) <= exported
+
+
+def test_version_and_empty_error():
+    assert "sm_103a" in fd.fdec_version()
+
+
+def _plan(lens, **kw):
+    args = dict(q_len=1, page_size=16, num_qo_heads=32, num_kv_heads=8, head_dim=128, dtype="bf16")
+    args.update(kw)
+    args.setdefault("num_sms", 152)
+    return fd.fdec_plan(lens, **args)
+
+
+def test_capacity_rounds_up_to_64_token_blocks_golden():
+    g = json.load(open(os.path.join(GOLDEN, "capacity_blocks.json")))
+    for length, blocks in g["rows"]:
+        p = _plan([length], blocks_per_split=1)
+        assert int(fd.fdec_plan_get_splits(p)[0]) == blocks, (length, blocks)
+        assert fd.fdec_plan_get_info(p)["max_splits"] == blocks
+
+
+def test_split_path_is_planned_at_every_length_across_the_2048_boundary():
+    # the pages' cliff: past 32 blocks the old matcher fell back to a serial kernel
+    for length in (1900, 2000, 2048, 2049, 2100, 3000, 4800, 4864, 8192, 32768, 131072, 262144):
+        p = _plan([length], num_qo_heads=32, num_kv_heads=4, page_size=64)
+        info = fd.fdec_plan_get_info(p)
+        assert info["path"] == fd.FDEC_PATH_SIMT
+        units = -(-length // 64) * 4
+        assert info["num_split_ctas"] >= min(units, 152) // 2, (length, info)  # the grid fills the SMs
+        if info["max_splits"] > 1:
+            assert info["reduce_passes"] >= 1
+
+
+def test_forced_one_block_per_split_uses_two_reduction_passes():
+    p = _plan([262144], num_qo_heads=32, num_kv_heads=4, page_size=64, blocks_per_split=1)
+    info = fd.fdec_plan_get_info(p)
+    assert info["max_splits"] == 4096
+    assert info["reduce_passes"] == 2          # 4096 -> 64 -> 1 with fan-in 64
+    assert info["launches"] == 3
+    p = _plan([262144], num_qo_heads=32, num_kv_heads=4, page_size=64, blocks_per_split=1, reducer_fanin=4)
+    assert fd.fdec_plan_get_info(p)["reduce_passes"] == 6   # 4096 = 4^6
+
+
+def test_single_split_needs_no_reduction():
+    p = _plan([300], num_qo_heads=4, num_kv_heads=1, head_dim=64, blocks_per_split=8)
+    info = fd.fdec_plan_get_info(p)
+    assert info["max_splits"] == 1 and info["reduce_passes"] == 0 and info["launches"] == 1
+
+
+def test_auto_plan_balances_ragged_batches():
+    lens = np.round(np.exp(np.random.default_rng(0).uniform(np.log(16), np.log(32768), 64))).astype(np.int32)
+    p = _plan(lens, num_qo_heads=16, num_kv_heads=8, head_dim=256, dtype="f16")
+    info = fd.fdec_plan_get_info(p)
+    splits = fd.fdec_plan_get_splits(p)
+    C = info["blocks_per_split"]
+    nb = np.maximum(1, -(-lens // 64))
+    assert np.array_equal(splits, -(-nb // C))
+    assert info["num_items"] == int(splits.sum())
+
+
+def test_row_groups_cover_all_query_rows():
+    p = _plan([8200] * 4, q_len=8, num_qo_heads=32, num_kv_heads=8, causal=True)
+    info = fd.fdec_plan_get_info(p)
+    assert info["rows_per_group"] * info["row_groups"] >= 32
+    p = _plan([1000], num_qo_heads=16, num_kv_heads=8, head_dim=512, q_len=3)
+    info = fd.fdec_plan_get_info(p)
+    assert info["rows_per_group"] <= 4 and info["rows_per_group"] * info["row_groups"] >= 6
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=100), "FDEC_ERR_UNSUPPORTED"),
+    (dict(page_size=3), "FDEC_ERR_UNSUPPORTED"),
+    (dict(page_size=512), "FDEC_ERR_UNSUPPORTED"),
+    (dict(num_qo_heads=30, num_kv_heads=8), "FDEC_ERR_INVALID_ARG"),
+    (dict(q_len=0), "FDEC_ERR_INVALID_ARG"),
+    (dict(reducer_fanin=1), "FDEC_ERR_INVALID_ARG"),
+    (dict(path=7), "FDEC_ERR_INVALID_ARG"),
+])
+def test_plan_rejects_bad_arguments(kw, status):
+    with pytest.raises(fd.FdecError) as ei:
+        _plan([100], **kw)
+    assert ei.value.status_name == status
+
+
+def test_plan_rejects_negative_capacity():
+    with pytest.raises(fd.FdecError) as ei:
+        _plan([10, -1])
+    assert ei.value.status_name == "FDEC_ERR_INVALID_ARG"
+
+
+def test_plan_without_device_or_sm_count_reports_cuda_error():
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    with pytest.raises(fd.FdecError) as ei:
+        fd.fdec_plan([100], 1, 16, 4, 1, 64, "f16", num_sms=0)
+    assert ei.value.status_name == "FDEC_ERR_CUDA"
+
+
+class _FakeTensor:
+    """Just enough of a tensor for argument marshalling (never dereferenced on the host)."""
+
+    def __init__(self, ptr, shape, strides):
+        self._ptr, self.shape, self._strides = ptr, shape, strides
+
+    def data_ptr(self):
+        return self._ptr
+
+    def stride(self, i=None):
+        return self._strides if i is None else self._strides[i]
+
+    def dim(self):
+        return len(self.shape)
+
+    def is_contiguous(self):
+        return True
+
+
+def _run_raw(plan, k, v, q=0x10000, out=0x20000, ws=0x30000, lse=None, pt_stride=None):
+    lib = fd._load()
+    st = lib.fdec_run(plan.handle, q, 128, 128 * 8, k, v, 0x40000, pt_stride or 256, 0x50000,
+                      ctypes.c_float(0.1), out, lse, ws, None)
+    return fd.STATUS_NAMES[st], fd.fdec_last_error()
+
+
+def test_run_layout_checks_happen_before_any_launch():
+    plan = _plan([2048], num_qo_heads=8, num_kv_heads=1, head_dim=128)
+    good = fd.KVDesc(0x100000, 10, 16 * 128, 0, 128)
+    assert _run_raw(plan, fd.KVDesc(0x100008, 10, 16 * 128, 0, 128), good)[0] == "FDEC_ERR_LAYOUT"
+    assert _run_raw(plan, good, fd.KVDesc(0x100000, 10, 16 * 128 + 4, 0, 128))[0] == "FDEC_ERR_LAYOUT"
+    assert _run_raw(plan, good, fd.KVDesc(0x100000, 10, 16 * 128, 0, 130))[0] == "FDEC_ERR_LAYOUT"
+    assert _run_raw(plan, good, fd.KVDesc(0, 10, 16 * 128, 0, 128))[0] == "FDEC_ERR_INVALID_ARG"
+    assert _run_raw(plan, good, fd.KVDesc(0x100000, 0, 16 * 128, 0, 128))[0] == "FDEC_ERR_INVALID_ARG"
+    assert _run_raw(plan, good, good, pt_stride=100)[0] == "FDEC_ERR_CAPACITY"   # needs 128 pages
+    assert _run_raw(plan, good, good, out=0x20002)[0] == "FDEC_ERR_LAYOUT"
+    # everything valid but never uploaded: the workspace check
+    assert _run_raw(plan, good, good)[0] == "FDEC_ERR_WORKSPACE"
+
+
+def test_merge_states_rejects_bad_sizes():
+    lib = fd._load()
+    assert fd.STATUS_NAMES[lib.fdec_merge_states(0x1000, 0x2000, 0, 4, 64, 0x3000, None, None)] == \
+        "FDEC_ERR_INVALID_ARG"
+    assert fd.STATUS_NAMES[lib.fdec_merge_states(0x1000, 0x2000, 2, 4, 513, 0x3000, None, None)] == \
+        "FDEC_ERR_INVALID_ARG"
+    assert fd.STATUS_NAMES[lib.fdec_merge_states(None, 0x2000, 2, 4, 64, 0x3000, None, None)] == \
+        "FDEC_ERR_INVALID_ARG"
+
+
+def test_upload_refuses_null_and_misaligned_workspace():
+    plan = _plan([100])
+    lib = fd._load()
+    assert fd.STATUS_NAMES[lib.fdec_plan_upload(plan.handle, None, None)] == "FDEC_ERR_INVALID_ARG"
+    assert fd.STATUS_NAMES[lib.fdec_plan_upload(plan.handle, 0x1008, None)] == "FDEC_ERR_WORKSPACE"

@@ -1,0 +1,298 @@
+"""CUDA path vs the float64 oracle, element by element, on seeded inputs.
+
+Tolerance (fp32 accumulation over 16-bit K/V): per output row,
+||out - ref||_inf / ||ref||_inf <= 2e-3, and |lse - ref| <= 1e-4.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_split_kv_gather_gb300 as fd
+from paged_split_kv_gather_gb300 import workloads as W
+from tests.helpers import assert_parity, gpu_run, oracle_run
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(w_gpu, rows=None, **plan_opts):
+    out, lse, pd = gpu_run(w_gpu, **plan_opts)
+    torch.cuda.synchronize()
+    assert pd.device_errors() == 0
+    w_cpu = w_gpu.to("cpu")
+    if rows is None:
+        ref_o, ref_l = oracle_run(w_cpu)
+        got_o, got_l = out.cpu(), lse.cpu()
+    else:
+        ref_o, ref_l = oracle_run(w_cpu, rows=rows)
+        flat_o = out.reshape(-1, w_gpu.head_dim).cpu()
+        flat_l = lse.reshape(-1).cpu()
+        idx = torch.as_tensor(np.asarray(rows, dtype=np.int64))
+        got_o, got_l = flat_o[idx], flat_l[idx]
+    return assert_parity(got_o, got_l, ref_o, ref_l, w_gpu.name), pd
+
+
+# ------------------------------------------------------------------ the five workloads
+
+def test_tiny_decode():
+    _check(W.tiny(device="cuda"))
+
+
+@pytest.mark.parametrize("peaked", [False, True])
+def test_batched_gqa_decode(peaked):
+    _check(W.batched_gqa(device="cuda", peaked=peaked))
+
+
+@pytest.mark.parametrize("length", W.LONG_CONTEXT_LENGTHS)
+def test_long_context_sweep(length):
+    _check(W.long_context(length, device="cuda"))
+
+
+@pytest.mark.parametrize("length", [2048, 2049, 4864, 32768])
+def test_long_context_peaked(length):
+    _check(W.long_context(length, device="cuda", peaked=True))
+
+
+def _ragged_rows(w, per_seq=2):
+    rows = []
+    for b in range(w.batch):
+        for j in range(per_seq):
+            h = (b * 7 + j * 5) % w.num_qo_heads
+            rows.append(b * w.num_qo_heads + h)
+    return rows
+
+
+@pytest.mark.parametrize("head_dim", W.RAGGED_HEAD_DIMS)
+@pytest.mark.parametrize("layout", ["interleaved", "split2"])
+def test_ragged_serving_batch_full_size_sampled(head_dim, layout):
+    w = W.ragged(head_dim, device="cuda", layout=layout)
+    before = [t.clone() for t in w.keep[1:]]
+    _check(w, rows=_ragged_rows(w))
+    for a, b in zip(before, w.keep[1:]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), "the KV cache changed"
+
+
+@pytest.mark.parametrize("q_len", [4, 8])
+def test_multi_token_spec_decode(q_len):
+    _check(W.multi_token(q_len, device="cuda"))
+
+
+def test_multi_token_prefill_chunk_sampled_rows():
+    w = W.multi_token(2048, device="cuda")
+    rows = []
+    for b in range(w.batch):
+        for i in [0, 1, 63, 64, 1000, 2046, 2047]:
+            for h in (0, 5, 31):
+                rows.append((b * w.q_len + i) * w.num_qo_heads + h)
+    _check(w, rows=rows)
+
+
+# ------------------------------------------------------------------ plans and reductions
+
+@pytest.mark.parametrize("bps,fanin", [(1, 0), (1, 4), (3, 2), (7, 0), (10**6, 0)])
+def test_any_split_plan_matches_the_oracle(bps, fanin):
+    w = W.long_context(4800, device="cuda", peaked=True)
+    (e_out, e_lse), pd = _check(w, blocks_per_split=bps, reducer_fanin=fanin)
+    info = pd.info
+    if bps == 1:
+        assert info["max_splits"] == 75
+    if bps >= 10**6:
+        assert info["max_splits"] == 1 and info["reduce_passes"] == 0
+
+
+def test_multipass_reduction_at_262144_with_one_partial_per_block():
+    w = W.long_context(262144, device="cuda")
+    (e_out, e_lse), pd = _check(w, blocks_per_split=1)
+    assert pd.info["max_splits"] == 4096 and pd.info["reduce_passes"] == 2
+
+
+def test_split_plans_agree_with_each_other():
+    w = W.long_context(32768, device="cuda")
+    outs = []
+    for bps in (1, 5, 64, 512):
+        out, lse, _ = gpu_run(w, blocks_per_split=bps)
+        outs.append((out, lse))
+    ref = outs[-1]
+    for out, lse in outs[:-1]:
+        assert torch.max(torch.abs(out - ref[0])) / torch.max(torch.abs(ref[0])) < 1e-3
+        assert torch.max(torch.abs(lse - ref[1])) < 1e-4
+
+
+def test_results_are_deterministic_for_a_fixed_plan():
+    w = W.batched_gqa(device="cuda")
+    a, la, pd = gpu_run(w)
+    b = torch.empty_like(a)
+    lb = torch.empty_like(la)
+    pd.run(w.q, w.k, w.v, torch.as_tensor(w.page_table, device="cuda"),
+           torch.as_tensor(w.seq_lens, device="cuda"), b, lb, scale=w.scale)
+    assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+# ------------------------------------------------------------------ layouts (read-only cache)
+
+LAYOUTS = ["hnd", "nhd", "interleaved", "split2", "mixed", "interleaved_nhd"]
+
+
+def _relayout(w, layout):
+    """Same K/V values, another physical layout."""
+    w2 = W.make(w.batch, w.q_len, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.page_size, w.seq_lens,
+                dtype=w.dtype, layout=layout, causal=w.causal, device=w.q.device, pool_pages=w.k.shape[0],
+                seed=999)
+    w2.page_table = w.page_table.copy()
+    w2.q = w.q
+    w2.k.copy_(w.k)
+    w2.v.copy_(w.v)
+    return w2
+
+
+def test_every_kv_layout_gives_bitwise_identical_results_and_leaves_the_cache_unchanged():
+    base = W.make(3, 1, 16, 4, 128, 16, [700, 33, 2100], dtype="bf16", device="cuda", seed=5, peaked=True)
+    ref_out, ref_lse, _ = gpu_run(base, blocks_per_split=4)
+    for layout in LAYOUTS:
+        w = _relayout(base, layout)
+        snap = [t.clone() for t in w.keep]
+        out, lse, _ = gpu_run(w, blocks_per_split=4)
+        assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse), layout
+        for a, b in zip(snap, w.keep):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"{layout}: cache written"
+    w_cpu = base.to("cpu")
+    ro, rl = oracle_run(w_cpu)
+    assert_parity(ref_out.cpu(), ref_lse.cpu(), ro, rl, "layouts")
+
+
+@pytest.mark.parametrize("q_layout", ["fused_qkv", "head_major"])
+def test_strided_q_matches_packed_q(q_layout):
+    w = W.make(3, 2, 8, 2, 64, 16, [90, 130, 64], dtype="f16", device="cuda", seed=8, causal=True,
+               q_layout=q_layout, peaked=True)
+    out, lse, _ = gpu_run(w)
+    packed = w.q.contiguous()
+    w2 = W.Workload(w.name, w.dtype, w.batch, w.q_len, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.page_size,
+                    w.causal, w.scale, w.seq_lens, w.page_table, packed, w.k, w.v, w.layout, w.keep)
+    out2, lse2, _ = gpu_run(w2)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    ro, rl = oracle_run(w.to("cpu"))
+    assert_parity(out.cpu(), lse.cpu(), ro, rl, q_layout)
+
+
+def test_shorter_v_pool_only_indexed_pages_are_read():
+    w = W.make(2, 1, 8, 2, 128, 16, [200, 90], dtype="bf16", device="cuda", seed=3, pool_pages=40)
+    used = int(w.page_table.max()) + 1
+    w.v = w.v[:used].clone()  # V holds only the pages the table uses
+    out, lse, pd = gpu_run(w)
+    assert pd.device_errors() == 0
+    ro, rl = oracle_run(w.to("cpu"))
+    assert_parity(out.cpu(), lse.cpu(), ro, rl, "short V pool")
+
+
+def test_unread_slots_and_pages_may_hold_nan():
+    w = W.make(4, 1, 16, 4, 128, 16, [33, 1, 500, 64], dtype="bf16", device="cuda", seed=12, pool_pages=80,
+               nan_guard=True)
+    out, lse, _ = gpu_run(w, blocks_per_split=1)
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    ro, rl = oracle_run(w.to("cpu"))
+    assert_parity(out.cpu(), lse.cpu(), ro, rl, "nan guard")
+
+
+# ------------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("head_dim", [64, 128, 192, 256, 512])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_head_dims_and_dtypes(head_dim, dtype):
+    w = W.make(3, 1, 8, 2, head_dim, 16, [1, 95, 321], dtype=dtype, device="cuda", seed=head_dim, peaked=True)
+    _check(w)
+    _check(w, blocks_per_split=1)
+
+
+@pytest.mark.parametrize("page_size", [1, 2, 8, 32, 64, 128, 256])
+def test_page_sizes(page_size):
+    w = W.make(2, 1, 8, 4, 64, page_size, [257, 1000], dtype="f16", device="cuda", seed=page_size)
+    _check(w)
+
+
+@pytest.mark.parametrize("group,q_len", [(1, 1), (3, 1), (5, 2), (16, 1), (8, 3)])
+def test_group_sizes_and_row_groups(group, q_len):
+    w = W.make(2, q_len, 2 * group, 2, 128, 16, [150, 77], dtype="bf16", device="cuda", seed=group,
+               causal=q_len > 1)
+    _check(w)
+
+
+def test_empty_sequences_and_rows_with_nothing_visible():
+    w = W.make(3, 1, 4, 2, 64, 16, [0, 5, 0], dtype="f16", device="cuda", seed=1)
+    out, lse, _ = gpu_run(w)
+    assert torch.all(out[0] == 0) and torch.all(out[2] == 0)
+    assert torch.all(torch.isneginf(lse[0])) and torch.all(torch.isneginf(lse[2]))
+    ro, rl = oracle_run(w.to("cpu"))
+    assert_parity(out.cpu(), lse.cpu(), ro, rl, "empty")
+    w = W.make(1, 6, 2, 1, 64, 16, [3], dtype="f16", device="cuda", seed=2, causal=True)
+    out, lse, _ = gpu_run(w)
+    ro, rl = oracle_run(w.to("cpu"))
+    assert_parity(out.cpu(), lse.cpu(), ro, rl, "causal-empty rows")
+
+
+def test_run_time_lengths_below_capacity():
+    caps = np.array([5000, 3000, 700], dtype=np.int32)
+    w = W.make(3, 1, 16, 4, 128, 16, caps, dtype="bf16", device="cuda", seed=4)
+    for lens in ([4999, 3000, 1], [64, 65, 0], [2048, 2049, 700]):
+        lens = np.array(lens, dtype=np.int32)
+        out, lse, _ = gpu_run(w, capacities=caps, seq_lens=lens, blocks_per_split=3)
+        ro, rl = oracle_run(w.to("cpu"), seq_lens=lens)
+        assert_parity(out.cpu(), lse.cpu(), ro, rl, f"lens {lens}")
+
+
+# ------------------------------------------------------------------ device-side checks
+
+def test_out_of_range_page_id_is_flagged_not_read():
+    w = W.make(1, 1, 4, 1, 64, 16, [100], dtype="f16", device="cuda", seed=1)
+    w.page_table[0, 2] = w.k.shape[0] + 5
+    out, lse, pd = gpu_run(w)
+    torch.cuda.synchronize()
+    assert pd.device_errors() & fd.DEVERR_PAGE_ID
+    assert pd.device_errors() == 0  # cleared by the first read
+
+
+def test_length_above_capacity_is_flagged_and_clamped():
+    w = W.make(1, 1, 4, 1, 64, 16, [100], dtype="f16", device="cuda", seed=1, pool_pages=20)
+    out, lse, pd = gpu_run(w, capacities=[100], seq_lens=[300])
+    torch.cuda.synchronize()
+    assert pd.device_errors() & fd.DEVERR_SEQ_LEN
+    ro, rl = oracle_run(w.to("cpu"))
+    assert_parity(out.cpu(), lse.cpu(), ro, rl, "clamped")
+
+
+# ------------------------------------------------------------------ merge of states
+
+@pytest.mark.parametrize("n", [1, 2, 7, 33, 100])
+def test_merge_states_matches_the_oracle_merge(n):
+    import oracle
+
+    rng = np.random.default_rng(n)
+    rows, d = 37, 128
+    o = rng.standard_normal((n, rows, d)).astype(np.float32)
+    l = (rng.standard_normal((n, rows)) * 4).astype(np.float32)
+    l[0, 3] = -np.inf
+    if n > 1:
+        l[:, 5] = -np.inf   # a row where every state is empty
+    ot, lt = torch.as_tensor(o, device="cuda"), torch.as_tensor(l, device="cuda")
+    oo = torch.empty((rows, d), device="cuda")
+    lo = torch.empty((rows,), device="cuda")
+    fd.fdec_merge_states(ot, lt, oo, lo)
+    ro, rl = oracle.merge_states(o.astype(np.float64), l.astype(np.float64))
+    assert_parity(oo.cpu(), lo.cpu(), ro, rl, f"merge n={n}")
+
+
+def test_two_runs_over_disjoint_ranges_merge_to_the_whole():
+    # cascade: attend to a prefix and a suffix separately, merge the states
+    w = W.make(1, 1, 8, 2, 128, 16, [1000], dtype="bf16", device="cuda", seed=6, peaked=True)
+    full_o, full_l, _ = gpu_run(w)
+    cut_pages = 640 // 16
+    pre = W.Workload(w.name, w.dtype, 1, 1, 8, 2, 128, 16, False, w.scale, np.array([640], np.int32),
+                     w.page_table[:, :cut_pages].copy(), w.q, w.k, w.v)
+    suf = W.Workload(w.name, w.dtype, 1, 1, 8, 2, 128, 16, False, w.scale, np.array([360], np.int32),
+                     w.page_table[:, cut_pages:].copy(), w.q, w.k, w.v)
+    o1, l1, _ = gpu_run(pre)
+    o2, l2, _ = gpu_run(suf)
+    oo = torch.empty((8, 128), device="cuda")
+    lo = torch.empty((8,), device="cuda")
+    fd.fdec_merge_states(torch.stack([o1.reshape(8, 128), o2.reshape(8, 128)]).contiguous(),
+                         torch.stack([l1.reshape(8), l2.reshape(8)]).contiguous(), oo, lo)
+    assert torch.max(torch.abs(oo - full_o.reshape(8, 128))) / torch.max(torch.abs(full_o)) < 1e-4
+    assert torch.max(torch.abs(lo - full_l.reshape(8))) < 1e-5
