@@ -61,7 +61,8 @@ def lse_abs_err(got, ref) -> float:
     got = np.asarray(got, dtype=np.float64).reshape(-1)
     ref = np.asarray(ref, dtype=np.float64).reshape(-1)
     both_inf = np.isneginf(got) & np.isneginf(ref)
-    d = np.where(both_inf, 0.0, np.abs(got - ref))
+    with np.errstate(invalid="ignore"):
+        d = np.where(both_inf, 0.0, np.abs(got - ref))
     return float(np.max(d)) if d.size else 0.0
 
 
