@@ -228,7 +228,7 @@ def _run_fdec(args):
     # ---- the long-context sweep: per-call time with an L2 flush before each call
     sweep = []
     if not args.no_sweep:
-        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
         for length in W.LONG_CONTEXT_LENGTHS:
             ws = w if length == HEADLINE_LENGTH else _make_inputs(length, dev)
             pds = pd if length == HEADLINE_LENGTH else fd.PagedDecode(
@@ -239,7 +239,7 @@ def _run_fdec(args):
                 pds.run(ws.q, ws.k, ws.v, tb, ln, out, lse, scale=ws.scale)
             times = []
             for _ in range(args.sweep_calls):
-                flush.zero_()
+                torch.sum(flush)  # read 256 MB: the L2 is left full of clean, unrelated lines
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record()
@@ -279,7 +279,8 @@ def _run_fdec(args):
             "config": {"workload": "long_context_decode_L262144", "batch": 1, "q_len": 1, "num_qo_heads": 32,
                        "num_kv_heads": 4, "head_dim": 128, "page_size": 64, "kv_len": HEADLINE_LENGTH,
                        "kv_bytes_per_call": kv_bytes, "out": "fp32 out + lse",
-                       "l2": "inputs larger than L2 (537 MB of K/V per step vs 129 MB L2); sweep points flush L2",
+                       "l2": "inputs larger than L2 (537 MB of K/V per step vs 129 MB L2); each sweep call follows a "
+                             "256 MB read that evicts the L2 (clean lines)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "plan": {k: info[k] for k in ("blocks_per_split", "num_split_ctas", "max_splits",
                                                       "reduce_passes", "launches")}},

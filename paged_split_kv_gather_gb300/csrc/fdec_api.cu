@@ -17,6 +17,10 @@
 #include <string>
 #include <vector>
 
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "../../include/fdec.h"
 #include "fdec_internal.h"
 #include "split_kernel.cuh"
@@ -131,6 +135,12 @@ struct fdec_plan_s {
     std::vector<uint8_t> meta;  // host image of [0, meta_bytes)
     void* uploaded = nullptr;
     cudaEvent_t split_event = nullptr;
+    // Tensor maps of the last K/V descriptors seen by fdec_run (re-encoded on change).
+    bool maps_valid = false;
+    fdec_kv_desc map_k{}, map_v{};
+    CUtensorMap tmap_k{};
+    CUtensorMap tmap_v{};
+    int k_pos[3] = {1, 2, 3}, v_pos[3] = {1, 2, 3};
 };
 
 namespace {
@@ -199,14 +209,69 @@ int choose_blocks_per_split(const std::vector<int>& nblocks, int copies, int slo
 
 cudaError_t dispatch_split(const fdec_plan_s* p, const SplitParams& sp, dim3 grid, cudaStream_t stream, bool launch) {
     const bool bf16 = p->dtype == FDEC_BF16;
+    const CUtensorMap& tk = p->tmap_k;
+    const CUtensorMap& tv = p->tmap_v;
     switch (p->head_dim) {
-        case 64: return launch_split_d64(sp, p->rc, bf16, grid, stream, launch);
-        case 128: return launch_split_d128(sp, p->rc, bf16, grid, stream, launch);
-        case 192: return launch_split_d192(sp, p->rc, bf16, grid, stream, launch);
-        case 256: return launch_split_d256(sp, p->rc, bf16, grid, stream, launch);
-        case 512: return launch_split_d512(sp, p->rc, bf16, grid, stream, launch);
+        case 64: return launch_split_d64(sp, tk, tv, p->rc, bf16, grid, stream, launch);
+        case 128: return launch_split_d128(sp, tk, tv, p->rc, bf16, grid, stream, launch);
+        case 192: return launch_split_d192(sp, tk, tv, p->rc, bf16, grid, stream, launch);
+        case 256: return launch_split_d256(sp, tk, tv, p->rc, bf16, grid, stream, launch);
+        case 512: return launch_split_d512(sp, tk, tv, p->rc, bf16, grid, stream, launch);
         default: return cudaErrorInvalidValue;
     }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// A 4-D tensor map over one K or V pool: dims (head_dim, and the slot, head and
+// page dims ordered by increasing stride), box = 64 dims x box_rows slots, 128-byte
+// swizzle.  pos[role] receives the coordinate position of slot (0), head (1), page (2).
+fdec_status encode_kv_map(CUtensorMap* map, const fdec_kv_desc& d, int head_dim, int page_size, int hk,
+                          int box_rows, int pos[3]) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) return fail(FDEC_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    struct Dim {
+        uint64_t size, stride;
+        int role;
+    } dims[3] = {{static_cast<uint64_t>(page_size), static_cast<uint64_t>(d.stride_token) * 2, 0},
+                 {static_cast<uint64_t>(hk), static_cast<uint64_t>(d.stride_head) * 2, 1},
+                 {static_cast<uint64_t>(d.num_pages), static_cast<uint64_t>(d.stride_page) * 2, 2}};
+    for (Dim& x : dims)
+        if (x.size == 1 && x.stride == 0) x.stride = 16;  // any stride works for a single index
+    std::stable_sort(dims, dims + 3, [](const Dim& a, const Dim& b) { return a.stride < b.stride; });
+    cuuint64_t gdim[4] = {static_cast<cuuint64_t>(head_dim), dims[0].size, dims[1].size, dims[2].size};
+    cuuint64_t gstride[3] = {dims[0].stride, dims[1].stride, dims[2].stride};
+    cuuint32_t box[4] = {64, 1, 1, 1};
+    cuuint32_t estride[4] = {1, 1, 1, 1};
+    for (int i = 0; i < 3; ++i) {
+        pos[dims[i].role] = i + 1;
+        if (dims[i].role == 0) box[i + 1] = static_cast<cuuint32_t>(box_rows);
+    }
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(d.base), gdim, gstride, box, estride,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FDEC_ERR_LAYOUT, "cuTensorMapEncodeTiled rejected the K/V layout (error " + std::to_string(r) + ")");
+    return FDEC_OK;
+}
+
+bool same_desc(const fdec_kv_desc& a, const fdec_kv_desc& b) {
+    return a.base == b.base && a.num_pages == b.num_pages && a.stride_page == b.stride_page &&
+           a.stride_head == b.stride_head && a.stride_token == b.stride_token;
 }
 
 void log_plan(const fdec_plan_s* p) {
@@ -500,6 +565,18 @@ fdec_status fdec_run(fdec_plan_t p, const void* q, int64_t q_stride_tok, int64_t
     if (workspace == nullptr || workspace != p->uploaded)
         return fail(FDEC_ERR_WORKSPACE, "workspace is not the buffer this plan was uploaded to");
 
+    if (p->page_size >= 8 && !(p->maps_valid && same_desc(p->map_k, k) && same_desc(p->map_v, v))) {
+        const int box_rows = std::min(p->page_size, kStageTokens);
+        fdec_status st = encode_kv_map(&p->tmap_k, k, p->head_dim, p->page_size, p->hk, box_rows, p->k_pos);
+        if (st == FDEC_OK) st = encode_kv_map(&p->tmap_v, v, p->head_dim, p->page_size, p->hk, box_rows, p->v_pos);
+        if (st != FDEC_OK) {
+            p->maps_valid = false;
+            return st;
+        }
+        p->map_k = k;
+        p->map_v = v;
+        p->maps_valid = true;
+    }
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     SplitParams sp;
     sp.q = static_cast<const uint16_t*>(q);
@@ -533,6 +610,12 @@ fdec_status fdec_run(fdec_plan_t p, const void* q, int64_t q_stride_tok, int64_t
     sp.page_shift = p->page_shift;
     sp.causal = p->causal;
     sp.scale_log2 = scale * 1.4426950408889634074f;
+    sp.k_pos_slot = p->k_pos[0];
+    sp.k_pos_head = p->k_pos[1];
+    sp.k_pos_page = p->k_pos[2];
+    sp.v_pos_slot = p->v_pos[0];
+    sp.v_pos_head = p->v_pos[1];
+    sp.v_pos_page = p->v_pos[2];
 
     const dim3 grid(static_cast<unsigned>(p->items.size()), static_cast<unsigned>(p->hk),
                     static_cast<unsigned>(p->row_groups));

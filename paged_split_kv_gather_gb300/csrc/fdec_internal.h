@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace fdec {
@@ -54,6 +55,9 @@ struct SplitParams {
     unsigned* err;
     int q_len, hq, hk, group, rows, page_shift, causal;
     float scale_log2;          // scale * log2(e): logits are kept in log2 units
+    // Coordinate position (1..3) of the slot, head and page dims in each tensor map.
+    int k_pos_slot, k_pos_head, k_pos_page;
+    int v_pos_slot, v_pos_head, v_pos_page;
 };
 
 struct ReduceParams {
@@ -73,11 +77,16 @@ struct ReduceParams {
 // Launch the split kernel for head_dim D (defined in split_d<D>.cu); rc is the
 // compile-time query-row group.  With launch == false only the kernel's
 // shared-memory attribute is set (done at upload, outside any capture).
-cudaError_t launch_split_d64(const SplitParams& p, int rc, bool bf16, dim3 grid, cudaStream_t s, bool launch);
-cudaError_t launch_split_d128(const SplitParams& p, int rc, bool bf16, dim3 grid, cudaStream_t s, bool launch);
-cudaError_t launch_split_d192(const SplitParams& p, int rc, bool bf16, dim3 grid, cudaStream_t s, bool launch);
-cudaError_t launch_split_d256(const SplitParams& p, int rc, bool bf16, dim3 grid, cudaStream_t s, bool launch);
-cudaError_t launch_split_d512(const SplitParams& p, int rc, bool bf16, dim3 grid, cudaStream_t s, bool launch);
+cudaError_t launch_split_d64(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int rc,
+                               bool bf16, dim3 grid, cudaStream_t s, bool launch);
+cudaError_t launch_split_d128(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int rc,
+                               bool bf16, dim3 grid, cudaStream_t s, bool launch);
+cudaError_t launch_split_d192(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int rc,
+                               bool bf16, dim3 grid, cudaStream_t s, bool launch);
+cudaError_t launch_split_d256(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int rc,
+                               bool bf16, dim3 grid, cudaStream_t s, bool launch);
+cudaError_t launch_split_d512(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int rc,
+                               bool bf16, dim3 grid, cudaStream_t s, bool launch);
 
 // Shared-memory bytes and threads of the split kernel for (D, RC); 0 if not built.
 size_t split_smem_bytes(int head_dim, int rc);

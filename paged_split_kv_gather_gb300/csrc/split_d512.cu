@@ -3,9 +3,9 @@
 
 namespace fdec {
 
-cudaError_t launch_split_d512(const SplitParams& p, int rc, bool bf16, dim3 grid, cudaStream_t s,
-                              bool launch) {
-    return launch_split_d<512>(p, rc, bf16, grid, s, launch);
+cudaError_t launch_split_d512(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int rc,
+                               bool bf16, dim3 grid, cudaStream_t s, bool launch) {
+    return launch_split_d<512>(p, tk, tv, rc, bf16, grid, s, launch);
 }
 
 }  // namespace fdec
