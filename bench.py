@@ -284,7 +284,8 @@ def _run_fdec(args):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "plan": {k: info[k] for k in ("blocks_per_split", "num_split_ctas", "max_splits",
                                                       "reduce_passes", "launches")}},
-            "roofline": {"bound": "hbm", "kernel": f"split_kernel<128,{info['rows_per_group']},bf16>", "achieved": round(achieved, 1),
+            "roofline": {"bound": "hbm", "kernel": ("split_mma_kernel<128,bf16>" if info["path"] == fd.FDEC_PATH_MMA
+                                                    else f"split_kernel<128,{info['rows_per_group']},bf16>"), "achieved": round(achieved, 1),
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes,
                          "split_kernel_us": round(split_ms * 1e3, 2)},

@@ -90,13 +90,14 @@ enum { FDEC_PATH_AUTO = 0, FDEC_PATH_SIMT = 1, FDEC_PATH_MMA = 2 };
 typedef struct {
     int blocks_per_split;  /* 64-token blocks per split; 0 = auto; 1 = one partial per block */
     int reducer_fanin;     /* partials merged per reduction task; 0 = auto (64); >= 2 */
-    int path;              /* FDEC_PATH_AUTO / _SIMT / _MMA */
+    int path;              /* FDEC_PATH_AUTO (tensor cores where built, else SIMT), _SIMT (fp32 FMA),
+                              _MMA (tensor cores; head_dim 64, 128, 192) */
     int num_sms;           /* 0 = query the current device; > 0 plans without a device */
 } fdec_plan_opts;
 
 /* What a plan decided (for logging, tests and benchmarks). */
 typedef struct {
-    int path;              /* FDEC_PATH_SIMT or FDEC_PATH_MMA */
+    int path;              /* FDEC_PATH_SIMT (fp32 FMA kernel) or FDEC_PATH_MMA (tensor-core kernel) */
     int blocks_per_split;
     int num_items;         /* split work items (each runs for every KV head and row group) */
     int num_split_ctas;    /* CTAs of the split launch */

@@ -53,15 +53,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the
+// phase completes or about `ns` nanoseconds pass, instead of spinning on issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return done != 0;
+}
+
 // Wait for the phase with the given parity to complete; false after kWaitLimitNs.
-// (try_wait itself suspends the thread for a while, so the clock is read only
-// every 32 attempts.)
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 31u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    while (true) {
+        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
 }
 
@@ -138,6 +150,44 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// 32-bit shared-window loads with a compile-time byte offset folded into the instruction.
+template <int OFF>
+__device__ __forceinline__ uint4 lds128(uint32_t base) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4+%5];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(base), "n"(OFF));
+    return v;
+}
+
+template <int OFF>
+__device__ __forceinline__ float4 lds128f(uint32_t base) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4+%5];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(base), "n"(OFF));
+    return v;
+}
+
+template <int OFF>
+__device__ __forceinline__ float2 lds64f(uint32_t base) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2+%3];" : "=f"(v.x), "=f"(v.y) : "r"(base), "n"(OFF));
+    return v;
+}
+
+template <int OFF>
+__device__ __forceinline__ uint32_t lds32(uint32_t base) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1+%2];" : "=r"(v) : "r"(base), "n"(OFF));
+    return v;
+}
+
+// Order this thread's generic-proxy shared-memory writes before later async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Named barrier over the first `threads` threads of the CTA (id 1..15).

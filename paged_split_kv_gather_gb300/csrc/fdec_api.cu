@@ -91,11 +91,11 @@ size_t split_smem_bytes(int d, int rc) {
 
 int split_threads(int d) {
     switch (d) {
-        case 64: return (SplitShape<64>::NW + 1) * 32;
-        case 128: return (SplitShape<128>::NW + 1) * 32;
-        case 192: return (SplitShape<192>::NW + 1) * 32;
-        case 256: return (SplitShape<256>::NW + 1) * 32;
-        case 512: return (SplitShape<512>::NW + 1) * 32;
+        case 64: return SplitLayout<64, SplitShape<64>::RCMAX>::THREADS;
+        case 128: return SplitLayout<128, SplitShape<128>::RCMAX>::THREADS;
+        case 192: return SplitLayout<192, SplitShape<192>::RCMAX>::THREADS;
+        case 256: return SplitLayout<256, SplitShape<256>::RCMAX>::THREADS;
+        case 512: return SplitLayout<512, SplitShape<512>::RCMAX>::THREADS;
         default: return 0;
     }
 }
@@ -211,6 +211,7 @@ cudaError_t dispatch_split(const fdec_plan_s* p, const SplitParams& sp, dim3 gri
     const bool bf16 = p->dtype == FDEC_BF16;
     const CUtensorMap& tk = p->tmap_k;
     const CUtensorMap& tv = p->tmap_v;
+    if (p->path == FDEC_PATH_MMA) return launch_split_mma(sp, tk, tv, p->head_dim, bf16, grid, stream, launch);
     switch (p->head_dim) {
         case 64: return launch_split_d64(sp, tk, tv, p->rc, bf16, grid, stream, launch);
         case 128: return launch_split_d128(sp, tk, tv, p->rc, bf16, grid, stream, launch);
@@ -319,7 +320,9 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
         return fail(FDEC_ERR_INVALID_ARG, "invalid plan options");
     if (o.path != FDEC_PATH_AUTO && o.path != FDEC_PATH_SIMT && o.path != FDEC_PATH_MMA)
         return fail(FDEC_ERR_INVALID_ARG, "invalid path option");
-    if (o.path == FDEC_PATH_MMA) return fail(FDEC_ERR_UNSUPPORTED, "the tensor-core path is not built in this version");
+    const bool mma_ok = head_dim == 64 || head_dim == 128 || head_dim == 192;
+    if (o.path == FDEC_PATH_MMA && !mma_ok)
+        return fail(FDEC_ERR_UNSUPPORTED, "the tensor-core path supports head_dim 64, 128 and 192");
     const long long rows_ll = static_cast<long long>(q_len) * (num_qo_heads / num_kv_heads);
     if (rows_ll > (1 << 24)) return fail(FDEC_ERR_UNSUPPORTED, "q_len x group too large");
     for (int b = 0; b < batch; ++b)
@@ -349,13 +352,19 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
     p->rows = static_cast<int>(rows_ll);
     p->dtype = dtype;
     p->causal = (causal != 0 && q_len > 1) ? 1 : 0;
-    p->path = FDEC_PATH_SIMT;
+    // Tensor cores by default where the kernel exists (see split_mma_kernel.cuh for
+    // why); the fp32 SIMT kernel on request and for head_dim 256 / 512.
+    p->path = (o.path == FDEC_PATH_SIMT || (o.path == FDEC_PATH_AUTO && !mma_ok)) ? FDEC_PATH_SIMT : FDEC_PATH_MMA;
     p->num_sms = num_sms;
     p->fanin = o.reducer_fanin > 0 ? o.reducer_fanin : 64;
-    p->rc = std::min(next_pow2(p->rows), split_max_rc(head_dim));
+    if (p->path == FDEC_PATH_MMA) {
+        p->rc = kMmaRows;
+    } else {
+        p->rc = std::min(next_pow2(p->rows), split_max_rc(head_dim));
+    }
     p->row_groups = (p->rows + p->rc - 1) / p->rc;
-    const size_t smem = split_smem_bytes(head_dim, p->rc);
-    const int threads = split_threads(head_dim);
+    const size_t smem = p->path == FDEC_PATH_MMA ? split_mma_smem_bytes(head_dim) : split_smem_bytes(head_dim, p->rc);
+    const int threads = p->path == FDEC_PATH_MMA ? split_mma_threads(head_dim) : split_threads(head_dim);
     p->ctas_per_sm = std::max(1, std::min(static_cast<int>(233472 / (smem + 1024)), 2048 / threads));
 
     p->capacity.assign(seq_lens_host, seq_lens_host + batch);

@@ -88,6 +88,13 @@ cudaError_t launch_split_d256(const SplitParams& p, const CUtensorMap& tk, const
 cudaError_t launch_split_d512(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int rc,
                                bool bf16, dim3 grid, cudaStream_t s, bool launch);
 
+// The tensor-core split kernel (head_dim 64, 128, 192; query rows in groups of 16).
+cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int head_dim,
+                             bool bf16, dim3 grid, cudaStream_t s, bool launch);
+size_t split_mma_smem_bytes(int head_dim);
+int split_mma_threads(int head_dim);
+constexpr int kMmaRows = 16;
+
 // Shared-memory bytes and threads of the split kernel for (D, RC); 0 if not built.
 size_t split_smem_bytes(int head_dim, int rc);
 int split_threads(int head_dim);

@@ -1,0 +1,256 @@
+// split_common.cuh -- pieces shared by the split kernels: the stage geometry,
+// the producer warp (page-table walk + TMA gather into swizzled stages), the
+// zeroing of a partial stage's tail, and the epilogue that merges the consumer
+// warps' (m, l, o) states and writes a partial or the final out / lse.
+//
+// Stage layout (per K and per V): D/64 regions of [32 rows][128 bytes]; the
+// 16-byte chunk c of row r sits at chunk position c ^ (r & 7) (TMA SWIZZLE_128B).
+// Stage i completes barrier full[i % 2S] (phase i / 2S) and is released on
+// empty[i % S]; see the consumer loops for why 2S full barriers are needed.
+#pragma once
+
+#include <cmath>
+#include <type_traits>
+
+#include "../../include/fdec.h"
+#include "device_utils.cuh"
+#include "fdec_internal.h"
+
+namespace fdec {
+
+template <int I, int N, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+    if constexpr (I < N) {
+        f(std::integral_constant<int, I>{});
+        static_for<I + 1, N>(f);
+    }
+}
+
+template <int D>
+struct StageGeom {
+    static constexpr int REGIONS = D / 64;
+    static constexpr int REGION_BYTES = kStageTokens * 128;  // 32 rows x 128 B
+    static constexpr int HALF_BYTES = REGIONS * REGION_BYTES;  // K (or V) of one stage
+    static constexpr int STAGE_BYTES = 2 * HALF_BYTES;         // K regions then V regions
+};
+
+// Token range of a work item, with the run-time length clamped to the planned capacity.
+struct ItemRange {
+    int L, tok_begin, tok_end, n_stage;
+};
+
+__device__ __forceinline__ ItemRange item_range(const SplitParams& p, const WorkItem& it) {
+    int L = p.seq_lens[it.seq];
+    const int cap = p.capacity[it.seq];
+    if (L > cap || L < 0) {
+        if (threadIdx.x == 0) atomicOr(p.err, FDEC_DEVERR_SEQ_LEN);
+        L = L < 0 ? 0 : cap;
+    }
+    ItemRange r;
+    r.L = L;
+    r.tok_begin = it.block_begin * kBlockTokens;
+    r.tok_end = min(it.block_end * kBlockTokens, L);
+    r.n_stage = r.tok_end > r.tok_begin ? (r.tok_end - r.tok_begin + kStageTokens - 1) / kStageTokens : 0;
+    return r;
+}
+
+// Initialise the 2S full and S empty barriers (thread 0).  Pages of >= 8 tokens
+// complete a stage with one expect-tx arrival (TMA); smaller pages with the 32
+// cp.async arrivals of the producer lanes.
+template <int S>
+__device__ __forceinline__ void init_stage_barriers(uint64_t* full, uint64_t* empty, bool tma_mode) {
+    const uint32_t full_count = tma_mode ? 1u : 32u;
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+        mbar_init(smem_addr(&full[s]), full_count);
+        mbar_init(smem_addr(&full[S + s]), full_count);
+        mbar_init(smem_addr(&empty[s]), 1);
+    }
+    fence_mbar_init();
+}
+
+// The producer warp: fills stage i into slot i % S once the slot is released.
+template <int D, int S>
+__device__ void produce_stages(const SplitParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv, uint64_t* full,
+                               uint64_t* empty, uint8_t* stages, int b, int kvh, const ItemRange& ir,
+                               bool tma_mode) {
+    using G = StageGeom<D>;
+    const int lane = threadIdx.x & 31;
+    const int tok_begin = ir.tok_begin, tok_end = ir.tok_end, n_stage = ir.n_stage;
+    if (n_stage == 0) return;
+    const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride;
+    const int page_mask = (1 << p.page_shift) - 1;
+    int issued = 0;
+    bool ok = true;
+    if (tma_mode) {
+        // Boxes of BR token rows, NB boxes per 32-token stage; the page id of
+        // box n is held by lane n % 32, one group of 32 boxes ahead.
+        const int BR = min(1 << p.page_shift, kStageTokens);
+        const int NB = kStageTokens / BR;
+        const int n_box = (tok_end - tok_begin + BR - 1) / BR;
+        const uint32_t box_bytes = static_cast<uint32_t>(BR) * 2u * (2u * D);  // K and V
+        auto box_page = [&](int n) -> int {
+            return n < n_box ? __ldg(pt + ((tok_begin + n * BR) >> p.page_shift)) : -1;
+        };
+        int pid = box_page(lane);
+        int pid_next = box_page(32 + lane);
+        int group = 0;
+        for (int i = 0; i < n_stage; ++i) {
+            const int s = i % S;
+            if (i >= S) {
+                bool got = true;
+                if (lane == 0) got = mbar_wait_bounded(smem_addr(&empty[s]), ((i / S) - 1) & 1);
+                if (!__shfl_sync(0xffffffffu, got, 0)) {
+                    ok = false;
+                    break;
+                }
+            }
+            const int box0 = i * NB;
+            if ((box0 >> 5) != group) {  // NB divides 32: a stage never straddles two groups
+                pid = pid_next;
+                group = box0 >> 5;
+                pid_next = box_page((group + 1) * 32 + lane);
+            }
+            // lane j < NB checks box box0 + j
+            const int my_page = __shfl_sync(0xffffffffu, pid, (box0 + lane) & 31);
+            const bool in_range = lane < NB && box0 + lane < n_box;
+            const bool valid = in_range && my_page >= 0 && my_page < p.k_pages && my_page < p.v_pages;
+            if (in_range && !valid) atomicOr(p.err, FDEC_DEVERR_PAGE_ID);
+            const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+            const uint32_t fbar = smem_addr(&full[i % (2 * S)]);
+            if (lane == 0) mbar_arrive_expect_tx(fbar, static_cast<uint32_t>(__popc(vmask)) * box_bytes);
+            for (int j = 0; j < NB; ++j) {
+                const int page = __shfl_sync(0xffffffffu, my_page, j);
+                if (lane == 0 && ((vmask >> j) & 1u)) {
+                    const int slot0 = (tok_begin + (box0 + j) * BR) & page_mask;
+                    uint8_t* kdst = stages + s * G::STAGE_BYTES + j * BR * 128;
+                    // coordinate n (1..3) of each map: whichever of slot, head, page sits there
+                    auto coord = [&](int n, int ps, int ph) { return n == ps ? slot0 : (n == ph ? kvh : page); };
+                    const int k1 = coord(1, p.k_pos_slot, p.k_pos_head), k2 = coord(2, p.k_pos_slot, p.k_pos_head),
+                              k3 = coord(3, p.k_pos_slot, p.k_pos_head);
+                    const int v1 = coord(1, p.v_pos_slot, p.v_pos_head), v2 = coord(2, p.v_pos_slot, p.v_pos_head),
+                              v3 = coord(3, p.v_pos_slot, p.v_pos_head);
+#pragma unroll
+                    for (int r = 0; r < G::REGIONS; ++r) {
+                        tma_load_4d(smem_addr(kdst + r * G::REGION_BYTES), tmk, r * 64, k1, k2, k3, fbar);
+                        tma_load_4d(smem_addr(kdst + G::HALF_BYTES + r * G::REGION_BYTES), tmv, r * 64, v1, v2, v3,
+                                    fbar);
+                    }
+                }
+            }
+            issued = i + 1;
+        }
+    } else {
+        // Small pages: 16-byte cp.async per (row, chunk) into the swizzled layout.
+        constexpr int CHUNKS = D / 8;
+        for (int i = 0; i < n_stage; ++i) {
+            const int s = i % S;
+            if (i >= S) {
+                bool got = true;
+                if (lane == 0) got = mbar_wait_bounded(smem_addr(&empty[s]), ((i / S) - 1) & 1);
+                if (!__shfl_sync(0xffffffffu, got, 0)) {
+                    ok = false;
+                    break;
+                }
+            }
+            const int t_lane = tok_begin + i * kStageTokens + lane;
+            const bool in_range = t_lane < tok_end;
+            const int my_page = in_range ? __ldg(pt + (t_lane >> p.page_shift)) : -1;
+            const bool valid = in_range && my_page >= 0 && my_page < p.k_pages && my_page < p.v_pages;
+            if (in_range && !valid) atomicOr(p.err, FDEC_DEVERR_PAGE_ID);
+            uint8_t* sbase = stages + s * G::STAGE_BYTES;
+            for (int idx = lane; idx < kStageTokens * CHUNKS; idx += 32) {
+                const int row = idx / CHUNKS;
+                const int c = idx - row * CHUNKS;
+                const int page = __shfl_sync(0xffffffffu, my_page, row);
+                const bool ok_row = __shfl_sync(0xffffffffu, valid, row);
+                if (ok_row) {
+                    const int slot = (tok_begin + i * kStageTokens + row) & page_mask;
+                    const uint32_t off = (c >> 3) * G::REGION_BYTES + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+                    cp_async_16(smem_addr(sbase + off), p.k_base + page * p.k_sp + kvh * p.k_sh + slot * p.k_st + c * 16);
+                    cp_async_16(smem_addr(sbase + G::HALF_BYTES + off),
+                                p.v_base + page * p.v_sp + kvh * p.v_sh + slot * p.v_st + c * 16);
+                }
+            }
+            cp_async_arrive_noinc(smem_addr(&full[i % (2 * S)]));
+            issued = i + 1;
+        }
+    }
+    // Do not leave while copies of this CTA may still be landing.
+    for (int i = issued > S ? issued - S : 0; i < issued; ++i) {
+        bool got = true;
+        if (lane == 0) got = mbar_wait_bounded(smem_addr(&full[i % (2 * S)]), (i / (2 * S)) & 1);
+        if (!__shfl_sync(0xffffffffu, got, 0)) ok = false;
+    }
+    if (!ok && lane == 0) atomicOr(p.err, FDEC_DEVERR_TIMEOUT);
+}
+
+// Consumer side of stage i: wait until it has landed.  Stage i completes
+// full[i % 2S] in phase i / 2S.  Stages land out of order and a slot's phases
+// are consumed by different warps, but the previous phase of this barrier (stage
+// i - 2S) was consumed before stage i - S was issued, and that was issued before
+// the caller's previous stage: so the barrier is in phase i / 2S or just past it,
+// and the parity test is unambiguous.
+template <int S>
+__device__ __forceinline__ bool wait_stage(uint64_t* full, int i) {
+    bool got = true;
+    if ((threadIdx.x & 31) == 0) got = mbar_wait_bounded(smem_addr(&full[i % (2 * S)]), (i / (2 * S)) & 1);
+    return __shfl_sync(0xffffffffu, got, 0) != 0;
+}
+
+// A partial (last) stage: rows past the sequence end hold whatever the page
+// held; zero its V rows [nv, 32) so that a fixed-size p.V loop adds 0 * 0.
+template <int D>
+__device__ __forceinline__ void zero_v_tail(uint8_t* stage, int nv) {
+    using G = StageGeom<D>;
+    const int lane = threadIdx.x & 31;
+    uint8_t* vrows = stage + G::HALF_BYTES;
+    for (int idx = lane; idx < (kStageTokens - nv) * G::REGIONS * 8; idx += 32) {
+        const int row = nv + idx / (G::REGIONS * 8);
+        const int rem = idx % (G::REGIONS * 8);
+        *reinterpret_cast<uint4*>(vrows + (rem >> 3) * G::REGION_BYTES + row * 128 + (rem & 7) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncwarp();
+}
+
+// Epilogue, after every consumer has written its state to the scratch
+// sm_m [NW][RC], sm_l [NW][RC], sm_o [NW][RC][D] and passed a barrier: merge the
+// NW states by log-sum-exp (m in log2 units) and write the split's partial or,
+// when one split covers the sequence, out = O / L and lse = ln 2 * (M + log2 L).
+template <int NW, int RC, int D>
+__device__ __forceinline__ void merge_and_store(const SplitParams& p, const WorkItem& it, int kvh, int row0,
+                                                const float* sm_m, const float* sm_l, const float* sm_o) {
+    constexpr float kLn2 = 0.69314718055994530942f;
+    for (int idx = threadIdx.x; idx < RC * D; idx += NW * 32) {
+        const int r = idx / D;
+        const int d = idx - r * D;
+        const int row = row0 + r;
+        if (row >= p.rows) continue;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w * RC + r]);
+        float Ls = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float e = exp2_approx(sm_m[w * RC + r] - M);
+                Ls += sm_l[w * RC + r] * e;
+                O += sm_o[(w * RC + r) * D + d] * e;
+            }
+        }
+        if (it.slot < 0) {
+            const int qi = row / p.group;
+            const int h = kvh * p.group + (row - qi * p.group);
+            const int64_t orow = static_cast<int64_t>(it.seq * p.q_len + qi) * p.hq + h;
+            p.out[orow * D + d] = Ls > 0.f ? O / Ls : 0.f;
+            if (d == 0 && p.lse != nullptr) p.lse[orow] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+        } else {
+            const int64_t prow = (static_cast<int64_t>(it.slot) * p.hk + kvh) * p.rows + row;
+            p.part_o[prow * D + d] = O;
+            if (d == 0) p.part_ml[prow] = make_float2(M, Ls);
+        }
+    }
+}
+
+}  // namespace fdec

@@ -28,43 +28,48 @@
 // empty partial (m = -inf, l = 0) that the reduction skips.
 #pragma once
 
-#include <cmath>
-
-#include "../../include/fdec.h"
-#include "device_utils.cuh"
-#include "fdec_internal.h"
+#include "split_common.cuh"
 
 namespace fdec {
 
 template <int D>
-struct SplitShape;
-// NW consumer warps, RCMAX largest query-row group, MINB CTAs per SM to aim for,
-// SMAX largest stage count.
-template <> struct SplitShape<64>  { static constexpr int NW = 8, RCMAX = 16, MINB = 2, SMAX = 16; };
-template <> struct SplitShape<128> { static constexpr int NW = 8, RCMAX = 16, MINB = 1, SMAX = 16; };
-template <> struct SplitShape<192> { static constexpr int NW = 4, RCMAX = 8,  MINB = 1, SMAX = 16; };
-template <> struct SplitShape<256> { static constexpr int NW = 4, RCMAX = 8,  MINB = 1, SMAX = 16; };
-template <> struct SplitShape<512> { static constexpr int NW = 2, RCMAX = 4,  MINB = 1, SMAX = 16; };
+struct SplitShape {
+    // Register file allocation rounds a CTA up to whole groups of four warps, so
+    // 12 warps (11 consumers + the producer) cost no more registers per thread
+    // than 9 do.  RCMAX bounds the per-lane accumulators (RC x D/32 floats).
+    static constexpr int NWMAX = D <= 128 ? 11 : (D <= 256 ? 7 : 3);
+    static constexpr int RCMAX = D <= 128 ? 16 : (D <= 256 ? 8 : 4);
+};
 
 template <int D, int RC>
 struct SplitLayout {
-    static constexpr int NW = SplitShape<D>::NW;
-    static constexpr int THREADS = (NW + 1) * 32;
-    static constexpr int REGIONS = D / 64;
-    static constexpr int REGION_BYTES = kStageTokens * 128;       // 32 rows x 128 B
-    static constexpr int HALF_BYTES = REGIONS * REGION_BYTES;      // K (or V) of one stage
-    static constexpr int STAGE_BYTES = 2 * HALF_BYTES;             // K regions then V regions
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int REGIONS = StageGeom<D>::REGIONS;
+    static constexpr int REGION_BYTES = StageGeom<D>::REGION_BYTES;
+    static constexpr int HALF_BYTES = StageGeom<D>::HALF_BYTES;
+    static constexpr int STAGE_BYTES = StageGeom<D>::STAGE_BYTES;
+    static constexpr int BAR_BYTES = 512;
     static constexpr int Q_BYTES = RC * D * 4;
-    static constexpr int P_BYTES = NW * kStageTokens * RC * 8;     // p as (p, p) pairs
     static constexpr int ALIGN_SLACK = 1024;                       // stage area is 1024-byte aligned
-    static constexpr int FIXED = BAR_BYTES + Q_BYTES + P_BYTES + ALIGN_SLACK;
-    static constexpr int BUDGET = (232448 / SplitShape<D>::MINB) - 1024;
-    static constexpr int S_FIT = (BUDGET - FIXED) / STAGE_BYTES;
-    static constexpr int S = S_FIT > SplitShape<D>::SMAX ? SplitShape<D>::SMAX : S_FIT;
-    static constexpr int SMEM = FIXED + S * STAGE_BYTES;
+    static constexpr int BUDGET = 232448 - 1024;
+    static constexpr int SMAX = 16;
+    static constexpr int p_bytes(int nw) { return nw * kStageTokens * RC * 8; }  // p as (p, p) pairs
+    static constexpr int fixed(int nw) { return BAR_BYTES + Q_BYTES + p_bytes(nw) + ALIGN_SLACK; }
+    static constexpr int stages(int nw) {
+        return (BUDGET - fixed(nw)) / STAGE_BYTES > SMAX ? SMAX : (BUDGET - fixed(nw)) / STAGE_BYTES;
+    }
+    // The most consumer warps that still leave a stage in flight beyond one per consumer.
+    static constexpr int pick_nw() {
+        for (int nw = SplitShape<D>::NWMAX; nw > 1; --nw)
+            if (stages(nw) >= nw + 1) return nw;
+        return 1;
+    }
+    static constexpr int NW = pick_nw();
+    static constexpr int THREADS = (NW + 1) * 32;
+    static constexpr int P_BYTES = p_bytes(NW);
+    static constexpr int S = stages(NW);
+    static constexpr int SMEM = fixed(NW) + S * STAGE_BYTES;
     static_assert(S >= NW, "each consumer warp needs its own stage in flight");
-    static_assert(2 * S * 8 <= BAR_BYTES, "barrier area too small");
+    static_assert(3 * S * 8 <= BAR_BYTES, "barrier area too small");
     static_assert(NW * RC * (D + 2) * 4 <= S * STAGE_BYTES, "merge scratch must fit the stage area");
     static_assert((BAR_BYTES + Q_BYTES + P_BYTES) % 16 == 0, "alignment");
 };
@@ -84,7 +89,7 @@ __device__ __forceinline__ void load_p_pairs(const float2* src, float2 (&pr)[RC]
 }
 
 template <int D, int RC, bool BF16>
-__global__ void __launch_bounds__(SplitLayout<D, RC>::THREADS, SplitShape<D>::MINB)
+__global__ void __launch_bounds__(SplitLayout<D, RC>::THREADS, 1)
 split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
              const __grid_constant__ CUtensorMap tmv) {
     using Lay = SplitLayout<D, RC>;
@@ -95,11 +100,10 @@ split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUte
     constexpr int HALF_BYTES = Lay::HALF_BYTES;
     constexpr int STAGE_BYTES = Lay::STAGE_BYTES;
     constexpr int DP = D / 64;  // dim pairs per lane in p.V
-    constexpr float kLn2 = 0.69314718055994530942f;
 
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + S;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // 2S: stage i uses full[i % 2S]
+    uint64_t* empty = full + 2 * S;                       // S: stage i releases empty[i % S]
     float* q_s = reinterpret_cast<float*>(smem + Lay::BAR_BYTES);
     float2* p_s = reinterpret_cast<float2*>(q_s + RC * D);
     uint8_t* stages;
@@ -116,26 +120,10 @@ split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUte
     const int kvh = blockIdx.y;
     const int row0 = blockIdx.z * RC;
 
-    int L = p.seq_lens[b];
-    const int cap = p.capacity[b];
-    if (L > cap || L < 0) {
-        if (threadIdx.x == 0) atomicOr(p.err, FDEC_DEVERR_SEQ_LEN);
-        L = L < 0 ? 0 : cap;
-    }
-    const int tok_begin = it.block_begin * kBlockTokens;
-    const int tok_end = min(it.block_end * kBlockTokens, L);
-    const int n_stage = tok_end > tok_begin ? (tok_end - tok_begin + kStageTokens - 1) / kStageTokens : 0;
+    const ItemRange ir = item_range(p, it);
+    const int L = ir.L, tok_begin = ir.tok_begin, tok_end = ir.tok_end, n_stage = ir.n_stage;
     const bool tma_mode = p.page_shift >= 3;  // pages of >= 8 tokens
-
-    if (threadIdx.x == 0) {
-        const uint32_t full_count = tma_mode ? 1u : 32u;
-#pragma unroll
-        for (int s = 0; s < S; ++s) {
-            mbar_init(smem_addr(&full[s]), full_count);
-            mbar_init(smem_addr(&empty[s]), 1);
-        }
-        fence_mbar_init();
-    }
+    if (threadIdx.x == 0) init_stage_barriers<S>(full, empty, tma_mode);
     if (warp == NW && lane == 0 && tma_mode) {
         prefetch_tmap(&tmk);
         prefetch_tmap(&tmv);
@@ -158,117 +146,7 @@ split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUte
     __syncthreads();
 
     if (warp == NW) {
-        // ------------------------------------------------------------------ producer
-        if (n_stage == 0) return;
-        const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride;
-        const int page_mask = (1 << p.page_shift) - 1;
-        int issued = 0;
-        bool ok = true;
-        if (tma_mode) {
-            // Boxes of BR token rows, NB boxes per 32-token stage; the page id of
-            // box n is held by lane n % 32, one group of 32 boxes ahead.
-            const int BR = min(1 << p.page_shift, kStageTokens);
-            const int NB = kStageTokens / BR;
-            const int n_box = (tok_end - tok_begin + BR - 1) / BR;
-            const uint32_t box_bytes = static_cast<uint32_t>(BR) * 2u * (2u * D);  // K and V
-            auto box_page = [&](int n) -> int {
-                return n < n_box ? __ldg(pt + ((tok_begin + n * BR) >> p.page_shift)) : -1;
-            };
-            int pid = box_page(lane);
-            int pid_next = box_page(32 + lane);
-            int group = 0;
-            for (int i = 0; i < n_stage; ++i) {
-                const int s = i % S;
-                if (i >= S) {
-                    bool got = true;
-                    if (lane == 0) got = mbar_wait_bounded(smem_addr(&empty[s]), ((i / S) - 1) & 1);
-                    if (!__shfl_sync(0xffffffffu, got, 0)) {
-                        ok = false;
-                        break;
-                    }
-                }
-                const int box0 = i * NB;
-                if ((box0 >> 5) != group) {  // NB divides 32: a stage never straddles two groups
-                    pid = pid_next;
-                    group = box0 >> 5;
-                    pid_next = box_page((group + 1) * 32 + lane);
-                }
-                // lane j < NB checks box box0 + j
-                const int my_page = __shfl_sync(0xffffffffu, pid, (box0 + lane) & 31);
-                const bool in_range = lane < NB && box0 + lane < n_box;
-                const bool valid = in_range && my_page >= 0 && my_page < p.k_pages && my_page < p.v_pages;
-                if (in_range && !valid) atomicOr(p.err, FDEC_DEVERR_PAGE_ID);
-                const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-                const uint32_t fbar = smem_addr(&full[s]);
-                if (lane == 0) mbar_arrive_expect_tx(fbar, static_cast<uint32_t>(__popc(vmask)) * box_bytes);
-                for (int j = 0; j < NB; ++j) {
-                    const int page = __shfl_sync(0xffffffffu, my_page, j);
-                    if (lane == 0 && ((vmask >> j) & 1u)) {
-                        const int slot0 = (tok_begin + (box0 + j) * BR) & page_mask;
-                        uint8_t* kdst = stages + s * STAGE_BYTES + j * BR * 128;
-                        int ck[4], cv[4];
-                        ck[0] = 0;
-                        ck[p.k_pos_slot] = slot0;
-                        ck[p.k_pos_head] = kvh;
-                        ck[p.k_pos_page] = page;
-                        cv[0] = 0;
-                        cv[p.v_pos_slot] = slot0;
-                        cv[p.v_pos_head] = kvh;
-                        cv[p.v_pos_page] = page;
-#pragma unroll
-                        for (int r = 0; r < REGIONS; ++r) {
-                            tma_load_4d(smem_addr(kdst + r * REGION_BYTES), &tmk, r * 64, ck[1], ck[2], ck[3], fbar);
-                            tma_load_4d(smem_addr(kdst + HALF_BYTES + r * REGION_BYTES), &tmv, r * 64, cv[1], cv[2],
-                                        cv[3], fbar);
-                        }
-                    }
-                }
-                issued = i + 1;
-            }
-        } else {
-            // Small pages: 16-byte cp.async per (row, chunk) into the swizzled layout.
-            constexpr int CHUNKS = D / 8;
-            for (int i = 0; i < n_stage; ++i) {
-                const int s = i % S;
-                if (i >= S) {
-                    bool got = true;
-                    if (lane == 0) got = mbar_wait_bounded(smem_addr(&empty[s]), ((i / S) - 1) & 1);
-                    if (!__shfl_sync(0xffffffffu, got, 0)) {
-                        ok = false;
-                        break;
-                    }
-                }
-                const int t_lane = tok_begin + i * kStageTokens + lane;
-                const bool in_range = t_lane < tok_end;
-                const int my_page = in_range ? __ldg(pt + (t_lane >> p.page_shift)) : -1;
-                const bool valid = in_range && my_page >= 0 && my_page < p.k_pages && my_page < p.v_pages;
-                if (in_range && !valid) atomicOr(p.err, FDEC_DEVERR_PAGE_ID);
-                uint8_t* sbase = stages + s * STAGE_BYTES;
-                for (int idx = lane; idx < kStageTokens * CHUNKS; idx += 32) {
-                    const int row = idx / CHUNKS;
-                    const int c = idx - row * CHUNKS;
-                    const int page = __shfl_sync(0xffffffffu, my_page, row);
-                    const bool ok_row = __shfl_sync(0xffffffffu, valid, row);
-                    if (ok_row) {
-                        const int slot = (tok_begin + i * kStageTokens + row) & page_mask;
-                        const uint32_t off = (c >> 3) * REGION_BYTES + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-                        cp_async_16(smem_addr(sbase + off),
-                                    p.k_base + page * p.k_sp + kvh * p.k_sh + slot * p.k_st + c * 16);
-                        cp_async_16(smem_addr(sbase + HALF_BYTES + off),
-                                    p.v_base + page * p.v_sp + kvh * p.v_sh + slot * p.v_st + c * 16);
-                    }
-                }
-                cp_async_arrive_noinc(smem_addr(&full[s]));
-                issued = i + 1;
-            }
-        }
-        // Do not leave while copies of this CTA may still be landing.
-        for (int i = issued > S ? issued - S : 0; i < issued; ++i) {
-            bool got = true;
-            if (lane == 0) got = mbar_wait_bounded(smem_addr(&full[i % S]), (i / S) & 1);
-            if (!__shfl_sync(0xffffffffu, got, 0)) ok = false;
-        }
-        if (!ok && lane == 0) atomicOr(p.err, FDEC_DEVERR_TIMEOUT);
+        produce_stages<D, S>(p, &tmk, &tmv, full, empty, stages, b, kvh, ir, tma_mode);
         return;
     }
 
@@ -285,8 +163,9 @@ split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUte
         const int qi = (row0 + r) / p.group;
         lim[r] = p.causal ? (L - p.q_len + qi) : (L - 1);
     }
-    float2* pw = p_s + warp * kStageTokens * RC;
-    const float4* q4 = reinterpret_cast<const float4*>(q_s);
+    const uint32_t q_base = smem_addr(q_s);
+    const uint32_t pw_base = smem_addr(p_s + warp * kStageTokens * RC);
+    const uint32_t stages_base = smem_addr(stages);
     // Swizzled byte offsets: K chunk j of this lane's row; this lane's V dim pair in a row r with r & 7 == j.
     uint32_t koff[8], voff[8];
 #pragma unroll
@@ -298,78 +177,109 @@ split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUte
 
     for (int i = warp; i < n_stage; i += NW) {
         const int s = i % S;
-        bool got = true;
-        if (lane == 0) got = mbar_wait_bounded(smem_addr(&full[s]), (i / S) & 1);
-        if (!__shfl_sync(0xffffffffu, got, 0)) {
+        if (!wait_stage<S>(full, i)) {
             ok = false;
             break;
         }
         const int t0 = tok_begin + i * kStageTokens;
         const int nv = min(kStageTokens, tok_end - t0);
-        const uint8_t* Ks = stages + s * STAGE_BYTES;
-        const uint8_t* Vs = Ks + HALF_BYTES;
+        const uint32_t kbase = stages_base + s * STAGE_BYTES;
+        const uint32_t vbase = kbase + HALF_BYTES;
+        if (nv < kStageTokens) zero_v_tail<D>(stages + s * STAGE_BYTES, nv);
 
-        // q.K: this lane's token against every row of the group
-        float2 acc[RC];
-#pragma unroll
-        for (int r = 0; r < RC; ++r) acc[r] = make_float2(0.f, 0.f);
-#pragma unroll 8
-        for (int c = 0; c < D / 8; ++c) {
-            const uint4 kr = *reinterpret_cast<const uint4*>(Ks + (c >> 3) * REGION_BYTES + koff[c & 7]);
-            const float2 k0 = unpack2<BF16>(kr.x);
-            const float2 k1 = unpack2<BF16>(kr.y);
-            const float2 k2 = unpack2<BF16>(kr.z);
-            const float2 k3 = unpack2<BF16>(kr.w);
-#pragma unroll
-            for (int r = 0; r < RC; ++r) {
-                const float4 qa = q4[r * (D / 4) + 2 * c];
-                const float4 qb = q4[r * (D / 4) + 2 * c + 1];
-                acc[r] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc[r]);
-                acc[r] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc[r]);
-                acc[r] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc[r]);
-                acc[r] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc[r]);
-            }
-        }
-
-        // online softmax over this stage's tokens (log2 units)
-        const int t = t0 + lane;
+        // q.K: this lane's token against every row of the group (two partial
+        // sums per row when registers allow, for independent FMA chains)
+        float2 acc[RC], acc2[RC];
 #pragma unroll
         for (int r = 0; r < RC; ++r) {
-            float z = acc[r].x + acc[r].y;
-            if (lane >= nv || t > lim[r]) z = -INFINITY;
-            const float mx = warp_max(z);
-            const float m_new = fmaxf(m[r], mx);
-            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = exp2_approx(m[r] - m_use);
-            const float pr = exp2_approx(z - m_use);
-            l[r] = l[r] * alpha + pr;
-            m[r] = m_new;
-            const float2 a2 = make_float2(alpha, alpha);
+            acc[r] = make_float2(0.f, 0.f);
+            acc2[r] = make_float2(0.f, 0.f);
+        }
+        uint32_t ka[8];
 #pragma unroll
-            for (int k = 0; k < DP; ++k) o2[r][k] = __fmul2_rn(o2[r][k], a2);
-            pw[lane * RC + r] = make_float2(pr, pr);
+        for (int j = 0; j < 8; ++j) ka[j] = kbase + koff[j];
+        // One 64-dim region (8 chunks of 8 dims) per iteration keeps the code small.
+#pragma unroll 1
+        for (int reg = 0; reg < REGIONS; ++reg) {
+            const uint32_t qreg = q_base + reg * 256;
+            static_for<0, 8>([&](auto cc) {
+                constexpr int c = decltype(cc)::value;
+                const uint4 kr = lds128<0>(ka[c] + reg * REGION_BYTES);
+                const float2 k0 = unpack2<BF16>(kr.x);
+                const float2 k1 = unpack2<BF16>(kr.y);
+                const float2 k2 = unpack2<BF16>(kr.z);
+                const float2 k3 = unpack2<BF16>(kr.w);
+                static_for<0, RC>([&](auto rr) {
+                    constexpr int r = decltype(rr)::value;
+                    const float4 qa = lds128f<(r * D + 8 * c) * 4>(qreg);
+                    const float4 qb = lds128f<(r * D + 8 * c + 4) * 4>(qreg);
+                    if constexpr (RC <= 8) {
+                        acc[r] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc[r]);
+                        acc2[r] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc2[r]);
+                        acc[r] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc[r]);
+                        acc2[r] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc2[r]);
+                    } else {  // many rows already give independent chains; save the registers
+                        acc[r] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc[r]);
+                        acc[r] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc[r]);
+                        acc[r] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc[r]);
+                        acc[r] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc[r]);
+                    }
+                });
+            });
+        }
+
+        // Online softmax over this stage's tokens, in log2 units.  The running
+        // max is raised (with the rescale of l and o) only when some token beats
+        // it by more than kLazyRescale; otherwise p = exp2(z - m) <= 2^kLazyRescale.
+        constexpr float kLazyRescale = 8.f;
+#pragma unroll
+        for (int r = 0; r < RC; ++r) {
+            const int vis = min(nv, lim[r] - t0 + 1);  // tokens of this stage row r may see
+            float z = (acc[r].x + acc[r].y) + (acc2[r].x + acc2[r].y);
+            if (lane >= vis) z = -INFINITY;
+            if (__any_sync(0xffffffffu, z > m[r] + kLazyRescale)) {
+                const float m_new = fmaxf(m[r], warp_max(z));
+                const float alpha = exp2_approx(m[r] - m_new);  // 0 when m was -inf
+                l[r] *= alpha;
+                const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+                for (int k = 0; k < DP; ++k) o2[r][k] = __fmul2_rn(o2[r][k], a2);
+                m[r] = m_new;
+            }
+            const float pr = exp2_approx(z - (m[r] == -INFINITY ? 0.f : m[r]));
+            l[r] += pr;
+            *reinterpret_cast<float2*>(p_s + warp * kStageTokens * RC + lane * RC + r) = make_float2(pr, pr);
         }
         __syncwarp();
 
-        // p.V: this lane's dim pairs over the stage's tokens
-        for (int tt0 = 0; tt0 < nv; tt0 += 8) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int tt = tt0 + j;
-                if (tt < nv) {
-                    float2 pr[RC];
-                    load_p_pairs<RC>(pw + tt * RC, pr);
-                    const uint8_t* vrow = Vs + tt0 * 128 + voff[j];
-#pragma unroll
-                    for (int k = 0; k < DP; ++k) {
-                        const uint32_t w = *reinterpret_cast<const uint32_t*>(vrow + k * REGION_BYTES);
-                        const float2 v2 = unpack2<BF16>(w);
-#pragma unroll
-                        for (int r = 0; r < RC; ++r) o2[r][k] = __ffma2_rn(pr[r], v2, o2[r][k]);
+        // p.V: this lane's dim pairs over the stage's tokens, eight at a time
+        const int groups = (nv + 7) >> 3;
+        for (int g = 0; g < groups; ++g) {
+            const uint32_t vg = vbase + g * 8 * 128;
+            const uint32_t pg = pw_base + g * 8 * RC * 8;
+            static_for<0, 8>([&](auto jj) {
+                constexpr int j = decltype(jj)::value;
+                float2 pr[RC];
+                static_for<0, (RC + 1) / 2>([&](auto hh) {
+                    constexpr int h = decltype(hh)::value;
+                    if constexpr (2 * h + 1 < RC) {
+                        const float4 x = lds128f<(j * RC + 2 * h) * 8>(pg);
+                        pr[2 * h] = make_float2(x.x, x.y);
+                        pr[2 * h + 1] = make_float2(x.z, x.w);
+                    } else {
+                        pr[2 * h] = lds64f<(j * RC + 2 * h) * 8>(pg);
                     }
-                }
-            }
+                });
+                const uint32_t vrow = vg + voff[j];
+                static_for<0, DP>([&](auto kk) {
+                    constexpr int k = decltype(kk)::value;
+                    const float2 v2 = unpack2<BF16>(lds32<k * REGION_BYTES>(vrow));
+#pragma unroll
+                    for (int r = 0; r < RC; ++r) o2[r][k] = __ffma2_rn(pr[r], v2, o2[r][k]);
+                });
+            });
         }
+        if (nv < kStageTokens) fence_proxy_async_shared();  // generic zeroing before the slot's next TMA write
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
     }
@@ -396,35 +306,7 @@ split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUte
             *reinterpret_cast<float2*>(sm_o + (warp * RC + r) * D + k * 64 + 2 * lane) = o2[r][k];
     named_barrier(1, NW * 32);
 
-    for (int idx = threadIdx.x; idx < RC * D; idx += NW * 32) {
-        const int r = idx / D;
-        const int d = idx - r * D;
-        const int row = row0 + r;
-        if (row >= p.rows) continue;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w * RC + r]);
-        float Ls = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float e = exp2_approx(sm_m[w * RC + r] - M);
-                Ls += sm_l[w * RC + r] * e;
-                O += sm_o[(w * RC + r) * D + d] * e;
-            }
-        }
-        if (it.slot < 0) {
-            const int qi = row / p.group;
-            const int h = kvh * p.group + (row - qi * p.group);
-            const int64_t orow = static_cast<int64_t>(b * p.q_len + qi) * p.hq + h;
-            p.out[orow * D + d] = Ls > 0.f ? O / Ls : 0.f;
-            if (d == 0 && p.lse != nullptr) p.lse[orow] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
-        } else {
-            const int64_t prow = (static_cast<int64_t>(it.slot) * p.hk + kvh) * p.rows + row;
-            p.part_o[prow * D + d] = O;
-            if (d == 0) p.part_ml[prow] = make_float2(M, Ls);
-        }
-    }
+    merge_and_store<NW, RC, D>(p, it, kvh, row0, sm_m, sm_l, sm_o);
 }
 
 template <int D, int RC, bool BF16>

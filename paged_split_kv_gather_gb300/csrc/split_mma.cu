@@ -1,0 +1,41 @@
+// split_mma.cu -- instantiations of the tensor-core split kernel (head_dim 64, 128, 192).
+#include "split_mma_kernel.cuh"
+
+namespace fdec {
+
+cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int head_dim,
+                             bool bf16, dim3 grid, cudaStream_t s, bool launch) {
+    switch (head_dim) {
+        case 64:
+            return bf16 ? launch_split_mma_one<64, true>(p, tk, tv, grid, s, launch)
+                        : launch_split_mma_one<64, false>(p, tk, tv, grid, s, launch);
+        case 128:
+            return bf16 ? launch_split_mma_one<128, true>(p, tk, tv, grid, s, launch)
+                        : launch_split_mma_one<128, false>(p, tk, tv, grid, s, launch);
+        case 192:
+            return bf16 ? launch_split_mma_one<192, true>(p, tk, tv, grid, s, launch)
+                        : launch_split_mma_one<192, false>(p, tk, tv, grid, s, launch);
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
+size_t split_mma_smem_bytes(int head_dim) {
+    switch (head_dim) {
+        case 64: return MmaLayout<64>::SMEM;
+        case 128: return MmaLayout<128>::SMEM;
+        case 192: return MmaLayout<192>::SMEM;
+        default: return 0;
+    }
+}
+
+int split_mma_threads(int head_dim) {
+    switch (head_dim) {
+        case 64: return MmaLayout<64>::THREADS;
+        case 128: return MmaLayout<128>::THREADS;
+        case 192: return MmaLayout<192>::THREADS;
+        default: return 0;
+    }
+}
+
+}  // namespace fdec

@@ -66,7 +66,7 @@ def test_split_path_is_planned_at_every_length_across_the_2048_boundary():
     for length in (1900, 2000, 2048, 2049, 2100, 3000, 4800, 4864, 8192, 32768, 131072, 262144):
         p = _plan([length], num_qo_heads=32, num_kv_heads=4, page_size=64)
         info = fd.fdec_plan_get_info(p)
-        assert info["path"] == fd.FDEC_PATH_SIMT
+        assert info["path"] == fd.FDEC_PATH_MMA  # tensor-core split kernel by default for head_dim 128
         units = -(-length // 64) * 4
         assert info["num_split_ctas"] >= min(units, 152) // 2, (length, info)  # the grid fills the SMs
         if info["max_splits"] > 1:
@@ -98,6 +98,17 @@ def test_auto_plan_balances_ragged_batches():
     nb = np.maximum(1, -(-lens // 64))
     assert np.array_equal(splits, -(-nb // C))
     assert info["num_items"] == int(splits.sum())
+
+
+def test_path_selection():
+    assert fd.fdec_plan_get_info(_plan([100], path=fd.FDEC_PATH_SIMT))["path"] == fd.FDEC_PATH_SIMT
+    for d in (64, 128, 192):
+        assert fd.fdec_plan_get_info(_plan([100], head_dim=d))["path"] == fd.FDEC_PATH_MMA
+    for d in (256, 512):
+        assert fd.fdec_plan_get_info(_plan([100], head_dim=d))["path"] == fd.FDEC_PATH_SIMT
+    with pytest.raises(fd.FdecError) as ei:
+        _plan([100], head_dim=256, path=fd.FDEC_PATH_MMA)
+    assert ei.value.status_name == "FDEC_ERR_UNSUPPORTED"
 
 
 def test_row_groups_cover_all_query_rows():

@@ -86,6 +86,36 @@ def test_multi_token_prefill_chunk_sampled_rows():
     _check(w, rows=rows)
 
 
+# ------------------------------------------------------------------ both split kernels
+
+PATHS = [fd.FDEC_PATH_SIMT, fd.FDEC_PATH_MMA]
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("case", ["tiny", "gqa", "L2049", "L131072", "spec4", "spec8", "peaked"])
+def test_fp32_simt_and_tensor_core_kernels(path, case):
+    w = {"tiny": lambda: W.tiny(device="cuda"),
+         "gqa": lambda: W.batched_gqa(device="cuda"),
+         "L2049": lambda: W.long_context(2049, device="cuda"),
+         "L131072": lambda: W.long_context(131072, device="cuda"),
+         "spec4": lambda: W.multi_token(4, device="cuda"),
+         "spec8": lambda: W.multi_token(8, device="cuda"),
+         "peaked": lambda: W.long_context(4800, device="cuda", peaked=True)}[case]()
+    (e_out, e_lse), pd = _check(w, path=path)
+    assert pd.info["path"] == path
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("page_size", [1, 4, 16, 128])
+def test_both_kernels_small_and_large_pages_with_nan_guard(path, page_size):
+    w = W.make(3, 2, 16, 4, 128, page_size, [5, 333, 1000], dtype="bf16", device="cuda", seed=page_size,
+               causal=True, nan_guard=True, pool_pages=2 * (1000 // page_size + 8))
+    out, lse, pd = gpu_run(w, path=path, blocks_per_split=3)
+    assert torch.isfinite(out).all()
+    ro, rl = oracle_run(w.to("cpu"))
+    assert_parity(out.cpu(), lse.cpu(), ro, rl, f"path {path} page {page_size}")
+
+
 # ------------------------------------------------------------------ plans and reductions
 
 @pytest.mark.parametrize("bps,fanin", [(1, 0), (1, 4), (3, 2), (7, 0), (10**6, 0)])
