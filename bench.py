@@ -237,16 +237,18 @@ def _run_fdec(args):
             ln = torch.as_tensor(ws.seq_lens, device=dev)
             for _ in range(3):
                 pds.run(ws.q, ws.k, ws.v, tb, ln, out, lse, scale=ws.scale)
-            times = []
-            for _ in range(args.sweep_calls):
-                torch.sum(flush)  # read 256 MB: the L2 is left full of clean, unrelated lines
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
+            # All calls are enqueued before one final synchronise, so the device
+            # never waits on the host between a call's two events; each call
+            # follows a 256 MB read that evicts the L2.
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.sweep_calls)]
+            for a, b in evs:
+                torch.sum(flush)
                 a.record()
                 pds.run(ws.q, ws.k, ws.v, tb, ln, out, lse, scale=ws.scale)
                 b.record()
-                b.synchronize()
-                times.append(a.elapsed_time(b) * 1e3)
+            torch.cuda.synchronize()
+            times = [a.elapsed_time(b) * 1e3 for a, b in evs]
             us = float(np.median(times))
             gbs = ws.kv_bytes / (us * 1e-6) / 1e9
             sweep.append({"kv_len": length, "us_per_call": round(us, 2), "us_min": round(min(times), 2),

@@ -89,7 +89,7 @@ enum { FDEC_PATH_AUTO = 0, FDEC_PATH_SIMT = 1, FDEC_PATH_MMA = 2 };
 /* Plan options; pass NULL for the defaults (all fields 0). */
 typedef struct {
     int blocks_per_split;  /* 64-token blocks per split; 0 = auto; 1 = one partial per block */
-    int reducer_fanin;     /* partials merged per reduction task; 0 = auto (64); >= 2 */
+    int reducer_fanin;     /* partials merged per reduction task; 0 = auto (256); >= 2 */
     int path;              /* FDEC_PATH_AUTO (tensor cores where built, else SIMT), _SIMT (fp32 FMA),
                               _MMA (tensor cores; head_dim 64, 128, 192) */
     int num_sms;           /* 0 = query the current device; > 0 plans without a device */

@@ -356,7 +356,7 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
     // why); the fp32 SIMT kernel on request and for head_dim 256 / 512.
     p->path = (o.path == FDEC_PATH_SIMT || (o.path == FDEC_PATH_AUTO && !mma_ok)) ? FDEC_PATH_SIMT : FDEC_PATH_MMA;
     p->num_sms = num_sms;
-    p->fanin = o.reducer_fanin > 0 ? o.reducer_fanin : 64;
+    p->fanin = o.reducer_fanin > 0 ? o.reducer_fanin : 256;
     if (p->path == FDEC_PATH_MMA) {
         p->rc = kMmaRows;
     } else {

@@ -289,6 +289,8 @@ split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUte
 
     // ---------------------------------------------------------------------- epilogue
     named_barrier(1, NW * 32);  // every consumer is done with the stage buffers
+    // The reduction (launched as a programmatic dependent) may start its launch now.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     float* sm_m = reinterpret_cast<float*>(stages);  // [NW][RC]
     float* sm_l = sm_m + NW * RC;                     // [NW][RC]
     float* sm_o = sm_l + NW * RC;                     // [NW][RC][D]
