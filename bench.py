@@ -58,7 +58,7 @@ def _kernel_source_hash() -> str:
 def _traffic_from_profile(workload: str):
     """DRAM bytes per launch of the split kernel from the committed ncu summary,
     only while the kernel sources are the ones that summary was taken from."""
-    path = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
+    path = os.path.join(ROOT, "profiles", "split_kernel_traffic.txt")
     if not os.path.exists(path):
         return None
     with open(path) as f:
