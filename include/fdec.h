@@ -201,6 +201,32 @@ fdec_status fdec_plan_set_split_event(fdec_plan_t plan, cudaEvent_t event);
 fdec_status fdec_read_device_errors(fdec_plan_t plan, void* workspace, uint32_t* flags, int clear,
                                     cudaStream_t stream);
 
+/*
+ * fdec_run without any workspace from the caller (the pages have no
+ * counterpart: this is a convenience of this library).  For callers that
+ * cannot allocate device memory at all, e.g. a plug-in inside a program whose
+ * memory pool owns the whole device, or a loop that must never call
+ * cudaMalloc because it may synchronise the device.  Inputs and outputs are
+ * as for fdec_run; the partials and work lists live in a 16 MiB array built
+ * into the library, which every GPU that loads the library keeps until the
+ * process exits.  A plan whose workspace_bytes exceeds 16 MiB is rejected
+ * with FDEC_ERR_WORKSPACE (use fdec_run with your own workspace).
+ *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - Each call copies the plan's work lists into the array on `stream`
+ *     (this also clears the device error word); the plan needs no upload.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (other
+ *     streams, other threads) race and corrupt each other's results.
+ *   - Device error bits land in the array and are not reported; use fdec_run
+ *     and fdec_read_device_errors where they matter.
+ */
+fdec_status fdec_run_static_workspace(fdec_plan_t plan, const void* q, int64_t q_stride_tok,
+                                      int64_t q_stride_head, fdec_kv_desc k, fdec_kv_desc v,
+                                      const int32_t* page_table, int64_t page_table_stride,
+                                      const int32_t* seq_lens_dev, float scale, float* out, float* lse,
+                                      cudaStream_t stream);
+
 /* Message of the last failure on this thread ("" if none). */
 const char* fdec_last_error(void);
 

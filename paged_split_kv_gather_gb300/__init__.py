@@ -20,7 +20,7 @@ __all__ = [
     "FdecError", "KVDesc", "Plan", "PlanInfo", "fdec_plan", "fdec_plan_upload", "fdec_run",
     "fdec_merge_states", "fdec_plan_destroy", "fdec_plan_get_info", "fdec_plan_get_splits",
     "fdec_plan_set_split_event", "fdec_read_device_errors", "fdec_last_error", "fdec_version",
-    "kv_desc", "library_path", "PagedDecode", "EXPORTED_SYMBOLS",
+    "fdec_run_static_workspace", "kv_desc", "library_path", "PagedDecode", "EXPORTED_SYMBOLS",
     "FDEC_F16", "FDEC_BF16", "FDEC_PATH_AUTO", "FDEC_PATH_SIMT", "FDEC_PATH_MMA",
     "DEVERR_PAGE_ID", "DEVERR_SEQ_LEN", "DEVERR_TIMEOUT",
 ]
@@ -42,7 +42,7 @@ STATUS_NAMES = {
 EXPORTED_SYMBOLS = (
     "fdec_plan", "fdec_plan_upload", "fdec_run", "fdec_merge_states", "fdec_plan_destroy",
     "fdec_plan_get_info", "fdec_plan_get_splits", "fdec_plan_set_split_event",
-    "fdec_read_device_errors", "fdec_last_error", "fdec_version",
+    "fdec_read_device_errors", "fdec_last_error", "fdec_version", "fdec_run_static_workspace",
 )
 
 
@@ -104,6 +104,9 @@ def _load():
         lib.fdec_plan_upload.argtypes = [P, P, P]
         lib.fdec_run.restype = I
         lib.fdec_run.argtypes = [P, P, I64, I64, KVDesc, KVDesc, P, I64, P, ctypes.c_float, P, P, P, P]
+        lib.fdec_run_static_workspace.restype = I
+        lib.fdec_run_static_workspace.argtypes = [P, P, I64, I64, KVDesc, KVDesc, P, I64, P, ctypes.c_float, P,
+                                                  P, P]
         lib.fdec_merge_states.restype = I
         lib.fdec_merge_states.argtypes = [P, P, I, I, I, P, P, P]
         lib.fdec_plan_destroy.restype = I
@@ -256,6 +259,22 @@ def fdec_run(plan: Plan, q, k, v, page_table, seq_lens, out, lse, workspace, sca
                             page_table.stride(0), seq_lens.data_ptr(), sc, out.data_ptr(),
                             None if lse is None else lse.data_ptr(), workspace.data_ptr(),
                             _stream_handle(stream)))
+
+
+def fdec_run_static_workspace(plan: Plan, q, k, v, page_table, seq_lens, out, lse, scale: Optional[float] = None,
+                              stream=None) -> None:
+    """fdec_run with the library's built-in workspace: no device allocation by anyone (see fdec.h)."""
+    kd = k if isinstance(k, KVDesc) else kv_desc(k)
+    vd = v if isinstance(v, KVDesc) else kv_desc(v)
+    if not out.is_contiguous() or (lse is not None and not lse.is_contiguous()):
+        raise ValueError("out and lse must be contiguous")
+    tok, head = _q_strides(q)
+    if page_table.stride(1) != 1:
+        raise ValueError("page_table rows must be contiguous")
+    sc = 1.0 / math.sqrt(plan.meta["head_dim"]) if scale is None else float(scale)
+    _check(_load().fdec_run_static_workspace(plan.handle, q.data_ptr(), tok, head, kd, vd, page_table.data_ptr(),
+                                             page_table.stride(0), seq_lens.data_ptr(), sc, out.data_ptr(),
+                                             None if lse is None else lse.data_ptr(), _stream_handle(stream)))
 
 
 def fdec_merge_states(o, lse, o_out, lse_out=None, stream=None) -> None:

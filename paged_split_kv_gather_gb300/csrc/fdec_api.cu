@@ -698,3 +698,66 @@ fdec_status fdec_merge_states(const float* o, const float* lse, int n_states, in
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// A run that allocates nothing, not even a caller-owned workspace.
+//
+// Some callers cannot allocate device memory at all: a plug-in loaded into a
+// host program whose memory pool owns the whole device, or a latency-critical
+// loop where a cudaMalloc (which may synchronise the device) is not allowed.
+// For them the partials and work lists live in one fixed array compiled into
+// this library.  Every GPU that loads the library keeps the array until the
+// process exits.
+namespace {
+
+constexpr size_t kStaticWorkspaceBytes = size_t(16) << 20;  // 16 MiB
+
+__device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
+
+std::mutex g_static_mutex;
+void* g_static_address[64] = {};  // device address of the array, per device
+
+}  // namespace
+
+extern "C" fdec_status fdec_run_static_workspace(fdec_plan_t p, const void* q, int64_t q_stride_tok,
+                                                 int64_t q_stride_head, fdec_kv_desc k, fdec_kv_desc v,
+                                                 const int32_t* page_table, int64_t page_table_stride,
+                                                 const int32_t* seq_lens_dev, float scale, float* out, float* lse,
+                                                 cudaStream_t stream) {
+    if (p == nullptr) return fail(FDEC_ERR_INVALID_ARG, "null plan");
+    if (p->ws_bytes > kStaticWorkspaceBytes)
+        return fail(FDEC_ERR_WORKSPACE, "this plan needs " + std::to_string(p->ws_bytes) +
+                                            " bytes of workspace but the built-in array holds " +
+                                            std::to_string(kStaticWorkspaceBytes) +
+                                            "; use fdec_run with a workspace of your own");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(FDEC_ERR_UNSUPPORTED, "device index above 63");
+    void* ws = nullptr;
+    {
+        // Once per device, with that device current: the array's device address.
+        // In host code the array's name is only a host-side stand-in.
+        std::lock_guard<std::mutex> lock(g_static_mutex);
+        if (g_static_address[dev] == nullptr) {
+            void* addr = nullptr;
+            e = cudaGetSymbolAddress(&addr, g_static_workspace);
+            if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress of the built-in workspace");
+            g_static_address[dev] = addr;
+        }
+        ws = g_static_address[dev];
+    }
+    // The work lists and capacities go in front; the device error word at the
+    // start of this image is zero, so every call starts with a clear word.
+    // The partials need no clearing: each is written before it is read.
+    e = cudaMemcpyAsync(ws, p->meta.data(), p->meta_bytes, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "copying the plan into the built-in workspace");
+    // fdec_run checks the workspace against the plan's uploaded buffer: point
+    // that at the array for this call only, then give the caller's back.
+    void* saved = p->uploaded;
+    p->uploaded = ws;
+    const fdec_status st = fdec_run(p, q, q_stride_tok, q_stride_head, k, v, page_table, page_table_stride,
+                                    seq_lens_dev, scale, out, lse, ws, stream);
+    p->uploaded = saved;
+    return st;
+}
