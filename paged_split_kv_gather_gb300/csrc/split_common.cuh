@@ -26,10 +26,11 @@ __device__ __forceinline__ void static_for(F&& f) {
     }
 }
 
-template <int D>
+template <int D, int TOK = kStageTokens>
 struct StageGeom {
+    static constexpr int TOKENS = TOK;                         // token rows per stage
     static constexpr int REGIONS = D / 64;
-    static constexpr int REGION_BYTES = kStageTokens * 128;  // 32 rows x 128 B
+    static constexpr int REGION_BYTES = TOK * 128;             // TOK rows x 128 B
     static constexpr int HALF_BYTES = REGIONS * REGION_BYTES;  // K (or V) of one stage
     static constexpr int STAGE_BYTES = 2 * HALF_BYTES;         // K regions then V regions
 };
@@ -39,6 +40,7 @@ struct ItemRange {
     int L, tok_begin, tok_end, n_stage;
 };
 
+template <int TOK = kStageTokens>
 __device__ __forceinline__ ItemRange item_range(const SplitParams& p, const WorkItem& it) {
     int L = p.seq_lens[it.seq];
     const int cap = p.capacity[it.seq];
@@ -50,7 +52,7 @@ __device__ __forceinline__ ItemRange item_range(const SplitParams& p, const Work
     r.L = L;
     r.tok_begin = it.block_begin * kBlockTokens;
     r.tok_end = min(it.block_end * kBlockTokens, L);
-    r.n_stage = r.tok_end > r.tok_begin ? (r.tok_end - r.tok_begin + kStageTokens - 1) / kStageTokens : 0;
+    r.n_stage = r.tok_end > r.tok_begin ? (r.tok_end - r.tok_begin + TOK - 1) / TOK : 0;
     return r;
 }
 
@@ -69,12 +71,13 @@ __device__ __forceinline__ void init_stage_barriers(uint64_t* full, uint64_t* em
     fence_mbar_init();
 }
 
-// The producer warp: fills stage i into slot i % S once the slot is released.
-template <int D, int S>
+// The producer warp: fills stage i (TOK tokens) into slot i % S once the slot is released.
+template <int D, int S, int TOK = kStageTokens>
 __device__ void produce_stages(const SplitParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv, uint64_t* full,
                                uint64_t* empty, uint8_t* stages, int b, int kvh, const ItemRange& ir,
                                bool tma_mode) {
-    using G = StageGeom<D>;
+    using G = StageGeom<D, TOK>;
+    static_assert(TOK % 32 == 0 && TOK <= 256, "stage rows");
     const int lane = threadIdx.x & 31;
     const int tok_begin = ir.tok_begin, tok_end = ir.tok_end, n_stage = ir.n_stage;
     if (n_stage == 0) return;
@@ -83,10 +86,10 @@ __device__ void produce_stages(const SplitParams& p, const CUtensorMap* tmk, con
     int issued = 0;
     bool ok = true;
     if (tma_mode) {
-        // Boxes of BR token rows, NB boxes per 32-token stage; the page id of
-        // box n is held by lane n % 32, one group of 32 boxes ahead.
-        const int BR = min(1 << p.page_shift, kStageTokens);
-        const int NB = kStageTokens / BR;
+        // Boxes of BR token rows, NB boxes per stage; the page id of box n is
+        // held by lane n % 32, one group of 32 boxes ahead.
+        const int BR = min(1 << p.page_shift, TOK);
+        const int NB = TOK / BR;
         const int n_box = (tok_end - tok_begin + BR - 1) / BR;
         const uint32_t box_bytes = static_cast<uint32_t>(BR) * 2u * (2u * D);  // K and V
         auto box_page = [&](int n) -> int {
@@ -153,23 +156,27 @@ __device__ void produce_stages(const SplitParams& p, const CUtensorMap* tmk, con
                     break;
                 }
             }
-            const int t_lane = tok_begin + i * kStageTokens + lane;
-            const bool in_range = t_lane < tok_end;
-            const int my_page = in_range ? __ldg(pt + (t_lane >> p.page_shift)) : -1;
-            const bool valid = in_range && my_page >= 0 && my_page < p.k_pages && my_page < p.v_pages;
-            if (in_range && !valid) atomicOr(p.err, FDEC_DEVERR_PAGE_ID);
             uint8_t* sbase = stages + s * G::STAGE_BYTES;
-            for (int idx = lane; idx < kStageTokens * CHUNKS; idx += 32) {
-                const int row = idx / CHUNKS;
-                const int c = idx - row * CHUNKS;
-                const int page = __shfl_sync(0xffffffffu, my_page, row);
-                const bool ok_row = __shfl_sync(0xffffffffu, valid, row);
-                if (ok_row) {
-                    const int slot = (tok_begin + i * kStageTokens + row) & page_mask;
-                    const uint32_t off = (c >> 3) * G::REGION_BYTES + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-                    cp_async_16(smem_addr(sbase + off), p.k_base + page * p.k_sp + kvh * p.k_sh + slot * p.k_st + c * 16);
-                    cp_async_16(smem_addr(sbase + G::HALF_BYTES + off),
-                                p.v_base + page * p.v_sp + kvh * p.v_sh + slot * p.v_st + c * 16);
+            for (int rb = 0; rb < TOK; rb += 32) {  // 32 rows at a time: lane = row for the page lookup
+                const int t_lane = tok_begin + i * TOK + rb + lane;
+                const bool in_range = t_lane < tok_end;
+                const int my_page = in_range ? __ldg(pt + (t_lane >> p.page_shift)) : -1;
+                const bool valid = in_range && my_page >= 0 && my_page < p.k_pages && my_page < p.v_pages;
+                if (in_range && !valid) atomicOr(p.err, FDEC_DEVERR_PAGE_ID);
+                for (int idx = lane; idx < 32 * CHUNKS; idx += 32) {
+                    const int r32 = idx / CHUNKS;
+                    const int c = idx - r32 * CHUNKS;
+                    const int page = __shfl_sync(0xffffffffu, my_page, r32);
+                    const bool ok_row = __shfl_sync(0xffffffffu, valid, r32);
+                    if (ok_row) {
+                        const int row = rb + r32;
+                        const int slot = (tok_begin + i * TOK + row) & page_mask;
+                        const uint32_t off = (c >> 3) * G::REGION_BYTES + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+                        cp_async_16(smem_addr(sbase + off),
+                                    p.k_base + page * p.k_sp + kvh * p.k_sh + slot * p.k_st + c * 16);
+                        cp_async_16(smem_addr(sbase + G::HALF_BYTES + off),
+                                    p.v_base + page * p.v_sp + kvh * p.v_sh + slot * p.v_st + c * 16);
+                    }
                 }
             }
             cp_async_arrive_noinc(smem_addr(&full[i % (2 * S)]));
@@ -199,19 +206,19 @@ __device__ __forceinline__ bool wait_stage(uint64_t* full, int i) {
 }
 
 // A partial (last) stage: rows past the sequence end hold whatever the page
-// held; zero its V rows [nv, 32) so that a fixed-size p.V loop adds 0 * 0.
-template <int D>
-__device__ __forceinline__ void zero_v_tail(uint8_t* stage, int nv) {
-    using G = StageGeom<D>;
-    const int lane = threadIdx.x & 31;
+// held; zero its V rows [nv, TOK) so that a fixed-size p.V loop adds 0 * 0.
+// `threads` consecutive threads (from `tid` 0) share the work.
+template <int D, int TOK = kStageTokens>
+__device__ __forceinline__ void zero_v_tail(uint8_t* stage, int nv, int tid = threadIdx.x & 31, int threads = 32) {
+    using G = StageGeom<D, TOK>;
     uint8_t* vrows = stage + G::HALF_BYTES;
-    for (int idx = lane; idx < (kStageTokens - nv) * G::REGIONS * 8; idx += 32) {
+    for (int idx = tid; idx < (TOK - nv) * G::REGIONS * 8; idx += threads) {
         const int row = nv + idx / (G::REGIONS * 8);
         const int rem = idx % (G::REGIONS * 8);
         *reinterpret_cast<uint4*>(vrows + (rem >> 3) * G::REGION_BYTES + row * 128 + (rem & 7) * 16) =
             make_uint4(0u, 0u, 0u, 0u);
     }
-    __syncwarp();
+    if (threads == 32) __syncwarp();
 }
 
 // Epilogue, after every consumer has written its state to the scratch
