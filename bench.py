@@ -45,6 +45,78 @@ def _peaks():
     return 6800.0, "fallback"
 
 
+def _bf16_peak():
+    """Dense bf16 TFLOP/s: the burst figure (a kernel timed alone, per call)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def _attention_flops(w) -> float:
+    """Algorithmic FLOPs of one call: 2 D per visible (query row, token) pair for
+    q.K and 2 D for p.V (bottom-right causal visibility)."""
+    total = 0
+    for b in range(w.batch):
+        L = int(w.seq_lens[b])
+        for i in range(w.q_len):
+            n = min(L, L - w.q_len + i + 1) if w.causal else L
+            total += max(n, 0)
+    return 4.0 * w.head_dim * w.num_qo_heads * total
+
+
+def _dense_query(dev, calls, hbm_peak):
+    """Multi-token queries over the paged cache (batch 4, 32/8 heads, D 128, bf16,
+    page 16, prefix 8192 + q_len, causal): q_len 4 and 8 (speculative decode) and
+    2048 (a prefill chunk, the tcgen05 path; also timed on the 16-row kernel)."""
+    import torch
+
+    import paged_split_kv_gather_gb300 as fd
+    from paged_split_kv_gather_gb300 import workloads as W
+
+    tflops_peak, tflops_kind = _bf16_peak()
+    names = {fd.FDEC_PATH_SIMT: "simt", fd.FDEC_PATH_MMA: "mma", fd.FDEC_PATH_TC: "tcgen05"}
+    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    res = []
+    for q_len in (4, 8, 2048):
+        w = W.multi_token(q_len, device=dev)
+        table = torch.as_tensor(w.page_table, device=dev)
+        lens = torch.as_tensor(w.seq_lens, device=dev)
+        out = torch.empty((w.batch, q_len, w.num_qo_heads, w.head_dim), device=dev)
+        lse = torch.empty((w.batch, q_len, w.num_qo_heads), device=dev)
+        flops = _attention_flops(w)
+        paths = [fd.FDEC_PATH_AUTO] + ([fd.FDEC_PATH_MMA] if q_len >= 64 else [])
+        for path in paths:
+            pd = fd.PagedDecode(w.seq_lens, q_len, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim,
+                                w.dtype, w.causal, device=dev, path=path)
+            for _ in range(3):
+                pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale)
+            n = calls if q_len < 64 else max(5, calls // 5)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            torch.cuda._sleep(int(n * 2e5))  # the host runs ahead: no host gap between a call's events
+            for a, b in evs:
+                torch.sum(flush)
+                a.record()
+                pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale)
+                b.record()
+            torch.cuda.synchronize()
+            assert pd.device_errors() == 0
+            us = float(np.median([a.elapsed_time(b) * 1e3 for a, b in evs]))
+            tf = flops / (us * 1e-6) / 1e12
+            gbs = w.kv_bytes / (us * 1e-6) / 1e9
+            res.append({"q_len": q_len, "path": names[pd.info["path"]], "us_per_call": round(us, 2),
+                        "TFLOP_per_s": round(tf, 1), "frac_of_bf16_peak": round(tf / tflops_peak, 4),
+                        "GB_per_s": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm_peak, 4),
+                        "launches": int(pd.info["launches"]), "split_ctas": int(pd.info["num_split_ctas"])})
+            del pd
+        del w, table, lens, out, lse
+    del flush
+    return {"workload": "multi_token: batch 4, 32/8 heads, head_dim 128, bf16, page 16, KV 8192 + q_len, causal",
+            "bf16_peak_tflops": tflops_peak, "bf16_peak_kind": tflops_kind,
+            "flops": "4 x head_dim per visible (query head, query token, key token)", "points": res}
+
+
 def _kernel_source_hash() -> str:
     csrc = os.path.join(ROOT, "paged_split_kv_gather_gb300", "csrc")
     h = hashlib.sha256()
@@ -169,27 +241,41 @@ def _run_fdec(args):
         step()
     torch.cuda.synchronize()
 
-    # ---- timed region: exactly K steps, barrier + synchronize on both sides
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for ev in starts + mids + ends:  # create the CUDA events before the timed region
-        ev.record(stream)
+    # ---- timed region: exactly K steps back to back, barrier + synchronize on
+    # both sides, one event pair around the whole region (an event between the
+    # split kernel and the reduction would stop the reduction's programmatic
+    # early launch, so none is recorded here).
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        t_start.record(stream)
         for i in range(args.steps):
-            starts[i].record(stream)
-            fd.fdec_plan_set_split_event(pd.plan, mids[i])
             step()
-            ends[i].record(stream)
+        t_end.record(stream)
         torch.cuda.synchronize()
-    fd.fdec_plan_set_split_event(pd.plan, None)
     if world > 1:
         dist.barrier()
-    total_ms = starts[0].elapsed_time(ends[-1])
+    total_ms = t_start.elapsed_time(t_end)
+
+    # ---- the split kernel alone, for the roofline: the same K steps again with
+    # events around each split launch (on the launching stream).
+    n_roof = min(args.steps, 2000)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_roof)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(n_roof)]
+    for ev in mids:  # created (and marked recorded) here; fdec_run re-records them after each split launch
+        ev.record(stream)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(2e6))  # let the host get ahead of the device
+    for i in range(n_roof):
+        starts[i].record(stream)
+        fd.fdec_plan_set_split_event(pd.plan, mids[i])
+        step()
+    torch.cuda.synchronize()
+    fd.fdec_plan_set_split_event(pd.plan, None)
     split_ms = float(np.mean([s.elapsed_time(m) for s, m in zip(starts, mids)]))
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
@@ -237,9 +323,10 @@ def _run_fdec(args):
             ln = torch.as_tensor(ws.seq_lens, device=dev)
             for _ in range(3):
                 pds.run(ws.q, ws.k, ws.v, tb, ln, out, lse, scale=ws.scale)
-            # All calls are enqueued before one final synchronise, so the device
-            # never waits on the host between a call's two events; each call
-            # follows a 256 MB read that evicts the L2.
+            # All calls are enqueued behind a device-side delay and before one
+            # final synchronise, so the device never waits on the host between a
+            # call's two events; each call follows a 256 MB read that evicts the L2.
+            torch.cuda._sleep(int(args.sweep_calls * 2e5))
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.sweep_calls)]
             for a, b in evs:
@@ -257,6 +344,10 @@ def _run_fdec(args):
             if ws is not w:
                 del pds, ws
         del flush
+
+    dense = None
+    if not args.no_dense:
+        dense = _dense_query(dev, args.sweep_calls, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -299,6 +390,7 @@ def _run_fdec(args):
             "clocks": clocks.summary(),
             "cpu_baseline": cpu,
             "sweep": sweep,
+            "dense_query": dense,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -416,6 +508,7 @@ def main():
     ap.add_argument("--impl", choices=["fdec", "reference"], default="fdec")
     ap.add_argument("--sweep-calls", type=int, default=50)
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-dense", action="store_true", help="skip the multi-token (q_len 4, 8, 2048) points")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=120.0)

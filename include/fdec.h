@@ -84,20 +84,30 @@ typedef struct {
 
 typedef struct fdec_plan_s* fdec_plan_t;
 
-enum { FDEC_PATH_AUTO = 0, FDEC_PATH_SIMT = 1, FDEC_PATH_MMA = 2 };
+/*
+ * Split-kernel paths.  SIMT: fp32 FMA (every head_dim).  MMA: warp-level
+ * tensor-core MMA on 16-row query groups (head_dim 64, 128, 192), the decode
+ * default.  TC: 5th-generation tensor cores (tcgen05, accumulators in tensor
+ * memory) on 128-row query tiles, head_dim 128; chosen by AUTO when q_len x
+ * group >= 64, where attention over the gathered pages is a dense contraction
+ * (speculative-decode and prefill chunks).  Below that the work is bound by
+ * streaming K/V and the 16-row kernels waste no tensor-core tile.
+ */
+enum { FDEC_PATH_AUTO = 0, FDEC_PATH_SIMT = 1, FDEC_PATH_MMA = 2, FDEC_PATH_TC = 3 };
 
 /* Plan options; pass NULL for the defaults (all fields 0). */
 typedef struct {
     int blocks_per_split;  /* 64-token blocks per split; 0 = auto; 1 = one partial per block */
     int reducer_fanin;     /* partials merged per reduction task; 0 = auto (256); >= 2 */
-    int path;              /* FDEC_PATH_AUTO (tensor cores where built, else SIMT), _SIMT (fp32 FMA),
-                              _MMA (tensor cores; head_dim 64, 128, 192) */
+    int path;              /* FDEC_PATH_AUTO (TC when head_dim 128 and q_len x group >= 64, else MMA
+                              where built, else SIMT), _SIMT, _MMA (head_dim 64, 128, 192),
+                              _TC (head_dim 128) */
     int num_sms;           /* 0 = query the current device; > 0 plans without a device */
 } fdec_plan_opts;
 
 /* What a plan decided (for logging, tests and benchmarks). */
 typedef struct {
-    int path;              /* FDEC_PATH_SIMT (fp32 FMA kernel) or FDEC_PATH_MMA (tensor-core kernel) */
+    int path;              /* FDEC_PATH_SIMT, FDEC_PATH_MMA or FDEC_PATH_TC */
     int blocks_per_split;
     int num_items;         /* split work items (each runs for every KV head and row group) */
     int num_split_ctas;    /* CTAs of the split launch */

@@ -21,7 +21,7 @@ __all__ = [
     "fdec_merge_states", "fdec_plan_destroy", "fdec_plan_get_info", "fdec_plan_get_splits",
     "fdec_plan_set_split_event", "fdec_read_device_errors", "fdec_last_error", "fdec_version",
     "fdec_run_static_workspace", "kv_desc", "library_path", "PagedDecode", "EXPORTED_SYMBOLS",
-    "FDEC_F16", "FDEC_BF16", "FDEC_PATH_AUTO", "FDEC_PATH_SIMT", "FDEC_PATH_MMA",
+    "FDEC_F16", "FDEC_BF16", "FDEC_PATH_AUTO", "FDEC_PATH_SIMT", "FDEC_PATH_MMA", "FDEC_PATH_TC",
     "DEVERR_PAGE_ID", "DEVERR_SEQ_LEN", "DEVERR_TIMEOUT",
 ]
 
@@ -29,7 +29,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libfdec.so")
 
 FDEC_F16, FDEC_BF16 = 0, 1
-FDEC_PATH_AUTO, FDEC_PATH_SIMT, FDEC_PATH_MMA = 0, 1, 2
+FDEC_PATH_AUTO, FDEC_PATH_SIMT, FDEC_PATH_MMA, FDEC_PATH_TC = 0, 1, 2, 3
 DEVERR_PAGE_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 
 STATUS_NAMES = {

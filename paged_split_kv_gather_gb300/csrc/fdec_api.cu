@@ -176,13 +176,15 @@ std::vector<int> item_sizes(const std::vector<int>& nblocks, int C) {
     return out;
 }
 
-int choose_blocks_per_split(const std::vector<int>& nblocks, int copies, int slots) {
+// partial_cost: the cost of one partial slot (written by the split kernel and
+// read back by the reduction: 2 x Hk x rows x (4 D + 8) bytes) in the same units.
+int choose_blocks_per_split(const std::vector<int>& nblocks, int copies, int slots, double partial_cost) {
     const int max_nb = std::max(1, *std::max_element(nblocks.begin(), nblocks.end()));
     long long total = 0;
     for (int nb : nblocks) total += std::max(nb, 1);
     // Cost model in units of one 64-token block streamed by one CTA slot: the
-    // LPT makespan of the items, a fixed start-up cost per item, and the extra
-    // reduction launch when any sequence is split.
+    // LPT makespan of the items, a fixed start-up cost per item, the extra
+    // reduction launch when any sequence is split, and the partials' traffic.
     const double per_item = 2.0;
     const double reduce_cost = 4.0;
     std::vector<int> cands;
@@ -198,7 +200,13 @@ int choose_blocks_per_split(const std::vector<int>& nblocks, int copies, int slo
     for (int C : cands) {
         const std::vector<int> sizes = item_sizes(nblocks, C);
         const bool split = sizes.size() > nblocks.size();
-        const double cost = lpt_makespan(sizes, copies, slots, per_item) + (split ? reduce_cost : 0.0);
+        size_t partials = 0;
+        for (int nb : nblocks) {
+            const int n = (std::max(nb, 1) + C - 1) / C;
+            if (n > 1) partials += n;
+        }
+        const double cost = lpt_makespan(sizes, copies, slots, per_item) +
+                            (split ? reduce_cost + partial_cost * static_cast<double>(partials) : 0.0);
         if (cost < best_cost - 1e-9 || (std::fabs(cost - best_cost) <= 1e-9 && C > best)) {
             best_cost = cost;
             best = C;
@@ -211,6 +219,7 @@ cudaError_t dispatch_split(const fdec_plan_s* p, const SplitParams& sp, dim3 gri
     const bool bf16 = p->dtype == FDEC_BF16;
     const CUtensorMap& tk = p->tmap_k;
     const CUtensorMap& tv = p->tmap_v;
+    if (p->path == FDEC_PATH_TC) return launch_split_tc(sp, tk, tv, p->rc / kTcRows, bf16, grid, stream, launch);
     if (p->path == FDEC_PATH_MMA) return launch_split_mma(sp, tk, tv, p->head_dim, bf16, grid, stream, launch);
     switch (p->head_dim) {
         case 64: return launch_split_d64(sp, tk, tv, p->rc, bf16, grid, stream, launch);
@@ -285,7 +294,7 @@ void log_plan(const fdec_plan_s* p) {
                  "blocks_per_split=%d items=%zu max_splits=%d reduce_passes=%zu sms=%d ctas/sm=%d "
                  "workspace=%zu B\n",
                  p->batch, p->q_len, p->hq, p->hk, p->head_dim, p->page_size, p->rows,
-                 p->path == FDEC_PATH_MMA ? "mma" : "simt", p->rc, p->row_groups, p->blocks_per_split,
+                 p->path == FDEC_PATH_TC ? "tc" : (p->path == FDEC_PATH_MMA ? "mma" : "simt"), p->rc, p->row_groups, p->blocks_per_split,
                  p->items.size(), max_s, p->passes.size(), p->num_sms, p->ctas_per_sm, p->ws_bytes);
 }
 
@@ -318,11 +327,14 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
     if (opts != nullptr) o = *opts;
     if (o.blocks_per_split < 0 || o.reducer_fanin < 0 || o.num_sms < 0 || (o.reducer_fanin == 1))
         return fail(FDEC_ERR_INVALID_ARG, "invalid plan options");
-    if (o.path != FDEC_PATH_AUTO && o.path != FDEC_PATH_SIMT && o.path != FDEC_PATH_MMA)
+    if (o.path != FDEC_PATH_AUTO && o.path != FDEC_PATH_SIMT && o.path != FDEC_PATH_MMA && o.path != FDEC_PATH_TC)
         return fail(FDEC_ERR_INVALID_ARG, "invalid path option");
     const bool mma_ok = head_dim == 64 || head_dim == 128 || head_dim == 192;
+    const bool tc_ok = head_dim == 128;
     if (o.path == FDEC_PATH_MMA && !mma_ok)
         return fail(FDEC_ERR_UNSUPPORTED, "the tensor-core path supports head_dim 64, 128 and 192");
+    if (o.path == FDEC_PATH_TC && !tc_ok)
+        return fail(FDEC_ERR_UNSUPPORTED, "the tcgen05 path supports head_dim 128");
     const long long rows_ll = static_cast<long long>(q_len) * (num_qo_heads / num_kv_heads);
     if (rows_ll > (1 << 24)) return fail(FDEC_ERR_UNSUPPORTED, "q_len x group too large");
     for (int b = 0; b < batch; ++b)
@@ -354,17 +366,35 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
     p->causal = (causal != 0 && q_len > 1) ? 1 : 0;
     // Tensor cores by default where the kernel exists (see split_mma_kernel.cuh for
     // why); the fp32 SIMT kernel on request and for head_dim 256 / 512.
-    p->path = (o.path == FDEC_PATH_SIMT || (o.path == FDEC_PATH_AUTO && !mma_ok)) ? FDEC_PATH_SIMT : FDEC_PATH_MMA;
+    // The tcgen05 kernel once a 128-row tile is at least half full.
+    if (o.path == FDEC_PATH_AUTO)
+        p->path = (tc_ok && p->rows >= kTcRows / 2) ? FDEC_PATH_TC : (mma_ok ? FDEC_PATH_MMA : FDEC_PATH_SIMT);
+    else
+        p->path = o.path;
     p->num_sms = num_sms;
     p->fanin = o.reducer_fanin > 0 ? o.reducer_fanin : 256;
-    if (p->path == FDEC_PATH_MMA) {
+    size_t smem = 0;
+    int threads = 0;
+    if (p->path == FDEC_PATH_TC) {
+        // Two 128-row tiles per CTA share each staged K/V block once there are more than 128 rows.
+        const int tiles = p->rows > kTcRows ? 2 : 1;
+        p->rc = kTcRows * tiles;
+        smem = split_tc_smem_bytes(tiles);
+        threads = split_tc_threads(tiles);
+    } else if (p->path == FDEC_PATH_MMA) {
         p->rc = kMmaRows;
+        smem = split_mma_smem_bytes(head_dim);
+        threads = split_mma_threads(head_dim);
     } else {
         p->rc = std::min(next_pow2(p->rows), split_max_rc(head_dim));
+        smem = split_smem_bytes(head_dim, p->rc);
+        threads = split_threads(head_dim);
     }
     p->row_groups = (p->rows + p->rc - 1) / p->rc;
-    const size_t smem = p->path == FDEC_PATH_MMA ? split_mma_smem_bytes(head_dim) : split_smem_bytes(head_dim, p->rc);
-    const int threads = p->path == FDEC_PATH_MMA ? split_mma_threads(head_dim) : split_threads(head_dim);
+    if (p->row_groups > 65535 || num_kv_heads > 65535) {
+        delete p;
+        return fail(FDEC_ERR_UNSUPPORTED, "q_len x group / rows per CTA or num_kv_heads above 65535");
+    }
     p->ctas_per_sm = std::max(1, std::min(static_cast<int>(233472 / (smem + 1024)), 2048 / threads));
 
     p->capacity.assign(seq_lens_host, seq_lens_host + batch);
@@ -375,7 +405,11 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
     }
     const int copies = p->hk * p->row_groups;
     const int slots = num_sms * p->ctas_per_sm;
-    p->blocks_per_split = o.blocks_per_split > 0 ? o.blocks_per_split : choose_blocks_per_split(nblocks, copies, slots);
+    // A block unit streams 64 tokens of K and V (64 x D x 4 bytes) at 1/slots of the machine's bandwidth.
+    const double partial_cost = 2.0 * p->hk * static_cast<double>(p->rows) * (4.0 * head_dim + 8.0) /
+                                (64.0 * head_dim * 4.0 * slots);
+    p->blocks_per_split = o.blocks_per_split > 0 ? o.blocks_per_split
+                                                 : choose_blocks_per_split(nblocks, copies, slots, partial_cost);
     const int C = p->blocks_per_split;
 
     // Work items and level-0 partial slots.
@@ -575,7 +609,7 @@ fdec_status fdec_run(fdec_plan_t p, const void* q, int64_t q_stride_tok, int64_t
         return fail(FDEC_ERR_WORKSPACE, "workspace is not the buffer this plan was uploaded to");
 
     if (p->page_size >= 8 && !(p->maps_valid && same_desc(p->map_k, k) && same_desc(p->map_v, v))) {
-        const int box_rows = std::min(p->page_size, kStageTokens);
+        const int box_rows = std::min(p->page_size, p->path == FDEC_PATH_TC ? kTcStageTokens : kStageTokens);
         fdec_status st = encode_kv_map(&p->tmap_k, k, p->head_dim, p->page_size, p->hk, box_rows, p->k_pos);
         if (st == FDEC_OK) st = encode_kv_map(&p->tmap_v, v, p->head_dim, p->page_size, p->hk, box_rows, p->v_pos);
         if (st != FDEC_OK) {
@@ -654,6 +688,9 @@ fdec_status fdec_run(fdec_plan_t p, const void* q, int64_t q_stride_tok, int64_t
         rp.head_dim = p->head_dim;
         rp.normalized_input = 0;
         rp.src_rows_stride = p->rows;
+        int max_count = 1;
+        for (const ReduceTask& t : p->passes[level]) max_count = std::max(max_count, t.count);
+        rp.warps_per_unit = reduce_warps_per_unit(max_count);
         e = launch_reduce(rp, static_cast<int>(p->passes[level].size()), stream);
         if (e != cudaSuccess) return fail_cuda(e, "launching the reduction");
     }
@@ -687,6 +724,7 @@ fdec_status fdec_merge_states(const float* o, const float* lse, int n_states, in
     rp.head_dim = head_dim;
     rp.normalized_input = 1;
     rp.src_rows_stride = rows;
+    rp.warps_per_unit = reduce_warps_per_unit(n_states);
     ReduceTask single;
     single.seq = 0;
     single.src = 0;

@@ -72,6 +72,7 @@ struct ReduceParams {
     int hk, rows, group, q_len, hq, head_dim;
     int normalized_input;      // 1: sources are normalised (o, lse) states (merge_states)
     int src_rows_stride;       // rows per (slot, kv head) in the source arrays
+    int warps_per_unit;        // 1, 2, 4 or 8 (reduce_warps_per_unit of the largest task)
 };
 
 // Launch the split kernel for head_dim D (defined in split_d<D>.cu); rc is the
@@ -95,11 +96,22 @@ size_t split_mma_smem_bytes(int head_dim);
 int split_mma_threads(int head_dim);
 constexpr int kMmaRows = 16;
 
+// The tcgen05 dense-query split kernel (head_dim 128; `tiles` (1 or 2) 128-row
+// query tiles per CTA, 64-token stages: its tensor maps use boxes of
+// min(page_size, 64) token rows).
+cudaError_t launch_split_tc(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int tiles, bool bf16,
+                            dim3 grid, cudaStream_t s, bool launch);
+size_t split_tc_smem_bytes(int tiles);
+int split_tc_threads(int tiles);
+constexpr int kTcRows = 128;
+constexpr int kTcStageTokens = 64;
+
 // Shared-memory bytes and threads of the split kernel for (D, RC); 0 if not built.
 size_t split_smem_bytes(int head_dim, int rc);
 int split_threads(int head_dim);
 int split_max_rc(int head_dim);
 
+int reduce_warps_per_unit(int max_count);
 cudaError_t launch_reduce(const ReduceParams& p, int num_tasks, cudaStream_t s);
 // One task given by value (p.tasks must be null): used by fdec_merge_states.
 cudaError_t launch_reduce_single(const ReduceParams& p, ReduceTask task, cudaStream_t s);

@@ -1,0 +1,452 @@
+// split_tc_kernel.cuh -- the dense-query split kernel on 5th-generation tensor
+// cores (tcgen05, accumulators in tensor memory), for q_len x group >= 64 rows
+// (speculative-decode and prefill chunks).
+//
+// One CTA: one work item (a run of 64-token blocks) x one KV head x NT tiles of
+// 128 query rows (rows = q positions x heads of the group, flattened).  The NT
+// tiles share every staged K/V block.  With a causal mask the item's token
+// range is clipped to the last token any row of the CTA can see.  Warps:
+//   warp 0      TMA producer: 64-token K/V stages (the shared producer).
+//   warp 1      MMA issuer (one lane), per tile t and block j:
+//                 S_t  = Q_t K^T            M 128 rows, N 64 tokens, K 128 dims  (8 MMAs)
+//                 O_t += P_t,hi V + P_t,lo V  M 128, N 128 dims, K 64 tokens      (2 x 4 MMAs)
+//               Q and K are K-major and V MN-major, 128B-swizzled in shared
+//               memory; S_t, P_t and O_t live in tensor memory.  S_t has two
+//               buffers (block parity); P_t overwrites the S_t it came from (hi
+//               in the first 32 columns, lo in the next 32, two 16-bit values per
+//               column) and is the A operand of the P V products, so P never
+//               goes through shared memory.  S_t of block j + 1 is issued before
+//               the P V products of block j wait for P_t, so it overlaps this
+//               block's softmax, and the tiles take turns with the tensor cores.
+//   warps 2+4t..5+4t  softmax warpgroup of tile t, thread = row = tensor-memory
+//               lane: load the row of S, mask, row max in registers, exp2, and the
+//               row of P split into a bf16/f16 high part and a residual (both
+//               multiplied, so p keeps ~16 significant bits), stored back into
+//               tensor memory.  The lazy rescale of the row of O (only when the
+//               max grew by more than 8 in log2 units; warp-uniform) first waits
+//               for the previous block's P V products.  After the last block:
+//               O, l, m -> one partial of the split, or out / lse.
+// Synchronisation: stage full / empty mbarriers (TMA / commit of the P V MMAs),
+// and per tile s_full[2] (commit of the QK MMAs, per S buffer), p_full[2] (the
+// four softmax warps, per buffer) and o_done (commit of the P V MMAs).  Every
+// wait is bounded.  Ordering of the S / P buffers: the tensor cores execute
+// one thread's MMAs in issue order, so S_t(j + 2), issued after the P V
+// products of block j, overwrites P_t(j) only after they have read it.
+#pragma once
+
+#include "split_common.cuh"
+#include "tc_common.cuh"
+
+namespace fdec {
+
+template <int NT>
+struct TcLayout {
+    static constexpr int D = 128;
+    static constexpr int TM = 128;                 // query rows per tile
+    static constexpr int ROWS = NT * TM;           // query rows per CTA
+    static constexpr int TOK = 64;                 // tokens per stage / S tile
+    using G = StageGeom<D, TOK>;
+    static constexpr int S = NT == 1 ? 6 : 5;      // stages
+    static constexpr int Q_BYTES = TM * D * 2;     // per tile: 2 regions x 128 rows x 128 B
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_STAGES = OFF_Q + NT * Q_BYTES;
+    static constexpr int OFF_BARS = OFF_STAGES + S * G::STAGE_BYTES;
+    static constexpr int NBARS = 3 * S + 5 * NT + 1;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM = OFF_BARS + BAR_BYTES + 1024;  // + alignment slack
+    static constexpr int THREADS = (2 + 4 * NT) * 32;
+    // tensor memory per tile t (base 256 t): S / P buffers at +0 and +64, O at +128
+    static constexpr uint32_t TMEM_COLS = NT == 1 ? 256u : 512u;
+    static_assert(SMEM <= 232448, "shared memory");
+    static_assert(NBARS * 8 + 8 <= BAR_BYTES, "barriers");
+    static_assert(NT == 1 || NT == 2, "tiles per CTA");
+};
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of row r in a 128B-swizzled region of 128-byte rows.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int chunk) {
+    return static_cast<uint32_t>(r * 128 + (((chunk ^ r) & 7) << 4));
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float x, float y) {
+    if constexpr (BF16) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+        const __half2 h = __floats2half2_rn(x, y);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float2 unpack_pair(uint32_t w) {
+    if constexpr (BF16) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    } else {
+        return __half22float2(*reinterpret_cast<const __half2*>(&w));
+    }
+}
+
+template <int NT, bool BF16>
+__global__ void __launch_bounds__(TcLayout<NT>::THREADS, 1)
+split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
+                const __grid_constant__ CUtensorMap tmv) {
+    using Lay = TcLayout<NT>;
+    using G = typename Lay::G;
+    constexpr int S = Lay::S;
+    constexpr int TOK = Lay::TOK;
+    constexpr int D = Lay::D;
+    constexpr float kLn2 = 0.69314718055994530942f;
+    constexpr float kLazyRescale = 8.f;
+
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint8_t* q_tiles = smem + Lay::OFF_Q;
+    uint8_t* stages = smem + Lay::OFF_STAGES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::OFF_BARS);
+    uint64_t* full = bars;            // 2S
+    uint64_t* empty = bars + 2 * S;   // S
+    uint64_t* s_full = bars + 3 * S;  // [NT][2]
+    uint64_t* p_full = s_full + 2 * NT;  // [NT][2]
+    uint64_t* o_done = p_full + 2 * NT;  // [NT]
+    uint64_t* mma_fin = o_done + NT;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_fin + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // Row tiles vary fastest over the launch, so the CTAs resident at one time
+    // share a few (sequence, KV head) streams and re-read them from L2.
+    const unsigned lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    const int cta_tile = static_cast<int>(lin % gridDim.z);
+    const int kvh = static_cast<int>((lin / gridDim.z) % gridDim.y);
+    const WorkItem it = p.items[lin / (gridDim.z * gridDim.y)];
+    const int b = it.seq;
+    const int row0 = cta_tile * Lay::ROWS;
+
+    ItemRange ir = item_range<TOK>(p, it);
+    if (p.causal) {  // no row of this CTA sees past L - Q + (its last q position)
+        const int last_row = min(row0 + Lay::ROWS, p.rows) - 1;
+        const int lim_max = ir.L - p.q_len + last_row / p.group;
+        ir.tok_end = min(ir.tok_end, lim_max + 1);
+        ir.n_stage = ir.tok_end > ir.tok_begin ? (ir.tok_end - ir.tok_begin + TOK - 1) / TOK : 0;
+    }
+    const int n_tiles = ir.n_stage;
+    const bool tma_mode = p.page_shift >= 3;
+
+    if (threadIdx.x == 0) {
+        init_stage_barriers<S>(full, empty, tma_mode);
+#pragma unroll
+        for (int i = 0; i < 2 * NT; ++i) {
+            mbar_init(smem_addr(&s_full[i]), 1);
+            mbar_init(smem_addr(&p_full[i]), 4);
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) mbar_init(smem_addr(&o_done[t]), 1);
+        mbar_init(smem_addr(mma_fin), 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0 && tma_mode) {
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmv);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), Lay::TMEM_COLS);
+        tmem_relinquish();
+    }
+    // Q tiles: K-major, 128B-swizzled (two 64-dim regions per tile); absent rows are zero.
+    const bool q_vec = ((reinterpret_cast<uintptr_t>(p.q) | static_cast<uintptr_t>(p.q_stride_tok * 2) |
+                         static_cast<uintptr_t>(p.q_stride_head * 2)) & 15u) == 0;
+    for (int idx = threadIdx.x; idx < Lay::ROWS * (D / 8); idx += Lay::THREADS) {
+        const int r = idx / (D / 8);
+        const int c = idx - r * (D / 8);  // 16-byte chunk of the row
+        const int row = row0 + r;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < p.rows) {
+            const int qi = row / p.group;
+            const int h = kvh * p.group + (row - qi * p.group);
+            const uint16_t* src = p.q + static_cast<int64_t>(b * p.q_len + qi) * p.q_stride_tok +
+                                  static_cast<int64_t>(h) * p.q_stride_head + c * 8;
+            if (q_vec) {
+                v = __ldg(reinterpret_cast<const uint4*>(src));
+            } else {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w[e] = static_cast<uint32_t>(src[2 * e]) | (static_cast<uint32_t>(src[2 * e + 1]) << 16);
+                v = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+        const int t = r / Lay::TM, rt = r - t * Lay::TM;
+        *reinterpret_cast<uint4*>(q_tiles + t * Lay::Q_BYTES + (c >> 3) * (Lay::TM * 128) + sw128_offset(rt, c & 7)) = v;
+    }
+    fence_proxy_async_shared();  // generic writes of Q, read by the tensor cores
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        produce_stages<D, S, TOK>(p, &tmk, &tmv, full, empty, stages, b, kvh, ir, tma_mode);
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n_tiles > 0) {
+            bool ok = true;
+            const uint32_t i_qk = idesc_f16(128, TOK, BF16, false, false);
+            const uint32_t i_pv = idesc_f16(128, D, BF16, false, true);
+            auto issue_qk = [&](int t, int j) {
+                const uint32_t q_addr = smem_addr(q_tiles + t * Lay::Q_BYTES);
+                const uint32_t k_addr = smem_addr(stages + (j % S) * G::STAGE_BYTES);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint64_t ad = smem_desc_sw128(q_addr + (ks >> 2) * (Lay::TM * 128) + (ks & 3) * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(k_addr + (ks >> 2) * G::REGION_BYTES + (ks & 3) * 32, 16, 1024);
+                    tc_mma_f16(tmem + 256 * t + 64 * (j & 1), ad, bd, i_qk, ks > 0);
+                }
+                tc_commit(smem_addr(&s_full[2 * t + (j & 1)]));
+            };
+            auto issue_pv = [&](int t, int j) {
+                const uint32_t v_addr = smem_addr(stages + (j % S) * G::STAGE_BYTES + G::HALF_BYTES);
+                const uint32_t p_tm = tmem + 256 * t + 64 * (j & 1);
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                    for (int ks = 0; ks < TOK / 16; ++ks) {
+                        const uint64_t bd = smem_desc_sw128(v_addr + ks * 16 * 128, G::REGION_BYTES, 1024);
+                        tc_mma_f16_ts(tmem + 256 * t + 128, p_tm + 32 * part + 8 * ks, bd, i_pv,
+                                      j > 0 || part > 0 || ks > 0);
+                    }
+                }
+                tc_commit(smem_addr(&o_done[t]));
+            };
+            // Stage j landed?  (this thread is the only consumer of the stages, in order)
+            auto wait_full = [&](int j) { return mbar_wait_bounded(smem_addr(&full[j % (2 * S)]), (j / (2 * S)) & 1); };
+            ok = wait_full(0);
+            if (ok) {
+                tc_fence_after_sync();
+#pragma unroll
+                for (int t = 0; t < NT; ++t) issue_qk(t, 0);
+            }
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                if (j + 1 < n_tiles) {
+                    // S_t(j + 1) goes to the other buffer, whose P_t(j - 1) the P V
+                    // products issued before have consumed by then (in-order execution).
+                    if (!(ok = wait_full(j + 1))) break;
+                    tc_fence_after_sync();
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) issue_qk(t, j + 1);
+                }
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    if (!(ok = mbar_wait_bounded(smem_addr(&p_full[2 * t + (j & 1)]), (j >> 1) & 1))) break;
+                    tc_fence_after_sync();
+                    issue_pv(t, j);
+                }
+                if (!ok) break;
+                tc_commit(smem_addr(&empty[j % S]));  // the stage is free once these MMAs completed
+            }
+            // Tensor memory is freed below: first let every MMA issued here complete.
+            tc_commit(smem_addr(mma_fin));
+            if (!mbar_wait_bounded(smem_addr(mma_fin), 0)) ok = false;
+            if (!ok) atomicOr(p.err, FDEC_DEVERR_TIMEOUT);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int t = (warp - 2) >> 2;       // tile of this warpgroup
+        const int wq = warp & 3;             // tensor-memory lane quarter of this warp
+        const int r = wq * 32 + lane;        // row within the tile = tensor-memory lane
+        const int row = row0 + t * Lay::TM + r;
+        const int qi = row / p.group;
+        const int lim = p.causal ? (ir.L - p.q_len + qi) : (ir.L - 1);
+        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tmem_t = tmem + 256 * t + lane_base;
+        const uint32_t tmem_o = tmem_t + 128;
+        const float c_log2 = p.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            const uint32_t buf = tmem_t + 64 * (j & 1);
+            if (!mbar_wait_bounded(smem_addr(&s_full[2 * t + (j & 1)]), (j >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            float sv[TOK];
+            {
+                float a[32];
+                tmem_ld32(buf + 0, a);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) sv[c] = a[c];
+                tmem_ld32(buf + 32, a);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) sv[32 + c] = a[c];
+                tmem_wait_ld();
+            }
+
+            const int t0 = ir.tok_begin + j * TOK;
+            const int nv = min(TOK, ir.tok_end - t0);
+            const int vis = min(nv, lim - t0 + 1);  // tokens of this block the row may see
+            // Row max of the logits in log2 units.  Blocks that some row of the
+            // warp sees only in part take the masked form; the others scale the
+            // raw maximum (minimum for a negative scale) and fold the scale into
+            // the exponent below.  Eight independent chains, then a tree.
+            float mx, cs;
+            if (__any_sync(0xffffffffu, vis < TOK)) {
+#pragma unroll
+                for (int c = 0; c < TOK; ++c) sv[c] = c < vis ? sv[c] * c_log2 : -INFINITY;
+                float q8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) q8[k] = sv[k];
+#pragma unroll
+                for (int c = 8; c < TOK; ++c) q8[c & 7] = fmaxf(q8[c & 7], sv[c]);
+                mx = fmaxf(fmaxf(fmaxf(q8[0], q8[1]), fmaxf(q8[2], q8[3])), fmaxf(fmaxf(q8[4], q8[5]), fmaxf(q8[6], q8[7])));
+                cs = 1.f;
+            } else {
+                float q8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) q8[k] = sv[k];
+                if (c_log2 >= 0.f) {
+#pragma unroll
+                    for (int c = 8; c < TOK; ++c) q8[c & 7] = fmaxf(q8[c & 7], sv[c]);
+                    mx = fmaxf(fmaxf(fmaxf(q8[0], q8[1]), fmaxf(q8[2], q8[3])), fmaxf(fmaxf(q8[4], q8[5]), fmaxf(q8[6], q8[7])));
+                } else {
+#pragma unroll
+                    for (int c = 8; c < TOK; ++c) q8[c & 7] = fminf(q8[c & 7], sv[c]);
+                    mx = fminf(fminf(fminf(q8[0], q8[1]), fminf(q8[2], q8[3])), fminf(fminf(q8[4], q8[5]), fminf(q8[6], q8[7])));
+                }
+                mx *= c_log2;
+                cs = c_log2;
+            }
+            const bool grow = mx > m + kLazyRescale;
+            const bool rescale = __any_sync(0xffffffffu, grow);
+            // 1 for rows that keep their max (also while it is still -inf), 0 when m was -inf
+            const float alpha = grow ? exp2_approx(m - mx) : 1.f;
+            if (grow) m = mx;
+            if (rescale && j > 0) {
+                // O_t holds blocks 0 .. j-1: wait for the last of their P V products,
+                // then rescale this row of O_t in tensor memory.  S_t(j) has landed,
+                // so the products of block j - 2 have executed; waiting for block
+                // j - 2's phase first keeps the parity test exact even if that
+                // phase's arrival is still on its way.
+                if ((j >= 2 && !mbar_wait_bounded(smem_addr(&o_done[t]), (j - 2) & 1)) ||
+                    !mbar_wait_bounded(smem_addr(&o_done[t]), (j - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    float a[32];
+                    tmem_ld32(tmem_o + c0, a);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) a[c] *= alpha;
+                    tmem_st32(tmem_o + c0, a);
+                }
+                tmem_wait_st();
+            }
+            const float mu = m == -INFINITY ? 0.f : m;
+            // p = exp2(s * cs - mu), its row sum, and the packed high / residual parts
+            uint32_t hi[TOK / 2], lo[TOK / 2];
+            float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            const float2 cs2 = make_float2(cs, cs), nmu2 = make_float2(-mu, -mu);
+#pragma unroll
+            for (int c = 0; c < TOK; c += 2) {
+                const float2 z = __ffma2_rn(make_float2(sv[c], sv[c + 1]), cs2, nmu2);
+                const float2 e = make_float2(exp2_approx(z.x), exp2_approx(z.y));
+                ls[(c >> 1) & 3] = __fadd2_rn(ls[(c >> 1) & 3], e);
+                hi[c / 2] = pack2<BF16>(e.x, e.y);
+                const float2 hf = unpack_pair<BF16>(hi[c / 2]);
+                const float2 rs = __fadd2_rn(e, make_float2(-hf.x, -hf.y));
+                lo[c / 2] = pack2<BF16>(rs.x, rs.y);
+            }
+            const float2 l01 = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
+            l = l * alpha + (l01.x + l01.y);
+            // P_t(j) over S_t(j): high parts in columns 0..31, residuals in 32..63
+            tmem_st32_u(buf + 0, hi);
+            tmem_st32_u(buf + 32, lo);
+            tmem_wait_st();
+            if (t == 0 && nv < TOK) {
+                // A partial stage: zero V rows past the sequence end (0 * NaN would
+                // poison O).  Tile 0's P V products come first for every stage.
+                zero_v_tail<D, TOK>(stages + (j % S) * G::STAGE_BYTES, nv, threadIdx.x - 64, 128);
+                fence_proxy_async_shared();  // read by the tensor cores
+                named_barrier(2, 128);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&p_full[2 * t + (j & 1)]));
+        }
+        // The last P V products: the barrier may be two phases behind here (the
+        // last S_t only shows that block n - 3's products executed), so wait for
+        // block n - 2 first.
+        if (ok && n_tiles > 1 && !mbar_wait_bounded(smem_addr(&o_done[t]), (n_tiles - 2) & 1)) ok = false;
+        if (ok && n_tiles > 0 && !mbar_wait_bounded(smem_addr(&o_done[t]), (n_tiles - 1) & 1)) ok = false;
+        tc_fence_after_sync();
+        if (!ok && lane == 0) atomicOr(p.err, FDEC_DEVERR_TIMEOUT);
+
+        const int h = kvh * p.group + (row - qi * p.group);
+        const int64_t orow = static_cast<int64_t>(b * p.q_len + qi) * p.hq + h;
+        const int64_t prow = (static_cast<int64_t>(it.slot) * p.hk + kvh) * p.rows + row;
+        if (n_tiles > 0 && ok) {
+            // O row from tensor memory -> partial (unnormalised) or final output
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float a[32];
+                tmem_ld32(tmem_o + c0, a);
+                tmem_wait_ld();
+                if (row < p.rows) {
+                    float* dst = it.slot < 0 ? p.out + orow * D + c0 : p.part_o + prow * D + c0;
+                    const float f = it.slot < 0 ? inv : 1.f;
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                        *reinterpret_cast<float4*>(dst + c) =
+                            make_float4(a[c] * f, a[c + 1] * f, a[c + 2] * f, a[c + 3] * f);
+                }
+            }
+        } else {
+            // nothing visible (or a failed wait): an empty state
+            if (row < p.rows) {
+                float* dst = it.slot < 0 ? p.out + orow * D : p.part_o + prow * D;
+                for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            m = -INFINITY;
+            l = 0.f;
+        }
+        if (row < p.rows) {
+            if (it.slot < 0) {
+                if (p.lse != nullptr) p.lse[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+            } else {
+                p.part_ml[prow] = make_float2(l > 0.f ? m : -INFINITY, l);
+            }
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, Lay::TMEM_COLS);
+    }
+}
+
+template <int NT, bool BF16>
+cudaError_t launch_split_tc_one(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
+                                cudaStream_t stream, bool launch) {
+    static unsigned long long attr_done = 0;  // one bit per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+        e = cudaFuncSetAttribute(split_tc_kernel<NT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 TcLayout<NT>::SMEM);
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_RELEASE);
+    }
+    if (!launch) return cudaSuccess;
+    split_tc_kernel<NT, BF16><<<grid, TcLayout<NT>::THREADS, TcLayout<NT>::SMEM, stream>>>(p, tk, tv);
+    return cudaGetLastError();
+}
+
+}  // namespace fdec

@@ -3,6 +3,8 @@
 //
 //   D1 (128 x 64)  = A (128 x 128, K-major) * B (64 x 128, K-major)^T
 //   D2 (128 x 128) = P (128 x 64, K-major)  * V (64 x 128, MN-major: stored [k][n])
+//   D3 (128 x 128) = P (128 x 64, in tensor memory: lane = row, element pairs per
+//                    32-bit column) * V (as for D2)
 //
 // One CTA of 128 threads; all operands are copied into 128B-swizzled shared
 // memory by plain stores, the MMAs are issued by thread 0, and the four warps
@@ -22,7 +24,8 @@ __device__ __forceinline__ uint32_t swz(int row, int e, int rows) {
 }
 
 __global__ void __launch_bounds__(128) tc_selftest_kernel(const uint16_t* a, const uint16_t* b, const uint16_t* pm,
-                                                         const uint16_t* v, float* d1, float* d2, unsigned* err) {
+                                                         const uint16_t* v, float* d1, float* d2, float* d3,
+                                                         unsigned* err) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t base = smem_addr(smem);
     uint8_t* s = smem + ((1024u - (base & 1023u)) & 1023u);
@@ -52,7 +55,7 @@ __global__ void __launch_bounds__(128) tc_selftest_kernel(const uint16_t* a, con
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(smem_addr(tmem_slot), 256);
+        tmem_alloc(smem_addr(tmem_slot), 512);
         tmem_relinquish();
     }
     fence_proxy_async_shared();  // the generic stores above are read by the tensor cores
@@ -60,6 +63,18 @@ __global__ void __launch_bounds__(128) tc_selftest_kernel(const uint16_t* a, con
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    const int row = warp * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    {  // row `row` of P into tensor-memory columns 256..287 of this lane
+        uint32_t w[32];
+        for (int c = 0; c < 32; ++c)
+            w[c] = static_cast<uint32_t>(pm[row * 64 + 2 * c]) | (static_cast<uint32_t>(pm[row * 64 + 2 * c + 1]) << 16);
+        tmem_st32_u(lane_addr + 256, w);
+        tmem_wait_st();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
 
     if (tid == 0) {
         const uint32_t i1 = idesc_f16(128, 64, true, false, false);
@@ -74,14 +89,16 @@ __global__ void __launch_bounds__(128) tc_selftest_kernel(const uint16_t* a, con
             const uint64_t bd = smem_desc_sw128(smem_addr(sv_) + ks * 2048, 8192, 1024);
             tc_mma_f16(tmem + 128, ad, bd, i2, ks > 0);
         }
+        for (int ks = 0; ks < 4; ++ks) {  // A from tensor memory: 8 columns (16 K elements) per step
+            const uint64_t bd = smem_desc_sw128(smem_addr(sv_) + ks * 2048, 8192, 1024);
+            tc_mma_f16_ts(tmem + 384, tmem + 256 + ks * 8, bd, i2, ks > 0);
+        }
         tc_commit(smem_addr(bar));
     }
     if (!mbar_wait_bounded(smem_addr(bar), 0)) {
         if (lane == 0) atomicOr(err, 1u);
     }
     tc_fence_after_sync();
-    const int row = warp * 32 + lane;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float vals[32];
     for (int c = 0; c < 64; c += 32) {
         tmem_ld32(lane_addr + c, vals);
@@ -92,18 +109,21 @@ __global__ void __launch_bounds__(128) tc_selftest_kernel(const uint16_t* a, con
         tmem_ld32(lane_addr + 128 + c, vals);
         tmem_wait_ld();
         for (int j = 0; j < 32; ++j) d2[row * 128 + c + j] = vals[j];
+        tmem_ld32(lane_addr + 384 + c, vals);
+        tmem_wait_ld();
+        for (int j = 0; j < 32; ++j) d3[row * 128 + c + j] = vals[j];
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 extern "C" int tc_selftest(const uint16_t* a, const uint16_t* b, const uint16_t* p, const uint16_t* v, float* d1,
-                           float* d2, unsigned* err) {
+                           float* d2, float* d3, unsigned* err) {
     const int smem = 81920 + 1024 + 1024;
     if (cudaFuncSetAttribute(tc_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return 1;
-    tc_selftest_kernel<<<1, 128, smem>>>(a, b, p, v, d1, d2, err);
+    tc_selftest_kernel<<<1, 128, smem>>>(a, b, p, v, d1, d2, d3, err);
     if (cudaGetLastError() != cudaSuccess) return 2;
     return cudaDeviceSynchronize() == cudaSuccess ? 0 : 3;
 }

@@ -109,6 +109,24 @@ def test_path_selection():
     with pytest.raises(fd.FdecError) as ei:
         _plan([100], head_dim=256, path=fd.FDEC_PATH_MMA)
     assert ei.value.status_name == "FDEC_ERR_UNSUPPORTED"
+    with pytest.raises(fd.FdecError) as ei:
+        _plan([100], head_dim=64, path=fd.FDEC_PATH_TC)
+    assert ei.value.status_name == "FDEC_ERR_UNSUPPORTED"
+
+
+def test_dense_query_rows_take_the_tcgen05_path():
+    # q_len x group: 8 x 4 = 32 rows stay on the 16-row kernel; 16 x 4 = 64 fill half a 128-row tile
+    assert fd.fdec_plan_get_info(_plan([8200] * 4, q_len=8, num_qo_heads=32, num_kv_heads=8,
+                                       causal=True))["path"] == fd.FDEC_PATH_MMA
+    info = fd.fdec_plan_get_info(_plan([8200] * 4, q_len=16, num_qo_heads=32, num_kv_heads=8, causal=True))
+    assert info["path"] == fd.FDEC_PATH_TC and info["rows_per_group"] == 128 and info["row_groups"] == 1
+    info = fd.fdec_plan_get_info(_plan([10240] * 4, q_len=2048, num_qo_heads=32, num_kv_heads=8, causal=True))
+    # more than 128 rows: two 128-row tiles per CTA share each staged K/V block
+    assert info["path"] == fd.FDEC_PATH_TC and info["rows_per_group"] == 256
+    assert info["row_groups"] == 2048 * 4 // 256
+    assert info["num_split_ctas"] == info["num_items"] * 8 * info["row_groups"]
+    # head_dim 64 / 192 keep the 16-row kernel at any row count
+    assert fd.fdec_plan_get_info(_plan([1000], q_len=64, head_dim=64))["path"] == fd.FDEC_PATH_MMA
 
 
 def test_row_groups_cover_all_query_rows():

@@ -80,10 +80,11 @@ def test_multi_token_prefill_chunk_sampled_rows():
     w = W.multi_token(2048, device="cuda")
     rows = []
     for b in range(w.batch):
-        for i in [0, 1, 63, 64, 1000, 2046, 2047]:
-            for h in (0, 5, 31):
+        for i in [0, 1, 31, 32, 63, 64, 1000, 2046, 2047]:
+            for h in (0, 3, 4, 5, 31):
                 rows.append((b * w.q_len + i) * w.num_qo_heads + h)
-    _check(w, rows=rows)
+    (e_out, e_lse), pd = _check(w, rows=rows)
+    assert pd.info["path"] == fd.FDEC_PATH_TC
 
 
 # ------------------------------------------------------------------ both split kernels
@@ -114,6 +115,72 @@ def test_both_kernels_small_and_large_pages_with_nan_guard(path, page_size):
     assert torch.isfinite(out).all()
     ro, rl = oracle_run(w.to("cpu"))
     assert_parity(out.cpu(), lse.cpu(), ro, rl, f"path {path} page {page_size}")
+
+
+# ------------------------------------------------------------------ the tcgen05 dense-query kernel
+
+TC_CASES = {
+    # q_len x group = 64: half of one 128-row tile; short and ragged sequences
+    "half_tile": lambda: W.make(2, 16, 32, 8, 128, 16, [300, 1000], dtype="bf16", device="cuda", seed=11,
+                                causal=True),
+    # 160 rows: one full tile and a ragged one (row groups 2)
+    "ragged_tile": lambda: W.make(2, 40, 16, 4, 128, 16, [2100, 777], dtype="bf16", device="cuda", seed=12,
+                                  causal=True),
+    "not_causal": lambda: W.make(2, 32, 8, 2, 128, 16, [1500, 4100], dtype="bf16", device="cuda", seed=13),
+    "f16": lambda: W.make(2, 64, 8, 4, 128, 32, [900, 3000], dtype="f16", device="cuda", seed=14, causal=True),
+    # 384 rows: a CTA of two tiles and a CTA whose second tile is empty
+    "f16_two_tiles": lambda: W.make(2, 96, 8, 2, 128, 32, [700, 2500], dtype="f16", device="cuda", seed=19,
+                                    causal=True),
+    "peaked": lambda: W.make(1, 64, 8, 2, 128, 64, [6000], dtype="bf16", device="cuda", seed=15, causal=True,
+                             peaked=True),
+    "gqa_group1": lambda: W.make(1, 128, 4, 4, 128, 16, [2000], dtype="bf16", device="cuda", seed=16,
+                                 causal=True),
+    # sequences shorter than the query chunk: leading rows see nothing
+    "short": lambda: W.make(3, 64, 4, 1, 128, 16, [0, 20, 64], dtype="bf16", device="cuda", seed=17,
+                            causal=True),
+    "hnd_interleaved": lambda: W.make(2, 32, 8, 2, 128, 16, [1234, 640], dtype="bf16", device="cuda", seed=18,
+                                      causal=True, layout="interleaved"),
+}
+
+
+@pytest.mark.parametrize("case", list(TC_CASES))
+def test_tcgen05_dense_query_kernel(case):
+    w = TC_CASES[case]()
+    (e_out, e_lse), pd = _check(w, path=fd.FDEC_PATH_TC)
+    assert pd.info["path"] == fd.FDEC_PATH_TC
+
+
+@pytest.mark.parametrize("bps", [1, 3, 10**6])
+def test_tcgen05_kernel_under_any_split_plan(bps):
+    w = W.make(2, 48, 8, 2, 128, 16, [3000, 5000], dtype="bf16", device="cuda", seed=21, causal=True,
+               peaked=True)
+    (e_out, e_lse), pd = _check(w, path=fd.FDEC_PATH_TC, blocks_per_split=bps)
+    if bps == 1:
+        assert pd.info["max_splits"] == 79
+
+
+@pytest.mark.parametrize("page_size", [1, 4, 8, 16, 64, 128, 256])
+def test_tcgen05_kernel_page_sizes_with_nan_guard(page_size):
+    w = W.make(3, 40, 16, 4, 128, page_size, [5, 333, 1000], dtype="bf16", device="cuda", seed=page_size,
+               causal=True, nan_guard=True, pool_pages=2 * (1000 // page_size + 8))
+    out, lse, pd = gpu_run(w, path=fd.FDEC_PATH_TC, blocks_per_split=3)
+    assert pd.info["path"] == fd.FDEC_PATH_TC
+    assert torch.isfinite(out).all()
+    ro, rl = oracle_run(w.to("cpu"))
+    assert_parity(out.cpu(), lse.cpu(), ro, rl, f"tcgen05 page {page_size}")
+
+
+def test_tcgen05_and_mma_kernels_agree_on_the_prefill_chunk():
+    w = W.multi_token(2048, device="cuda")
+    o_tc, l_tc, pd = gpu_run(w)
+    assert pd.info["path"] == fd.FDEC_PATH_TC
+    o_mma, l_mma, pd2 = gpu_run(w, path=fd.FDEC_PATH_MMA)
+    torch.cuda.synchronize()
+    assert pd.device_errors() == 0 and pd2.device_errors() == 0
+    # both within the oracle tolerance of each other on every row (not only the sampled ones)
+    d = (o_tc - o_mma).abs().amax(dim=-1) / o_mma.abs().amax(dim=-1)
+    assert float(d.max()) <= 2 * 2e-3
+    assert float((l_tc - l_mma).abs().max()) <= 2 * 1e-4
 
 
 # ------------------------------------------------------------------ plans and reductions

@@ -20,7 +20,7 @@ def selftest_lib(tmp_path_factory):
                    check=True)
     lib = ctypes.CDLL(str(out))
     lib.tc_selftest.restype = ctypes.c_int
-    lib.tc_selftest.argtypes = [ctypes.c_void_p] * 7
+    lib.tc_selftest.argtypes = [ctypes.c_void_p] * 8
     return lib
 
 
@@ -33,10 +33,14 @@ def test_k_major_and_mn_major_products(selftest_lib):
     dev = [t.cuda().contiguous() for t in (a, b, p, v)]
     d1 = torch.full((128, 64), float("nan"), device="cuda")
     d2 = torch.full((128, 128), float("nan"), device="cuda")
+    d3 = torch.full((128, 128), float("nan"), device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rc = selftest_lib.tc_selftest(*[t.data_ptr() for t in dev], d1.data_ptr(), d2.data_ptr(), err.data_ptr())
+    rc = selftest_lib.tc_selftest(*[t.data_ptr() for t in dev], d1.data_ptr(), d2.data_ptr(), d3.data_ptr(),
+                                  err.data_ptr())
     assert rc == 0 and int(err.item()) == 0
     ref1 = a.double() @ b.double().T
     ref2 = p.double() @ v.double()
     np.testing.assert_allclose(d1.cpu().double().numpy(), ref1.numpy(), rtol=1e-5, atol=1e-4)
     np.testing.assert_allclose(d2.cpu().double().numpy(), ref2.numpy(), rtol=1e-5, atol=1e-4)
+    # the same product with P read from tensor memory
+    np.testing.assert_allclose(d3.cpu().double().numpy(), ref2.numpy(), rtol=1e-5, atol=1e-4)
