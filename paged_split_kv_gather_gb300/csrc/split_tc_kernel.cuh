@@ -20,16 +20,16 @@
 //               block's softmax, and the tiles take turns with the tensor cores.
 //   warps 2+4t..5+4t  softmax warpgroup of tile t, thread = row = tensor-memory
 //               lane: load the row of S, mask, row max in registers, exp2, and the
-//               row of P split into a bf16/f16 high part and a residual (both
-//               multiplied, so p keeps ~16 significant bits), stored back into
-//               tensor memory.  The lazy rescale of the row of O (only when the
+//               row of P stored back into tensor memory: for bf16 a high part and
+//               a residual (both multiplied, so p keeps ~15 significant bits), for
+//               f16 one value (11 bits; the f16 P V products need half the MMAs).  The lazy rescale of the row of O (only when the
 //               max grew by more than 8 in log2 units; warp-uniform) first waits
 //               for the previous block's P V products.  After the last block:
 //               O, l, m -> one partial of the split, or out / lse.
 // Synchronisation: stage full / empty mbarriers (TMA / commit of the P V MMAs),
 // and per tile s_full[2] (commit of the QK MMAs, per S buffer), p_full[2] (the
-// four softmax warps, per buffer) and o_done (commit of the P V MMAs).  Every
-// wait is bounded.  Ordering of the S / P buffers: the tensor cores execute
+// four softmax warps, per buffer), o_done (commit of the P V MMAs) and o_final
+// (commit after the last block's P V MMAs).  Every wait is bounded.  Ordering of the S / P buffers: the tensor cores execute
 // one thread's MMAs in issue order, so S_t(j + 2), issued after the P V
 // products of block j, overwrites P_t(j) only after they have read it.
 #pragma once
@@ -51,7 +51,7 @@ struct TcLayout {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_STAGES = OFF_Q + NT * Q_BYTES;
     static constexpr int OFF_BARS = OFF_STAGES + S * G::STAGE_BYTES;
-    static constexpr int NBARS = 3 * S + 5 * NT + 1;
+    static constexpr int NBARS = 3 * S + 6 * NT + 1;
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM = OFF_BARS + BAR_BYTES + 1024;  // + alignment slack
     static constexpr int THREADS = (2 + 4 * NT) * 32;
@@ -67,6 +67,18 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int chunk) {
     return static_cast<uint32_t>(r * 128 + (((chunk ^ r) & 7) << 4));
 }
 
+// (y & 0xffff0000) | (x >> 16): the bf16 truncations of x (low half) and y (high
+// half) in one word, with a shift and a LOP3.  Written in PTX so that it stays
+// those two instructions: byte-permute and float -> 16-bit conversion
+// instructions issued by the softmax warps slow the tensor cores' MMA stream
+// (measured on sm_103a), while shifts and logic ops do not.
+__device__ __forceinline__ uint32_t pack_upper_halves(uint32_t x, uint32_t y) {
+    uint32_t t, r;
+    asm volatile("shr.u32 %0, %1, 16;" : "=r"(t) : "r"(x));
+    asm volatile("lop3.b32 %0, %1, 0xffff0000, %2, 0xEA;" : "=r"(r) : "r"(y), "r"(t));
+    return r;
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float x, float y) {
     if constexpr (BF16) {
@@ -75,15 +87,6 @@ __device__ __forceinline__ uint32_t pack2(float x, float y) {
     } else {
         const __half2 h = __floats2half2_rn(x, y);
         return *reinterpret_cast<const uint32_t*>(&h);
-    }
-}
-
-template <bool BF16>
-__device__ __forceinline__ float2 unpack_pair(uint32_t w) {
-    if constexpr (BF16) {
-        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-    } else {
-        return __half22float2(*reinterpret_cast<const __half2*>(&w));
     }
 }
 
@@ -98,6 +101,14 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
     constexpr int D = Lay::D;
     constexpr float kLn2 = 0.69314718055994530942f;
     constexpr float kLazyRescale = 8.f;
+    // bf16: P = hi + lo, both bf16 (hi = p truncated to bf16, lo = the residual
+    // truncated), ~15 significant bits; split with shifts, logic ops and FMAs
+    // only (see pack_upper_halves).  f16: P is one f16 value
+    // per token (11 significant bits), scaled by 2^kPShift so that small p stay
+    // normal; l carries the same factor and the stored max drops by kPShift.
+    constexpr bool kSplit = BF16;
+    constexpr int kParts = kSplit ? 2 : 1;
+    constexpr float kPShift = BF16 ? 0.f : 7.f;
 
     extern __shared__ __align__(128) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -109,7 +120,8 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
     uint64_t* s_full = bars + 3 * S;  // [NT][2]
     uint64_t* p_full = s_full + 2 * NT;  // [NT][2]
     uint64_t* o_done = p_full + 2 * NT;  // [NT]
-    uint64_t* mma_fin = o_done + NT;
+    uint64_t* o_final = o_done + NT;     // [NT]
+    uint64_t* mma_fin = o_final + NT;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_fin + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -141,7 +153,10 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
             mbar_init(smem_addr(&p_full[i]), 4);
         }
 #pragma unroll
-        for (int t = 0; t < NT; ++t) mbar_init(smem_addr(&o_done[t]), 1);
+        for (int t = 0; t < NT; ++t) {
+            mbar_init(smem_addr(&o_done[t]), 1);
+            mbar_init(smem_addr(&o_final[t]), 1);
+        }
         mbar_init(smem_addr(mma_fin), 1);
         fence_mbar_init();
     }
@@ -194,28 +209,32 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
             bool ok = true;
             const uint32_t i_qk = idesc_f16(128, TOK, BF16, false, false);
             const uint32_t i_pv = idesc_f16(128, D, BF16, false, true);
-            auto issue_qk = [&](int t, int j) {
-                const uint32_t q_addr = smem_addr(q_tiles + t * Lay::Q_BYTES);
-                const uint32_t k_addr = smem_addr(stages + (j % S) * G::STAGE_BYTES);
+            // Descriptors are built once; a byte offset x within shared memory is
+            // x >> 4 added to the start-address field (the sum stays below 2^14).
+            const uint64_t qd0 = smem_desc_sw128(smem_addr(q_tiles), 16, 1024);
+            const uint64_t kd0 = smem_desc_sw128(smem_addr(stages), 16, 1024);
+            const uint64_t vd0 = smem_desc_sw128(smem_addr(stages + G::HALF_BYTES), G::REGION_BYTES, 1024);
+            constexpr uint32_t kQTile = Lay::Q_BYTES >> 4, kQRegion = (Lay::TM * 128) >> 4;
+            constexpr uint32_t kStage = G::STAGE_BYTES >> 4, kKRegion = G::REGION_BYTES >> 4;
+            auto issue_qk = [&](int t, int slot, int buf) {
+                const uint64_t qd = qd0 + t * kQTile;
+                const uint64_t kd = kd0 + static_cast<uint32_t>(slot) * kStage;
+                const uint32_t d = tmem + 256 * t + 64 * buf;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t ad = smem_desc_sw128(q_addr + (ks >> 2) * (Lay::TM * 128) + (ks & 3) * 32, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(k_addr + (ks >> 2) * G::REGION_BYTES + (ks & 3) * 32, 16, 1024);
-                    tc_mma_f16(tmem + 256 * t + 64 * (j & 1), ad, bd, i_qk, ks > 0);
-                }
-                tc_commit(smem_addr(&s_full[2 * t + (j & 1)]));
+                for (int ks = 0; ks < D / 16; ++ks)
+                    tc_mma_f16(d, qd + (ks >> 2) * kQRegion + (ks & 3) * 2, kd + (ks >> 2) * kKRegion + (ks & 3) * 2, i_qk,
+                               ks > 0);
+                tc_commit(smem_addr(&s_full[2 * t + buf]));
             };
-            auto issue_pv = [&](int t, int j) {
-                const uint32_t v_addr = smem_addr(stages + (j % S) * G::STAGE_BYTES + G::HALF_BYTES);
-                const uint32_t p_tm = tmem + 256 * t + 64 * (j & 1);
+            auto issue_pv = [&](int t, int slot, int buf, bool acc) {
+                const uint64_t vd = vd0 + static_cast<uint32_t>(slot) * kStage;
+                const uint32_t p_tm = tmem + 256 * t + 64 * buf;
+                const uint32_t o_tm = tmem + 256 * t + 128;
+                tc_mma_f16_ts(o_tm, p_tm, vd, i_pv, acc);
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-#pragma unroll
-                    for (int ks = 0; ks < TOK / 16; ++ks) {
-                        const uint64_t bd = smem_desc_sw128(v_addr + ks * 16 * 128, G::REGION_BYTES, 1024);
-                        tc_mma_f16_ts(tmem + 256 * t + 128, p_tm + 32 * part + 8 * ks, bd, i_pv,
-                                      j > 0 || part > 0 || ks > 0);
-                    }
+                for (int i = 1; i < kParts * (TOK / 16); ++i) {  // i = part * 4 + ks: 16 tokens (128 rows of V) per step
+                    const int part = i / (TOK / 16), ks = i % (TOK / 16);
+                    tc_mma_f16_ts(o_tm, p_tm + 32 * part + 8 * ks, vd + ks * 128, i_pv, true);
                 }
                 tc_commit(smem_addr(&o_done[t]));
             };
@@ -225,25 +244,29 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
             if (ok) {
                 tc_fence_after_sync();
 #pragma unroll
-                for (int t = 0; t < NT; ++t) issue_qk(t, 0);
+                for (int t = 0; t < NT; ++t) issue_qk(t, 0, 0);
             }
+            int slot = 0;  // stage slot of block j
             for (int j = 0; j < n_tiles && ok; ++j) {
+                const int next_slot = slot + 1 == S ? 0 : slot + 1;
                 if (j + 1 < n_tiles) {
                     // S_t(j + 1) goes to the other buffer, whose P_t(j - 1) the P V
                     // products issued before have consumed by then (in-order execution).
                     if (!(ok = wait_full(j + 1))) break;
                     tc_fence_after_sync();
 #pragma unroll
-                    for (int t = 0; t < NT; ++t) issue_qk(t, j + 1);
+                    for (int t = 0; t < NT; ++t) issue_qk(t, next_slot, (j + 1) & 1);
                 }
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
                     if (!(ok = mbar_wait_bounded(smem_addr(&p_full[2 * t + (j & 1)]), (j >> 1) & 1))) break;
                     tc_fence_after_sync();
-                    issue_pv(t, j);
+                    issue_pv(t, slot, j & 1, j > 0);
+                    if (j + 1 == n_tiles) tc_commit(smem_addr(&o_final[t]));
                 }
                 if (!ok) break;
-                tc_commit(smem_addr(&empty[j % S]));  // the stage is free once these MMAs completed
+                tc_commit(smem_addr(&empty[slot]));  // the stage is free once these MMAs completed
+                slot = next_slot;
             }
             // Tensor memory is freed below: first let every MMA issued here complete.
             tc_commit(smem_addr(mma_fin));
@@ -324,12 +347,11 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
             if (grow) m = mx;
             if (rescale && j > 0) {
                 // O_t holds blocks 0 .. j-1: wait for the last of their P V products,
-                // then rescale this row of O_t in tensor memory.  S_t(j) has landed,
-                // so the products of block j - 2 have executed; waiting for block
-                // j - 2's phase first keeps the parity test exact even if that
-                // phase's arrival is still on its way.
-                if ((j >= 2 && !mbar_wait_bounded(smem_addr(&o_done[t]), (j - 2) & 1)) ||
-                    !mbar_wait_bounded(smem_addr(&o_done[t]), (j - 1) & 1)) {
+                // then rescale this row of O_t in tensor memory.  o_done_t is in
+                // phase j - 1 or j here: S_t(j) has landed, so the products of
+                // block j - 2 (issued before it) have completed, and those of
+                // block j wait for this warp's P_t(j).  The parity test is exact.
+                if (!mbar_wait_bounded(smem_addr(&o_done[t]), (j - 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -347,24 +369,29 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
             }
             const float mu = m == -INFINITY ? 0.f : m;
             // p = exp2(s * cs - mu), its row sum, and the packed high / residual parts
-            uint32_t hi[TOK / 2], lo[TOK / 2];
+            uint32_t hi[TOK / 2], lo[kSplit ? TOK / 2 : 1];
             float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            const float2 cs2 = make_float2(cs, cs), nmu2 = make_float2(-mu, -mu);
+            const float2 cs2 = make_float2(cs, cs), nmu2 = make_float2(kPShift - mu, kPShift - mu);
 #pragma unroll
             for (int c = 0; c < TOK; c += 2) {
                 const float2 z = __ffma2_rn(make_float2(sv[c], sv[c + 1]), cs2, nmu2);
                 const float2 e = make_float2(exp2_approx(z.x), exp2_approx(z.y));
                 ls[(c >> 1) & 3] = __fadd2_rn(ls[(c >> 1) & 3], e);
-                hi[c / 2] = pack2<BF16>(e.x, e.y);
-                const float2 hf = unpack_pair<BF16>(hi[c / 2]);
-                const float2 rs = __fadd2_rn(e, make_float2(-hf.x, -hf.y));
-                lo[c / 2] = pack2<BF16>(rs.x, rs.y);
+                if constexpr (kSplit) {
+                    const uint32_t bx = __float_as_uint(e.x), by = __float_as_uint(e.y);
+                    hi[c / 2] = pack_upper_halves(bx, by);  // truncation to bf16
+                    const float2 hf = make_float2(__uint_as_float(bx & 0xffff0000u), __uint_as_float(by & 0xffff0000u));
+                    const float2 rs = __ffma2_rn(hf, make_float2(-1.f, -1.f), e);  // exact residual
+                    lo[c / 2] = pack_upper_halves(__float_as_uint(rs.x), __float_as_uint(rs.y));
+                } else {
+                    hi[c / 2] = pack2<false>(e.x, e.y);
+                }
             }
             const float2 l01 = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
             l = l * alpha + (l01.x + l01.y);
             // P_t(j) over S_t(j): high parts in columns 0..31, residuals in 32..63
             tmem_st32_u(buf + 0, hi);
-            tmem_st32_u(buf + 32, lo);
+            if constexpr (kSplit) tmem_st32_u(buf + 32, lo);
             tmem_wait_st();
             if (t == 0 && nv < TOK) {
                 // A partial stage: zero V rows past the sequence end (0 * NaN would
@@ -377,11 +404,9 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&p_full[2 * t + (j & 1)]));
         }
-        // The last P V products: the barrier may be two phases behind here (the
-        // last S_t only shows that block n - 3's products executed), so wait for
-        // block n - 2 first.
-        if (ok && n_tiles > 1 && !mbar_wait_bounded(smem_addr(&o_done[t]), (n_tiles - 2) & 1)) ok = false;
-        if (ok && n_tiles > 0 && !mbar_wait_bounded(smem_addr(&o_done[t]), (n_tiles - 1) & 1)) ok = false;
+        // The last P V products: o_done_t may be anywhere from phase n - 2 to n
+        // here, so the MMA thread signals them on a barrier of their own.
+        if (ok && n_tiles > 0 && !mbar_wait_bounded(smem_addr(&o_final[t]), 0)) ok = false;
         tc_fence_after_sync();
         if (!ok && lane == 0) atomicOr(p.err, FDEC_DEVERR_TIMEOUT);
 
@@ -416,9 +441,9 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
         }
         if (row < p.rows) {
             if (it.slot < 0) {
-                if (p.lse != nullptr) p.lse[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+                if (p.lse != nullptr) p.lse[orow] = l > 0.f ? (m - kPShift + log2f(l)) * kLn2 : -INFINITY;
             } else {
-                p.part_ml[prow] = make_float2(l > 0.f ? m : -INFINITY, l);
+                p.part_ml[prow] = make_float2(l > 0.f ? m - kPShift : -INFINITY, l);
             }
         }
     }
