@@ -66,10 +66,11 @@ def _attention_flops(w) -> float:
     return 4.0 * w.head_dim * w.num_qo_heads * total
 
 
-def _dense_query(dev, calls, hbm_peak):
+def _dense_query(dev, calls, hbm_peak, q_lens=(4, 8, 2048)):
     """Multi-token queries over the paged cache (batch 4, 32/8 heads, D 128, bf16,
     page 16, prefix 8192 + q_len, causal): q_len 4 and 8 (speculative decode) and
-    2048 (a prefill chunk, the tcgen05 path; also timed on the 16-row kernel)."""
+    2048 (a prefill chunk).  q_len x group > 16 takes the tcgen05 path, also
+    timed on the 16-row warp-level kernel for comparison."""
     import torch
 
     import paged_split_kv_gather_gb300 as fd
@@ -77,16 +78,17 @@ def _dense_query(dev, calls, hbm_peak):
 
     tflops_peak, tflops_kind = _bf16_peak()
     names = {fd.FDEC_PATH_SIMT: "simt", fd.FDEC_PATH_MMA: "mma", fd.FDEC_PATH_TC: "tcgen05"}
-    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
     res = []
-    for q_len in (4, 8, 2048):
+    for q_len in q_lens:
         w = W.multi_token(q_len, device=dev)
         table = torch.as_tensor(w.page_table, device=dev)
         lens = torch.as_tensor(w.seq_lens, device=dev)
         out = torch.empty((w.batch, q_len, w.num_qo_heads, w.head_dim), device=dev)
         lse = torch.empty((w.batch, q_len, w.num_qo_heads), device=dev)
         flops = _attention_flops(w)
-        paths = [fd.FDEC_PATH_AUTO] + ([fd.FDEC_PATH_MMA] if q_len >= 64 else [])
+        # the warp-level tensor-core kernel beside the tcgen05 one wherever the plan picks the latter
+        paths = [fd.FDEC_PATH_AUTO] + ([fd.FDEC_PATH_MMA] if q_len * (w.num_qo_heads // w.num_kv_heads) > 16 else [])
         for path in paths:
             pd = fd.PagedDecode(w.seq_lens, q_len, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim,
                                 w.dtype, w.causal, device=dev, path=path)
@@ -96,7 +98,7 @@ def _dense_query(dev, calls, hbm_peak):
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
             torch.cuda._sleep(int(n * 2e5))  # the host runs ahead: no host gap between a call's events
             for a, b in evs:
-                torch.sum(flush)
+                flush()
                 a.record()
                 pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale)
                 b.record()
@@ -117,13 +119,190 @@ def _dense_query(dev, calls, hbm_peak):
             "flops": "4 x head_dim per visible (query head, query token, key token)", "points": res}
 
 
-def _kernel_source_hash() -> str:
+class L2Flush:
+    """Evict the L2 between timed calls: write one buffer larger than the L2, then
+    read another, so that the write-back of the dirty lines happens here, outside
+    the timed call, and the L2 is left holding clean lines of an unrelated buffer."""
+
+    def __init__(self, torch, dev):
+        self.torch = torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.fill_(0.0)
+        self.torch.sum(self.r)
+
+
+def _time_calls(torch, run, calls, flush):
+    """Median and min µs of `calls` calls of run(), each after an L2-evicting read,
+    all enqueued behind a device-side delay (no host gap inside a call's events)."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
+    torch.cuda._sleep(int(calls * 2e5))
+    for a, b in evs:
+        flush()
+        a.record()
+        run()
+        b.record()
+    torch.cuda.synchronize()
+    t = [a.elapsed_time(b) * 1e3 for a, b in evs]
+    return float(np.median(t)), float(min(t))
+
+
+def _time_graph(torch, run, reps, flush, flush_us=None):
+    """µs per call replayed from a CUDA graph: a graph of `reps` (L2 eviction, call)
+    pairs against a graph of the evictions alone (or the given per-eviction µs)."""
+    def capture(with_call):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(reps):
+                    flush()
+                    if with_call:
+                        run()
+        torch.cuda.current_stream().wait_stream(side)
+        return g
+
+    res = []
+    for with_call in ((True, False) if flush_us is None else (True,)):
+        g = capture(with_call)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        best = 1e30
+        for _ in range(5):
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b) * 1e3)
+        res.append(best)
+        del g
+    base = res[1] if flush_us is None else flush_us * reps
+    return max(0.0, (res[0] - base) / reps)
+
+
+def _time_flush_graph(torch, reps, flush):
+    """µs of one L2 eviction, replayed from a CUDA graph of `reps` evictions (best of 5)."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(reps):
+                flush()
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = 1e30
+    for _ in range(5):
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b) * 1e3)
+    return best / reps
+
+
+def _config_points(dev, calls, hbm_peak):
+    """The other workloads' µs/call and GB/s (tiny decode, batched GQA decode, the
+    ragged serving batch at head_dim 192/256/512), a no-cliff sweep of the long-context
+    shape over L = 1024 ... 8192 step 64, and CUDA-graph-replayed µs/call where launch
+    latency matters (tiny decode, long-context L <= 4800)."""
+    import torch
+
+    import paged_split_kv_gather_gb300 as fd
+    from paged_split_kv_gather_gb300 import workloads as W
+
+    flush = L2Flush(torch, dev)
+
+    def runner(w, capacities=None):
+        caps = w.seq_lens if capacities is None else capacities
+        pd = fd.PagedDecode(caps, w.q_len, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
+                            w.causal, device=dev)
+        table = torch.as_tensor(w.page_table, device=dev)
+        lens = torch.as_tensor(np.asarray(caps, dtype=np.int32), device=dev)
+        out = torch.empty((w.batch, w.q_len, w.num_qo_heads, w.head_dim), device=dev)
+        lse = torch.empty((w.batch, w.q_len, w.num_qo_heads), device=dev)
+
+        def run():
+            pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale)
+
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize()
+        return pd, run
+
+    points = {}
+    for name, make in (("tiny_decode", lambda: W.tiny(device=dev)),
+                       ("batched_gqa_decode", lambda: W.batched_gqa(device=dev)),
+                       *[(f"ragged_serving_D{d}", (lambda d=d: W.ragged(d, device=dev))) for d in W.RAGGED_HEAD_DIMS]):
+        w = make()
+        pd, run = runner(w)
+        med, mn = _time_calls(torch, run, calls, flush)
+        gbs = w.kv_bytes / (med * 1e-6) / 1e9
+        pt = {"us_per_call": round(med, 2), "us_min": round(mn, 2), "kv_bytes": int(w.kv_bytes),
+              "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / hbm_peak, 4),
+              "path": int(pd.info["path"]), "launches": int(pd.info["launches"])}
+        if name == "tiny_decode":
+            pt["graph_us_per_call"] = round(_time_graph(torch, run, 20, flush), 2)
+        points[name] = pt
+        del pd, run, w
+        torch.cuda.empty_cache()
+
+    # Graph-replayed long-context points where launch latency matters.
+    graph = {}
+    for L in (1900, 2000, 2100, 3000, 4800):
+        w = W.long_context(L, device=dev)
+        pd, run = runner(w)
+        graph[str(L)] = round(_time_graph(torch, run, 20, flush), 2)
+    points["long_context_graph_us_per_call"] = graph
+
+    # No-cliff sweep: one pool of 8192 tokens, plans of capacity L (the page table's
+    # prefix); per-call times from graphs of 20 (eviction, call) pairs, whose
+    # resolution is finer than single-call events at these ~20 us calls.
+    w = W.long_context(8192, device=dev)
+    flush_us = min(_time_flush_graph(torch, 20, flush) for _ in range(3))
+    sweep = []
+    for L in range(1024, 8192 + 1, 64):
+        pd, run = runner(w, capacities=[L])
+        us = _time_graph(torch, run, 20, flush, flush_us=flush_us)
+        sweep.append((L, us, int(pd.info["max_splits"])))
+        del pd, run
+    ratios = [b[1] / a[1] for a, b in zip(sweep, sweep[1:])]
+    gbs = [L * w.num_kv_heads * w.head_dim * 4 / (us * 1e-6) / 1e9 for L, us, _ in sweep]
+    drops = [(sweep[i + 1][0], round(gbs[i + 1] / gbs[i], 3)) for i in range(len(sweep) - 1)
+             if sweep[i + 1][2] != sweep[i][2] and gbs[i + 1] < gbs[i]]
+    points["no_cliff_sweep"] = {
+        "kv_lens": "1024..8192 step 64 (long-context shape: 32/4 heads, D 128, bf16, page 64)",
+        "timing": "CUDA graph of 20 (L2 eviction, call) pairs minus a graph of 20 evictions, best of 5 replays",
+        "max_adjacent_time_ratio": round(max(ratios), 3),
+        "at_kv_len": sweep[int(np.argmax(ratios)) + 1][0],
+        "gbs_drops_at_split_changes": drops,
+        "us_per_call": {str(L): round(us, 2) for L, us, _ in sweep},
+        "splits": {str(L): sp for L, _, sp in sweep},
+    }
+    del flush
+    return points
+
+
+# The sources each profiled kernel is built from: a committed traffic figure
+# stands only while these files are unchanged.
+KERNEL_SOURCES = {
+    "split_mma_kernel": ["device_utils.cuh", "fdec_internal.h", "split_common.cuh", "split_mma_kernel.cuh",
+                         "split_mma.cu"],
+}
+
+
+def _kernel_source_hash(kernel: str = "split_mma_kernel") -> str:
     csrc = os.path.join(ROOT, "paged_split_kv_gather_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -220,6 +399,15 @@ def _run_fdec(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
+    if args.only_dense:
+        # The multi-token points alone (for profiling the tcgen05 kernel); not a bench line.
+        peak, _ = _peaks()
+        dense = _dense_query(dev, args.sweep_calls, peak, tuple(args.dense_q))
+        if rank == 0:
+            print(json.dumps({"dense_query": dense}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     from paged_split_kv_gather_gb300 import workloads as W
 
@@ -314,7 +502,7 @@ def _run_fdec(args):
     # ---- the long-context sweep: per-call time with an L2 flush before each call
     sweep = []
     if not args.no_sweep:
-        flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        flush = L2Flush(torch, dev)
         for length in W.LONG_CONTEXT_LENGTHS:
             ws = w if length == HEADLINE_LENGTH else _make_inputs(length, dev)
             pds = pd if length == HEADLINE_LENGTH else fd.PagedDecode(
@@ -325,12 +513,12 @@ def _run_fdec(args):
                 pds.run(ws.q, ws.k, ws.v, tb, ln, out, lse, scale=ws.scale)
             # All calls are enqueued behind a device-side delay and before one
             # final synchronise, so the device never waits on the host between a
-            # call's two events; each call follows a 256 MB read that evicts the L2.
+            # call's two events; each call follows an L2 eviction (L2Flush).
             torch.cuda._sleep(int(args.sweep_calls * 2e5))
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.sweep_calls)]
             for a, b in evs:
-                torch.sum(flush)
+                flush()
                 a.record()
                 pds.run(ws.q, ws.k, ws.v, tb, ln, out, lse, scale=ws.scale)
                 b.record()
@@ -345,9 +533,13 @@ def _run_fdec(args):
                 del pds, ws
         del flush
 
+    extra = None
+    if not args.no_configs:
+        extra = _config_points(dev, args.sweep_calls, peak)
+
     dense = None
     if not args.no_dense:
-        dense = _dense_query(dev, args.sweep_calls, peak)
+        dense = _dense_query(dev, args.sweep_calls, peak, tuple(args.dense_q))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -372,8 +564,8 @@ def _run_fdec(args):
             "config": {"workload": "long_context_decode_L262144", "batch": 1, "q_len": 1, "num_qo_heads": 32,
                        "num_kv_heads": 4, "head_dim": 128, "page_size": 64, "kv_len": HEADLINE_LENGTH,
                        "kv_bytes_per_call": kv_bytes, "out": "fp32 out + lse",
-                       "l2": "inputs larger than L2 (537 MB of K/V per step vs 129 MB L2); each sweep call follows a "
-                             "256 MB read that evicts the L2 (clean lines)",
+                       "l2": "inputs larger than L2 (537 MB of K/V per step vs 129 MB L2); every other timed call "
+                             "follows a 256 MB write and a 256 MB read that evict the L2 (left holding clean lines)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "plan": {k: info[k] for k in ("blocks_per_split", "num_split_ctas", "max_splits",
                                                       "reduce_passes", "launches")}},
@@ -391,6 +583,7 @@ def _run_fdec(args):
             "cpu_baseline": cpu,
             "sweep": sweep,
             "dense_query": dense,
+            "other_workloads": extra,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -430,10 +623,46 @@ def _cpu_baseline(c, kv_bytes, seconds):
         if el >= seconds or passes >= 1000:
             break
     per = el / passes
+
+    # Single-core times of the two small decode workloads (the oracle with one thread).
+    from paged_split_kv_gather_gb300 import workloads as W
+
+    single = {}
+    for name, wl in (("tiny_decode", W.tiny()), ("batched_gqa_decode", W.batched_gqa())):
+        qa, qo, _ = storage_view(wl.q)
+        qn = qa.view(__import__("torch").int16).numpy().view(np.uint16)
+        kpw, vpw = pool(wl.k), pool(wl.v)
+        t1 = time.perf_counter()
+        oracle.paged_attention(qn, qo, q_token_stride(wl.q), wl.q.stride(2), kpw, vpw, wl.page_table, wl.seq_lens,
+                               q_len=1, num_qo_heads=wl.num_qo_heads, num_kv_heads=wl.num_kv_heads,
+                               head_dim=wl.head_dim, page_size=wl.page_size, is_bf16=(wl.dtype == "bf16"),
+                               causal=False, scale=wl.scale, n_threads=1)
+        single[name] = round((time.perf_counter() - t1) * 1e3, 2)
     return {"value": round(kv_bytes / per / 1e9, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "ms_per_call": round(per * 1e3, 2),
+            "ms_per_call": round(per * 1e3, 2), "cpu_model": _cpu_model(),
+            "single_core_ms_per_call": single,
             "sample": f"{passes} full passes (all 32 query rows x 262144 tokens) of the headline workload in "
                       f"{el:.1f} s, float64, OpenMP over rows"}
+
+
+def _cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+
+    return platform.processor() or platform.machine()
 
 
 def _run_reference(args):
@@ -509,6 +738,11 @@ def main():
     ap.add_argument("--sweep-calls", type=int, default=50)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-dense", action="store_true", help="skip the multi-token (q_len 4, 8, 2048) points")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads, the no-cliff sweep and the graph-replayed points")
+    ap.add_argument("--only-dense", action="store_true",
+                    help="run only the multi-token points and print them (profiling; no bench line)")
+    ap.add_argument("--dense-q", type=int, nargs="+", default=[4, 8, 2048], help="q_len of the multi-token points")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=120.0)

@@ -89,9 +89,10 @@ typedef struct fdec_plan_s* fdec_plan_t;
  * tensor-core MMA on 16-row query groups (head_dim 64, 128, 192), the decode
  * default.  TC: 5th-generation tensor cores (tcgen05, accumulators in tensor
  * memory) on 128-row query tiles, head_dim 128; chosen by AUTO when q_len x
- * group >= 64, where attention over the gathered pages is a dense contraction
- * (speculative-decode and prefill chunks).  Below that the work is bound by
- * streaming K/V and the 16-row kernels waste no tensor-core tile.
+ * group > 16, where attention over the gathered pages turns into a dense
+ * contraction (speculative-decode and prefill chunks) and the 16-row kernel
+ * would stream K/V once per 16-row group.  Up to 16 rows the work is bound by
+ * streaming K/V and the 16-row kernel wastes no tensor-core tile.
  */
 enum { FDEC_PATH_AUTO = 0, FDEC_PATH_SIMT = 1, FDEC_PATH_MMA = 2, FDEC_PATH_TC = 3 };
 
@@ -99,7 +100,7 @@ enum { FDEC_PATH_AUTO = 0, FDEC_PATH_SIMT = 1, FDEC_PATH_MMA = 2, FDEC_PATH_TC =
 typedef struct {
     int blocks_per_split;  /* 64-token blocks per split; 0 = auto; 1 = one partial per block */
     int reducer_fanin;     /* partials merged per reduction task; 0 = auto (256); >= 2 */
-    int path;              /* FDEC_PATH_AUTO (TC when head_dim 128 and q_len x group >= 64, else MMA
+    int path;              /* FDEC_PATH_AUTO (TC when head_dim 128 and q_len x group > 16, else MMA
                               where built, else SIMT), _SIMT, _MMA (head_dim 64, 128, 192),
                               _TC (head_dim 128) */
     int num_sms;           /* 0 = query the current device; > 0 plans without a device */

@@ -366,9 +366,10 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
     p->causal = (causal != 0 && q_len > 1) ? 1 : 0;
     // Tensor cores by default where the kernel exists (see split_mma_kernel.cuh for
     // why); the fp32 SIMT kernel on request and for head_dim 256 / 512.
-    // The tcgen05 kernel once a 128-row tile is at least half full.
+    // The tcgen05 kernel once the rows need more than one 16-row group of the
+    // warp-level kernel (which would stream K/V once per group).
     if (o.path == FDEC_PATH_AUTO)
-        p->path = (tc_ok && p->rows >= kTcRows / 2) ? FDEC_PATH_TC : (mma_ok ? FDEC_PATH_MMA : FDEC_PATH_SIMT);
+        p->path = (tc_ok && p->rows > kMmaRows) ? FDEC_PATH_TC : (mma_ok ? FDEC_PATH_MMA : FDEC_PATH_SIMT);
     else
         p->path = o.path;
     p->num_sms = num_sms;

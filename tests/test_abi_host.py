@@ -115,9 +115,12 @@ def test_path_selection():
 
 
 def test_dense_query_rows_take_the_tcgen05_path():
-    # q_len x group: 8 x 4 = 32 rows stay on the 16-row kernel; 16 x 4 = 64 fill half a 128-row tile
-    assert fd.fdec_plan_get_info(_plan([8200] * 4, q_len=8, num_qo_heads=32, num_kv_heads=8,
+    # q_len x group: 4 x 4 = 16 rows fit one group of the 16-row kernel; 8 x 4 = 32 would need two
+    assert fd.fdec_plan_get_info(_plan([8200] * 4, q_len=4, num_qo_heads=32, num_kv_heads=8,
                                        causal=True))["path"] == fd.FDEC_PATH_MMA
+    assert fd.fdec_plan_get_info(_plan([8200] * 4, q_len=8, num_qo_heads=32, num_kv_heads=8,
+                                       causal=True))["path"] == fd.FDEC_PATH_TC
+    assert fd.fdec_plan_get_info(_plan([1000], q_len=1, num_qo_heads=32, num_kv_heads=2))["path"] == fd.FDEC_PATH_MMA
     info = fd.fdec_plan_get_info(_plan([8200] * 4, q_len=16, num_qo_heads=32, num_kv_heads=8, causal=True))
     assert info["path"] == fd.FDEC_PATH_TC and info["rows_per_group"] == 128 and info["row_groups"] == 1
     info = fd.fdec_plan_get_info(_plan([10240] * 4, q_len=2048, num_qo_heads=32, num_kv_heads=8, causal=True))
