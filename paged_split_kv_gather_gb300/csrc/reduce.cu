@@ -49,12 +49,15 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceP
     const int kvh = static_cast<int>(unit / p.rows);
     const int row = static_cast<int>(unit - static_cast<int64_t>(kvh) * p.rows);
     const int D = p.head_dim;
+    // The first task is plan data (not written by the split kernel): read it early.
+    ReduceTask task = single;
+    if (p.tasks != nullptr && static_cast<int>(blockIdx.y) < num_tasks) task = p.tasks[blockIdx.y];
     // Launched as a programmatic dependent of the split kernel: everything above
     // overlaps its tail; wait here until its partials are complete and visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     for (int ti = blockIdx.y; ti < num_tasks; ti += gridDim.y) {
-        const ReduceTask task = p.tasks != nullptr ? p.tasks[ti] : single;
+        if (ti != static_cast<int>(blockIdx.y) && p.tasks != nullptr) task = p.tasks[ti];
         const int64_t base = (static_cast<int64_t>(task.src) * p.hk + kvh) * p.src_rows_stride + row;
         const int64_t step = static_cast<int64_t>(p.hk) * p.src_rows_stride;
 

@@ -35,25 +35,33 @@ struct StageGeom {
     static constexpr int STAGE_BYTES = 2 * HALF_BYTES;         // K regions then V regions
 };
 
-// Token range of a work item, with the run-time length clamped to the planned capacity.
+// Token range of a work item, with the run-time length clamped to the planned
+// capacity.  tok_end_alloc is the item's range by plan (its blocks), known
+// before the run-time length arrives; bad records a length outside [0, capacity]
+// for report_item_range.  No branch depends on the loaded length here, so the
+// producer's page-table loads can be issued while it is in flight.
 struct ItemRange {
-    int L, tok_begin, tok_end, n_stage;
+    int L, tok_begin, tok_end, n_stage, tok_end_alloc;
+    bool bad;
 };
 
 template <int TOK = kStageTokens>
 __device__ __forceinline__ ItemRange item_range(const SplitParams& p, const WorkItem& it) {
-    int L = p.seq_lens[it.seq];
+    const int L0 = p.seq_lens[it.seq];
     const int cap = p.capacity[it.seq];
-    if (L > cap || L < 0) {
-        if (threadIdx.x == 0) atomicOr(p.err, FDEC_DEVERR_SEQ_LEN);
-        L = L < 0 ? 0 : cap;
-    }
     ItemRange r;
-    r.L = L;
+    r.bad = L0 > cap || L0 < 0;
+    r.L = L0 < 0 ? 0 : (L0 > cap ? cap : L0);
     r.tok_begin = it.block_begin * kBlockTokens;
-    r.tok_end = min(it.block_end * kBlockTokens, L);
+    r.tok_end_alloc = it.block_end * kBlockTokens;
+    r.tok_end = min(r.tok_end_alloc, r.L);
     r.n_stage = r.tok_end > r.tok_begin ? (r.tok_end - r.tok_begin + TOK - 1) / TOK : 0;
     return r;
+}
+
+// One thread of the CTA flags a length outside [0, capacity] (it was clamped).
+__device__ __forceinline__ void report_item_range(const SplitParams& p, const ItemRange& ir) {
+    if (ir.bad) atomicOr(p.err, FDEC_DEVERR_SEQ_LEN);
 }
 
 // Initialise the 2S full and S empty barriers (thread 0).  Pages of >= 8 tokens
@@ -73,30 +81,35 @@ __device__ __forceinline__ void init_stage_barriers(uint64_t* full, uint64_t* em
 
 // The producer warp: fills stage i (TOK tokens) into slot i % S once the slot is released.
 template <int D, int S, int TOK = kStageTokens>
-__device__ void produce_stages(const SplitParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv, uint64_t* full,
+__device__ __forceinline__ void produce_stages(const SplitParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv, uint64_t* full,
                                uint64_t* empty, uint8_t* stages, int b, int kvh, const ItemRange& ir,
                                bool tma_mode) {
     using G = StageGeom<D, TOK>;
     static_assert(TOK % 32 == 0 && TOK <= 256, "stage rows");
     const int lane = threadIdx.x & 31;
-    const int tok_begin = ir.tok_begin, tok_end = ir.tok_end, n_stage = ir.n_stage;
-    if (n_stage == 0) return;
+    const int tok_begin = ir.tok_begin;
     const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride;
     const int page_mask = (1 << p.page_shift) - 1;
     int issued = 0;
     bool ok = true;
     if (tma_mode) {
         // Boxes of BR token rows, NB boxes per stage; the page id of box n is
-        // held by lane n % 32, one group of 32 boxes ahead.
+        // held by lane n % 32, one group of 32 boxes ahead.  The first two groups
+        // are loaded before the run-time length is known (bounded by the item's
+        // planned blocks and the table row, so every read is in bounds; ids of
+        // boxes past the length are never used).
         const int BR = min(1 << p.page_shift, TOK);
         const int NB = TOK / BR;
-        const int n_box = (tok_end - tok_begin + BR - 1) / BR;
-        const uint32_t box_bytes = static_cast<uint32_t>(BR) * 2u * (2u * D);  // K and V
         auto box_page = [&](int n) -> int {
-            return n < n_box ? __ldg(pt + ((tok_begin + n * BR) >> p.page_shift)) : -1;
+            const int t = tok_begin + n * BR;
+            return (t < ir.tok_end_alloc && (t >> p.page_shift) < p.pt_stride) ? __ldg(pt + (t >> p.page_shift)) : -1;
         };
         int pid = box_page(lane);
         int pid_next = box_page(32 + lane);
+        const int tok_end = ir.tok_end, n_stage = ir.n_stage;
+        if (n_stage == 0) return;
+        const int n_box = (tok_end - tok_begin + BR - 1) / BR;
+        const uint32_t box_bytes = static_cast<uint32_t>(BR) * 2u * (2u * D);  // K and V
         int group = 0;
         for (int i = 0; i < n_stage; ++i) {
             const int s = i % S;
@@ -145,6 +158,8 @@ __device__ void produce_stages(const SplitParams& p, const CUtensorMap* tmk, con
         }
     } else {
         // Small pages: 16-byte cp.async per (row, chunk) into the swizzled layout.
+        const int tok_end = ir.tok_end, n_stage = ir.n_stage;
+        if (n_stage == 0) return;
         constexpr int CHUNKS = D / 8;
         for (int i = 0; i < n_stage; ++i) {
             const int s = i % S;

@@ -120,16 +120,24 @@ split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUte
     const int kvh = blockIdx.y;
     const int row0 = blockIdx.z * RC;
 
-    const ItemRange ir = item_range(p, it);
-    const int L = ir.L, tok_begin = ir.tok_begin, tok_end = ir.tok_end, n_stage = ir.n_stage;
     const bool tma_mode = p.page_shift >= 3;  // pages of >= 8 tokens
     if (threadIdx.x == 0) init_stage_barriers<S>(full, empty, tma_mode);
-    if (warp == NW && lane == 0 && tma_mode) {
-        prefetch_tmap(&tmk);
-        prefetch_tmap(&tmv);
+    __syncthreads();  // barriers initialised (nothing before this waits on memory)
+    const ItemRange ir = item_range(p, it);
+
+    if (warp == NW) {
+        // The producer starts at once: its page-table reads overlap the length and q loads.
+        if (lane == 0 && tma_mode) {
+            prefetch_tmap(&tmk);
+            prefetch_tmap(&tmv);
+        }
+        produce_stages<D, S>(p, &tmk, &tmv, full, empty, stages, b, kvh, ir, tma_mode);
+        return;
     }
+    if (threadIdx.x == 0) report_item_range(p, ir);
+    const int L = ir.L, tok_begin = ir.tok_begin, tok_end = ir.tok_end, n_stage = ir.n_stage;
     // The group's query rows in fp32, pre-multiplied by scale*log2(e).
-    for (int idx = threadIdx.x; idx < RC * D; idx += Lay::THREADS) {
+    for (int idx = threadIdx.x; idx < RC * D; idx += NW * 32) {
         const int r = idx / D;
         const int d = idx - r * D;
         const int row = row0 + r;
@@ -143,12 +151,7 @@ split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUte
         }
         q_s[idx] = v;
     }
-    __syncthreads();
-
-    if (warp == NW) {
-        produce_stages<D, S>(p, &tmk, &tmv, full, empty, stages, b, kvh, ir, tma_mode);
-        return;
-    }
+    named_barrier(1, NW * 32);
 
     // ---------------------------------------------------------------------- consumers
     float2 o2[RC][DP];

@@ -131,15 +131,23 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
     const int b = it.seq;
     const int kvh = blockIdx.y;
     const int row0 = blockIdx.z * RC;
-    const ItemRange ir = item_range(p, it);
     const bool tma_mode = p.page_shift >= 3;
     if (threadIdx.x == 0) init_stage_barriers<S>(full, empty, tma_mode);
-    if (warp == NW && lane == 0 && tma_mode) {
-        prefetch_tmap(&tmk);
-        prefetch_tmap(&tmv);
+    __syncthreads();  // barriers initialised (nothing before this waits on memory)
+    const ItemRange ir = item_range(p, it);
+
+    if (warp == NW) {
+        // The producer starts at once: its page-table reads overlap the length and q loads.
+        if (lane == 0 && tma_mode) {
+            prefetch_tmap(&tmk);
+            prefetch_tmap(&tmv);
+        }
+        produce_stages<D, S>(p, &tmk, &tmv, full, empty, stages, b, kvh, ir, tma_mode);
+        return;
     }
+    if (threadIdx.x == 0) report_item_range(p, ir);
     // The group's query rows, as stored (16-bit); rows past the group are zero.
-    for (int idx = threadIdx.x; idx < RC * D; idx += Lay::THREADS) {
+    for (int idx = threadIdx.x; idx < RC * D; idx += NW * 32) {
         const int r = idx / D;
         const int d = idx - r * D;
         const int row = row0 + r;
@@ -152,12 +160,7 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
         }
         q_s[idx] = v;
     }
-    __syncthreads();
-
-    if (warp == NW) {
-        produce_stages<D, S>(p, &tmk, &tmv, full, empty, stages, b, kvh, ir, tma_mode);
-        return;
-    }
+    named_barrier(1, NW * 32);
 
     // ---------------------------------------------------------------------- consumers
     const int g = lane >> 2;   // fragment row (and row + 8)

@@ -203,6 +203,7 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         produce_stages<D, S, TOK>(p, &tmk, &tmv, full, empty, stages, b, kvh, ir, tma_mode);
+        if (lane == 0) report_item_range(p, ir);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n_tiles > 0) {
