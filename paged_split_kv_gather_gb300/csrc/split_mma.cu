@@ -1,4 +1,4 @@
-// split_mma.cu -- instantiations of the tensor-core split kernel (head_dim 64, 128, 192).
+// split_mma.cu -- instantiations of the tensor-core split kernel (head_dim 64, 128, 192, 256).
 #include "split_mma_kernel.cuh"
 
 namespace fdec {
@@ -15,6 +15,9 @@ cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tk, const 
         case 192:
             return bf16 ? launch_split_mma_one<192, true>(p, tk, tv, grid, s, launch)
                         : launch_split_mma_one<192, false>(p, tk, tv, grid, s, launch);
+        case 256:
+            return bf16 ? launch_split_mma_one<256, true>(p, tk, tv, grid, s, launch)
+                        : launch_split_mma_one<256, false>(p, tk, tv, grid, s, launch);
         default:
             return cudaErrorInvalidValue;
     }
@@ -25,6 +28,7 @@ size_t split_mma_smem_bytes(int head_dim) {
         case 64: return MmaLayout<64>::SMEM;
         case 128: return MmaLayout<128>::SMEM;
         case 192: return MmaLayout<192>::SMEM;
+        case 256: return MmaLayout<256>::SMEM;
         default: return 0;
     }
 }
@@ -34,6 +38,7 @@ int split_mma_threads(int head_dim) {
         case 64: return MmaLayout<64>::THREADS;
         case 128: return MmaLayout<128>::THREADS;
         case 192: return MmaLayout<192>::THREADS;
+        case 256: return MmaLayout<256>::THREADS;
         default: return 0;
     }
 }

@@ -42,7 +42,12 @@ struct MmaLayout {
     // Two CTAs per SM (measured: 103 us against 131 us with one CTA of 7
     // consumers for 537 MB at 262144 tokens): each CTA gets half the shared
     // memory and four warps (3 consumers + the producer), 255 registers each.
+    // head_dim 256 fits three stages and two consumers per CTA.
     static constexpr int CTAS_PER_SM = 2;
+    // Q's A fragments stay in registers up to head_dim 192; at 256 the O
+    // accumulators take 128 registers and the fragments are re-read from shared
+    // memory (ldmatrix) at every k-step instead.
+    static constexpr bool Q_IN_REGS = D <= 192;
     static constexpr int BUDGET = 232448 / CTAS_PER_SM - 1024;
     static constexpr int FIXED = BAR_BYTES + Q_BYTES + ALIGN_SLACK;
     static constexpr int S_FIT = (BUDGET - FIXED) / G::STAGE_BYTES;
@@ -167,14 +172,13 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
     const int tq = lane & 3;   // fragment column pair
     const int mi = lane >> 3;  // ldmatrix: which 8x8 matrix this lane addresses
 
-    uint32_t qa[KSTEPS][4];
-    {
-        const uint32_t qbase = smem_addr(q_s);
-        const int qrow = (mi & 1) * 8 + (lane & 7);
+    constexpr int QREGS = Lay::Q_IN_REGS ? KSTEPS : 1;
+    uint32_t qa[QREGS][4];
+    const uint32_t q_lane = smem_addr(q_s) + ((mi & 1) * 8 + (lane & 7)) * (D * 2) + (mi >> 1) * 16;
+    if constexpr (Lay::Q_IN_REGS) {
         static_for<0, KSTEPS>([&](auto kk_) {
             constexpr int kk = decltype(kk_)::value;
-            ldmatrix_x4(qbase + qrow * (D * 2) + (2 * kk + (mi >> 1)) * 16, qa[kk][0], qa[kk][1], qa[kk][2],
-                        qa[kk][3]);
+            ldmatrix_x4(q_lane + 2 * kk * 16, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
         });
     }
     // ldmatrix row addresses within a stage (swizzled: chunk c of row r at c ^ (r & 7)).
@@ -222,12 +226,14 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
         for (int n = 0; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
         static_for<0, KSTEPS>([&](auto kk_) {
             constexpr int kk = decltype(kk_)::value;
+            constexpr int qk = Lay::Q_IN_REGS ? kk : 0;
+            if constexpr (!Lay::Q_IN_REGS) ldmatrix_x4(q_lane + 2 * kk * 16, qa[0][0], qa[0][1], qa[0][2], qa[0][3]);
 #pragma unroll
             for (int pr = 0; pr < 2; ++pr) {
                 uint32_t b0, b1, b2, b3;
                 ldmatrix_x4(kbase + (kk >> 2) * G::REGION_BYTES + kb_row[pr] + kb_x[kk & 3], b0, b1, b2, b3);
-                mma_16816<BF16>(sc[2 * pr], qa[kk], b0, b1);
-                mma_16816<BF16>(sc[2 * pr + 1], qa[kk], b2, b3);
+                mma_16816<BF16>(sc[2 * pr], qa[qk], b0, b1);
+                mma_16816<BF16>(sc[2 * pr + 1], qa[qk], b2, b3);
             }
         });
 

@@ -102,12 +102,11 @@ def test_auto_plan_balances_ragged_batches():
 
 def test_path_selection():
     assert fd.fdec_plan_get_info(_plan([100], path=fd.FDEC_PATH_SIMT))["path"] == fd.FDEC_PATH_SIMT
-    for d in (64, 128, 192):
+    for d in (64, 128, 192, 256):
         assert fd.fdec_plan_get_info(_plan([100], head_dim=d))["path"] == fd.FDEC_PATH_MMA
-    for d in (256, 512):
-        assert fd.fdec_plan_get_info(_plan([100], head_dim=d))["path"] == fd.FDEC_PATH_SIMT
+    assert fd.fdec_plan_get_info(_plan([100], head_dim=512))["path"] == fd.FDEC_PATH_SIMT
     with pytest.raises(fd.FdecError) as ei:
-        _plan([100], head_dim=256, path=fd.FDEC_PATH_MMA)
+        _plan([100], head_dim=512, path=fd.FDEC_PATH_MMA)
     assert ei.value.status_name == "FDEC_ERR_UNSUPPORTED"
     with pytest.raises(fd.FdecError) as ei:
         _plan([100], head_dim=64, path=fd.FDEC_PATH_TC)

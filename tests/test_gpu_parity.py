@@ -183,6 +183,21 @@ def test_tcgen05_and_mma_kernels_agree_on_the_prefill_chunk():
     assert float((l_tc - l_mma).abs().max()) <= 2 * 1e-4
 
 
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("page_size", [4, 16, 64])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_head_dim_256_on_both_kernels(path, page_size, dtype):
+    # 3 q positions x 6 heads per KV head = 18 rows: two 16-row groups on the tensor-core kernel
+    w = W.make(3, 3, 12, 2, 256, page_size, [7, 400, 1500], dtype=dtype, device="cuda", seed=page_size + 256,
+               causal=True, nan_guard=True, pool_pages=2 * (1500 // page_size + 8), peaked=True)
+    out, lse, pd = gpu_run(w, path=path, blocks_per_split=2)
+    assert pd.info["path"] == path
+    torch.cuda.synchronize()
+    assert pd.device_errors() == 0 and torch.isfinite(out).all()
+    ro, rl = oracle_run(w.to("cpu"))
+    assert_parity(out.cpu(), lse.cpu(), ro, rl, f"D256 path {path} page {page_size} {dtype}")
+
+
 # ------------------------------------------------------------------ plans and reductions
 
 @pytest.mark.parametrize("bps,fanin", [(1, 0), (1, 4), (3, 2), (7, 0), (10**6, 0)])
