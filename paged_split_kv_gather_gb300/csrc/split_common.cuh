@@ -98,7 +98,8 @@ __device__ __forceinline__ void produce_stages(const SplitParams& p, const CUten
         // are loaded before the run-time length is known (bounded by the item's
         // planned blocks and the table row, so every read is in bounds; ids of
         // boxes past the length are never used).
-        const int BR = min(1 << p.page_shift, TOK);
+        // (boxes never cross a page: a stage starts on a 64-token block boundary)
+        const int BR = min(1 << p.page_shift, min(TOK, kBlockTokens));
         const int NB = TOK / BR;
         auto box_page = [&](int n) -> int {
             const int t = tok_begin + n * BR;
