@@ -64,6 +64,48 @@ __device__ __forceinline__ void report_item_range(const SplitParams& p, const It
     if (ir.bad) atomicOr(p.err, FDEC_DEVERR_SEQ_LEN);
 }
 
+// Fetch the CTA's query rows: 16-byte chunk k of the (RC rows x D) block of 16-bit
+// values, by threads tid = 0 .. NTHREADS-1, chunk k at tid + i NTHREADS.  All
+// loads are issued before any of them is used (a loop that stores each value
+// before loading the next waits one memory round trip per iteration); rows past
+// p.rows are zero.  16-byte loads when q and its strides allow, else 2-byte loads.
+template <int RC, int D, int NTHREADS>
+struct QChunks {
+    static constexpr int CH = RC * D / 8;
+    static constexpr int PER = (CH + NTHREADS - 1) / NTHREADS;
+    uint4 v[PER];
+
+    __device__ __forceinline__ void load(const SplitParams& p, int b, int kvh, int row0, int tid) {
+        const bool vec = ((reinterpret_cast<uintptr_t>(p.q) | static_cast<uintptr_t>(p.q_stride_tok * 2) |
+                           static_cast<uintptr_t>(p.q_stride_head * 2)) & 15u) == 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int idx = tid + i * NTHREADS;
+            v[i] = make_uint4(0u, 0u, 0u, 0u);
+            const int r = idx / (D / 8);
+            const int row = row0 + r;
+            if (idx < CH && row < p.rows) {
+                const int qi = row / p.group;
+                const int h = kvh * p.group + (row - qi * p.group);
+                const uint16_t* src = p.q + static_cast<int64_t>(b * p.q_len + qi) * p.q_stride_tok +
+                                      static_cast<int64_t>(h) * p.q_stride_head + (idx - r * (D / 8)) * 8;
+                if (vec) {
+                    v[i] = __ldg(reinterpret_cast<const uint4*>(src));
+                } else {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = static_cast<uint32_t>(__ldg(src + 2 * e)) |
+                               (static_cast<uint32_t>(__ldg(src + 2 * e + 1)) << 16);
+                    v[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+        }
+    }
+    // chunk index of v[i] (valid when < CH)
+    __device__ __forceinline__ static int chunk(int tid, int i) { return tid + i * NTHREADS; }
+};
+
 // Initialise the 2S full and S empty barriers (thread 0).  Pages of >= 8 tokens
 // complete a stage with one expect-tx arrival (TMA); smaller pages with the 32
 // cp.async arrivals of the producer lanes.

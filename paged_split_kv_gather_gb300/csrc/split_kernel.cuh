@@ -136,20 +136,26 @@ split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUte
     }
     if (threadIdx.x == 0) report_item_range(p, ir);
     const int L = ir.L, tok_begin = ir.tok_begin, tok_end = ir.tok_end, n_stage = ir.n_stage;
-    // The group's query rows in fp32, pre-multiplied by scale*log2(e).
-    for (int idx = threadIdx.x; idx < RC * D; idx += NW * 32) {
-        const int r = idx / D;
-        const int d = idx - r * D;
-        const int row = row0 + r;
-        float v = 0.f;
-        if (row < p.rows) {
-            const int qi = row / p.group;
-            const int h = kvh * p.group + (row - qi * p.group);
-            v = load_16bit<BF16>(p.q + static_cast<int64_t>(b * p.q_len + qi) * p.q_stride_tok +
-                                 static_cast<int64_t>(h) * p.q_stride_head + d) *
-                p.scale_log2;
+    // The group's query rows in fp32 ([RC][D]), pre-multiplied by scale*log2(e).
+    {
+        QChunks<RC, D, NW * 32> qc;
+        qc.load(p, b, kvh, row0, threadIdx.x);
+#pragma unroll
+        for (int i = 0; i < qc.PER; ++i) {
+            const int idx = qc.chunk(threadIdx.x, i);
+            if (idx < qc.CH) {
+                const uint32_t w[4] = {qc.v[i].x, qc.v[i].y, qc.v[i].z, qc.v[i].w};
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 pr = unpack2<BF16>(w[e]);
+                    f[2 * e] = pr.x * p.scale_log2;
+                    f[2 * e + 1] = pr.y * p.scale_log2;
+                }
+                *reinterpret_cast<float4*>(q_s + idx * 8) = make_float4(f[0], f[1], f[2], f[3]);
+                *reinterpret_cast<float4*>(q_s + idx * 8 + 4) = make_float4(f[4], f[5], f[6], f[7]);
+            }
         }
-        q_s[idx] = v;
     }
     named_barrier(1, NW * 32);
 

@@ -151,19 +151,15 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
         return;
     }
     if (threadIdx.x == 0) report_item_range(p, ir);
-    // The group's query rows, as stored (16-bit); rows past the group are zero.
-    for (int idx = threadIdx.x; idx < RC * D; idx += NW * 32) {
-        const int r = idx / D;
-        const int d = idx - r * D;
-        const int row = row0 + r;
-        uint16_t v = 0;
-        if (row < p.rows) {
-            const int qi = row / p.group;
-            const int h = kvh * p.group + (row - qi * p.group);
-            v = p.q[static_cast<int64_t>(b * p.q_len + qi) * p.q_stride_tok + static_cast<int64_t>(h) * p.q_stride_head +
-                    d];
+    // The group's query rows, as stored (16-bit, [RC][D]); rows past the group are zero.
+    {
+        QChunks<RC, D, NW * 32> qc;
+        qc.load(p, b, kvh, row0, threadIdx.x);
+#pragma unroll
+        for (int i = 0; i < qc.PER; ++i) {
+            const int idx = qc.chunk(threadIdx.x, i);
+            if (idx < qc.CH) *reinterpret_cast<uint4*>(q_s + idx * 8) = qc.v[i];
         }
-        q_s[idx] = v;
     }
     named_barrier(1, NW * 32);
 

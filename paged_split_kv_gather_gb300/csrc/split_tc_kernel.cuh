@@ -169,30 +169,20 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
         tmem_relinquish();
     }
     // Q tiles: K-major, 128B-swizzled (two 64-dim regions per tile); absent rows are zero.
-    const bool q_vec = ((reinterpret_cast<uintptr_t>(p.q) | static_cast<uintptr_t>(p.q_stride_tok * 2) |
-                         static_cast<uintptr_t>(p.q_stride_head * 2)) & 15u) == 0;
-    for (int idx = threadIdx.x; idx < Lay::ROWS * (D / 8); idx += Lay::THREADS) {
-        const int r = idx / (D / 8);
-        const int c = idx - r * (D / 8);  // 16-byte chunk of the row
-        const int row = row0 + r;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (row < p.rows) {
-            const int qi = row / p.group;
-            const int h = kvh * p.group + (row - qi * p.group);
-            const uint16_t* src = p.q + static_cast<int64_t>(b * p.q_len + qi) * p.q_stride_tok +
-                                  static_cast<int64_t>(h) * p.q_stride_head + c * 8;
-            if (q_vec) {
-                v = __ldg(reinterpret_cast<const uint4*>(src));
-            } else {
-                uint32_t w[4];
+    {
+        QChunks<Lay::ROWS, D, Lay::THREADS> qc;
+        qc.load(p, b, kvh, row0, threadIdx.x);
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    w[e] = static_cast<uint32_t>(src[2 * e]) | (static_cast<uint32_t>(src[2 * e + 1]) << 16);
-                v = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int i = 0; i < qc.PER; ++i) {
+            const int idx = qc.chunk(threadIdx.x, i);
+            if (idx < qc.CH) {
+                const int r = idx / (D / 8);
+                const int c = idx - r * (D / 8);  // 16-byte chunk of the row
+                const int t = r / Lay::TM, rt = r - t * Lay::TM;
+                *reinterpret_cast<uint4*>(q_tiles + t * Lay::Q_BYTES + (c >> 3) * (Lay::TM * 128) +
+                                          sw128_offset(rt, c & 7)) = qc.v[i];
             }
         }
-        const int t = r / Lay::TM, rt = r - t * Lay::TM;
-        *reinterpret_cast<uint4*>(q_tiles + t * Lay::Q_BYTES + (c >> 3) * (Lay::TM * 128) + sw128_offset(rt, c & 7)) = v;
     }
     fence_proxy_async_shared();  // generic writes of Q, read by the tensor cores
     tc_fence_before_sync();
