@@ -381,6 +381,23 @@ def _dist():
     return world, rank, local
 
 
+def _max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: the job is done when its last replica is."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_throughput(world: int, bytes_per_rank_step: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank streams its own replica (weak scaling)."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def _make_inputs(length, device):
     from paged_split_kv_gather_gb300 import workloads as W
 
@@ -465,14 +482,11 @@ def _run_fdec(args):
     torch.cuda.synchronize()
     fd.fdec_plan_set_split_event(pd.plan, None)
     split_ms = float(np.mean([s.elapsed_time(m) for s, m in zip(starts, mids)]))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = _max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
     assert pd.device_errors() == 0, "device-side check fired during the benchmark"
 
-    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    value = _job_throughput(world, kv_bytes, ms_per_step)
     peak, peak_kind = _peaks()
     achieved = kv_bytes / (split_ms * 1e-3) / 1e9
 
