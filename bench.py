@@ -219,10 +219,10 @@ def _config_points(dev, calls, hbm_peak):
 
     flush = L2Flush(torch, dev)
 
-    def runner(w, capacities=None):
+    def runner(w, capacities=None, **plan_opts):
         caps = w.seq_lens if capacities is None else capacities
         pd = fd.PagedDecode(caps, w.q_len, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
-                            w.causal, device=dev)
+                            w.causal, device=dev, **plan_opts)
         table = torch.as_tensor(w.page_table, device=dev)
         lens = torch.as_tensor(np.asarray(caps, dtype=np.int32), device=dev)
         out = torch.empty((w.batch, w.q_len, w.num_qo_heads, w.head_dim), device=dev)
@@ -260,6 +260,20 @@ def _config_points(dev, calls, hbm_peak):
         pd, run = runner(w)
         graph[str(L)] = round(_time_graph(torch, run, 20, flush), 2)
     points["long_context_graph_us_per_call"] = graph
+
+    # Controlled comparison: the planned split against one split per (sequence, KV
+    # head) with no reduction (the serial shape the split path replaces).
+    versus = {}
+    for L in (2100, 4800, 32768):
+        w = W.long_context(L, device=dev)
+        pd, run = runner(w)
+        planned, _ = _time_calls(torch, run, calls, flush)
+        splits = int(pd.info["max_splits"])
+        pd1, run1 = runner(w, blocks_per_split=1 << 30)
+        single, _ = _time_calls(torch, run1, max(5, calls // 5), flush)
+        versus[str(L)] = {"planned_us": round(planned, 2), "planned_splits": splits, "single_split_us": round(single, 2)}
+        del pd, run, pd1, run1, w
+    points["planned_vs_single_split"] = versus
 
     # No-cliff sweep: one pool of 8192 tokens, plans of capacity L (the page table's
     # prefix); per-call times from graphs of 20 (eviction, call) pairs, whose

@@ -86,7 +86,11 @@ def gpu_run(w: Workload, capacities=None, seq_lens=None, stream=None, **plan_opt
     lse = torch.full((w.batch, w.q_len, w.num_qo_heads), float("nan"), device=dev)
     table = torch.as_tensor(w.page_table, device=dev)
     lens = torch.as_tensor(w.seq_lens if seq_lens is None else seq_lens, dtype=torch.int32, device=dev)
+    # every storage the workload holds (q and the K/V pools) must come back bit-identical
+    before = [t.clone() for t in w.keep]
     pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale, stream=stream)
+    for a, b in zip(before, w.keep):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), "an input buffer changed"
     return out, lse, pd
 
 

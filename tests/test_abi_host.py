@@ -226,3 +226,17 @@ def test_upload_refuses_null_and_misaligned_workspace():
     lib = fd._load()
     assert fd.STATUS_NAMES[lib.fdec_plan_upload(plan.handle, None, None)] == "FDEC_ERR_INVALID_ARG"
     assert fd.STATUS_NAMES[lib.fdec_plan_upload(plan.handle, 0x1008, None)] == "FDEC_ERR_WORKSPACE"
+
+
+def test_binding_refuses_views_without_a_unit_dim_stride():
+    import torch
+
+    kv = torch.zeros(4, 2, 16, 64, dtype=torch.bfloat16)
+    assert fd.kv_desc(kv).stride_token == 64
+    with pytest.raises(ValueError):
+        fd.kv_desc(kv.transpose(2, 3))          # dim stride 16
+    with pytest.raises(ValueError):
+        fd.kv_desc(kv[:, :, :, ::2])             # dim stride 2
+    q = torch.zeros(2, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fd._q_strides(q.transpose(2, 3).contiguous().transpose(2, 3))
