@@ -86,7 +86,7 @@ typedef struct fdec_plan_s* fdec_plan_t;
 
 /*
  * Split-kernel paths.  SIMT: fp32 FMA (every head_dim).  MMA: warp-level
- * tensor-core MMA on 16-row query groups (head_dim 64, 128, 192, 256), the decode
+ * tensor-core MMA on 16-row query groups (every head_dim), the decode
  * default.  TC: 5th-generation tensor cores (tcgen05, accumulators in tensor
  * memory) on 128-row query tiles, head_dim 128; chosen by AUTO when q_len x
  * group > 16, where attention over the gathered pages turns into a dense
@@ -101,7 +101,7 @@ typedef struct {
     int blocks_per_split;  /* 64-token blocks per split; 0 = auto; 1 = one partial per block */
     int reducer_fanin;     /* partials merged per reduction task; 0 = auto (256); >= 2 */
     int path;              /* FDEC_PATH_AUTO (TC when head_dim 128 and q_len x group > 16, else MMA
-                              where built, else SIMT), _SIMT, _MMA (head_dim 64 ... 256),
+                              where built, else SIMT), _SIMT, _MMA (every head_dim),
                               _TC (head_dim 128) */
     int num_sms;           /* 0 = query the current device; > 0 plans without a device */
 } fdec_plan_opts;

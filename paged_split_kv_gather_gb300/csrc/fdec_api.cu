@@ -329,10 +329,10 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
         return fail(FDEC_ERR_INVALID_ARG, "invalid plan options");
     if (o.path != FDEC_PATH_AUTO && o.path != FDEC_PATH_SIMT && o.path != FDEC_PATH_MMA && o.path != FDEC_PATH_TC)
         return fail(FDEC_ERR_INVALID_ARG, "invalid path option");
-    const bool mma_ok = head_dim == 64 || head_dim == 128 || head_dim == 192 || head_dim == 256;
+    const bool mma_ok = head_dim_supported(head_dim);  // every supported head_dim
     const bool tc_ok = head_dim == 128;
     if (o.path == FDEC_PATH_MMA && !mma_ok)
-        return fail(FDEC_ERR_UNSUPPORTED, "the tensor-core path supports head_dim 64, 128, 192 and 256");
+        return fail(FDEC_ERR_UNSUPPORTED, "the tensor-core path supports head_dim 64, 128, 192, 256 and 512");
     if (o.path == FDEC_PATH_TC && !tc_ok)
         return fail(FDEC_ERR_UNSUPPORTED, "the tcgen05 path supports head_dim 128");
     const long long rows_ll = static_cast<long long>(q_len) * (num_qo_heads / num_kv_heads);

@@ -89,7 +89,7 @@ cudaError_t launch_split_d256(const SplitParams& p, const CUtensorMap& tk, const
 cudaError_t launch_split_d512(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int rc,
                                bool bf16, dim3 grid, cudaStream_t s, bool launch);
 
-// The tensor-core split kernel (head_dim 64, 128, 192, 256; query rows in groups of 16).
+// The tensor-core split kernel (head_dim 64, 128, 192, 256, 512; query rows in groups of 16).
 cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int head_dim,
                              bool bf16, dim3 grid, cudaStream_t s, bool launch);
 size_t split_mma_smem_bytes(int head_dim);

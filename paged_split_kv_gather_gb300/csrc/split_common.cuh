@@ -110,13 +110,14 @@ struct QChunks {
 // complete a stage with one expect-tx arrival (TMA); smaller pages with the 32
 // cp.async arrivals of the producer lanes.
 template <int S>
-__device__ __forceinline__ void init_stage_barriers(uint64_t* full, uint64_t* empty, bool tma_mode) {
+__device__ __forceinline__ void init_stage_barriers(uint64_t* full, uint64_t* empty, bool tma_mode,
+                                                    uint32_t empty_count = 1) {
     const uint32_t full_count = tma_mode ? 1u : 32u;
 #pragma unroll
     for (int s = 0; s < S; ++s) {
         mbar_init(smem_addr(&full[s]), full_count);
         mbar_init(smem_addr(&full[S + s]), full_count);
-        mbar_init(smem_addr(&empty[s]), 1);
+        mbar_init(smem_addr(&empty[s]), empty_count);
     }
     fence_mbar_init();
 }
@@ -283,11 +284,12 @@ __device__ __forceinline__ void zero_v_tail(uint8_t* stage, int nv, int tid = th
 // sm_m [NW][RC], sm_l [NW][RC], sm_o [NW][RC][D] and passed a barrier: merge the
 // NW states by log-sum-exp (m in log2 units) and write the split's partial or,
 // when one split covers the sequence, out = O / L and lse = ln 2 * (M + log2 L).
-template <int NW, int RC, int D>
+// NTHREADS consumer threads (from thread 0) share the work.
+template <int NW, int RC, int D, int NTHREADS = NW * 32>
 __device__ __forceinline__ void merge_and_store(const SplitParams& p, const WorkItem& it, int kvh, int row0,
                                                 const float* sm_m, const float* sm_l, const float* sm_o) {
     constexpr float kLn2 = 0.69314718055994530942f;
-    for (int idx = threadIdx.x; idx < RC * D; idx += NW * 32) {
+    for (int idx = threadIdx.x; idx < RC * D; idx += NTHREADS) {
         const int r = idx / D;
         const int d = idx - r * D;
         const int row = row0 + r;

@@ -1,4 +1,4 @@
-// split_mma.cu -- instantiations of the tensor-core split kernel (head_dim 64, 128, 192, 256).
+// split_mma.cu -- instantiations of the tensor-core split kernel (head_dim 64, 128, 192, 256, 512).
 #include "split_mma_kernel.cuh"
 
 namespace fdec {
@@ -18,6 +18,9 @@ cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tk, const 
         case 256:
             return bf16 ? launch_split_mma_one<256, true>(p, tk, tv, grid, s, launch)
                         : launch_split_mma_one<256, false>(p, tk, tv, grid, s, launch);
+        case 512:
+            return bf16 ? launch_split_mma_one<512, true>(p, tk, tv, grid, s, launch)
+                        : launch_split_mma_one<512, false>(p, tk, tv, grid, s, launch);
         default:
             return cudaErrorInvalidValue;
     }
@@ -29,6 +32,7 @@ size_t split_mma_smem_bytes(int head_dim) {
         case 128: return MmaLayout<128>::SMEM;
         case 192: return MmaLayout<192>::SMEM;
         case 256: return MmaLayout<256>::SMEM;
+        case 512: return MmaLayout<512>::SMEM;
         default: return 0;
     }
 }
@@ -39,6 +43,7 @@ int split_mma_threads(int head_dim) {
         case 128: return MmaLayout<128>::THREADS;
         case 192: return MmaLayout<192>::THREADS;
         case 256: return MmaLayout<256>::THREADS;
+        case 512: return MmaLayout<512>::THREADS;
         default: return 0;
     }
 }

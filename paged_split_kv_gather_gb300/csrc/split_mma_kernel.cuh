@@ -42,8 +42,14 @@ struct MmaLayout {
     // Two CTAs per SM (measured: 103 us against 131 us with one CTA of 7
     // consumers for 537 MB at 262144 tokens): each CTA gets half the shared
     // memory and four warps (3 consumers + the producer), 255 registers each.
-    // head_dim 256 fits three stages and two consumers per CTA.
-    static constexpr int CTAS_PER_SM = 2;
+    // head_dim 256 fits three stages and two consumers per CTA; head_dim 512
+    // runs one CTA per SM (stages of 64 KB).
+    static constexpr int CTAS_PER_SM = D <= 256 ? 2 : 1;
+    // head_dim 512: the O accumulators of all 512 columns would need 256
+    // registers, so two consumer warps share each stage, both computing S and
+    // each accumulating P V for one half of the columns (DH).
+    static constexpr int DSPLIT = D > 256 ? 2 : 1;
+    static constexpr int DH = D / DSPLIT;
     // Q's A fragments stay in registers up to head_dim 192; at 256 the O
     // accumulators take 128 registers and the fragments are re-read from shared
     // memory (ldmatrix) at every k-step instead.
@@ -52,12 +58,13 @@ struct MmaLayout {
     static constexpr int FIXED = BAR_BYTES + Q_BYTES + ALIGN_SLACK;
     static constexpr int S_FIT = (BUDGET - FIXED) / G::STAGE_BYTES;
     static constexpr int S = S_FIT > 16 ? 16 : S_FIT;
-    static constexpr int NW = (S - 1) < 3 ? (S - 1) : 3;
+    static constexpr int NP = (S - 1) < 3 ? (S - 1) : 3;  // consumer groups (stages in flight at once)
+    static constexpr int NW = NP * DSPLIT;                 // consumer warps
     static constexpr int THREADS = (NW + 1) * 32;
     static constexpr int SMEM = FIXED + S * G::STAGE_BYTES;
-    static_assert(S >= NW + 1, "stage ring too small");
+    static_assert(S >= NP + 1, "stage ring too small");
     static_assert(3 * S * 8 <= BAR_BYTES, "barrier area too small");
-    static_assert(NW * RC * (D + 2) * 4 <= S * G::STAGE_BYTES, "merge scratch must fit the stage area");
+    static_assert(NP * RC * (D + 2) * 4 <= S * G::STAGE_BYTES, "merge scratch must fit the stage area");
 };
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -116,8 +123,11 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
     constexpr int NW = Lay::NW;
     constexpr int S = Lay::S;
     constexpr int RC = Lay::RC;
-    constexpr int KSTEPS = D / 16;  // k-steps of S = Q K^T
-    constexpr int NT = D / 8;       // n-tiles of O
+    constexpr int NP = Lay::NP;          // consumer groups, one stage each
+    constexpr int DSPLIT = Lay::DSPLIT;  // warps per group (each owns DH columns of O)
+    constexpr int DH = Lay::DH;
+    constexpr int KSTEPS = D / 16;       // k-steps of S = Q K^T
+    constexpr int NT = DH / 8;           // n-tiles of this warp's O
 
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -137,7 +147,7 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
     const int kvh = blockIdx.y;
     const int row0 = blockIdx.z * RC;
     const bool tma_mode = p.page_shift >= 3;
-    if (threadIdx.x == 0) init_stage_barriers<S>(full, empty, tma_mode);
+    if (threadIdx.x == 0) init_stage_barriers<S>(full, empty, tma_mode, DSPLIT);
     __syncthreads();  // barriers initialised (nothing before this waits on memory)
     const ItemRange ir = item_range(p, it);
 
@@ -204,7 +214,10 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
     const uint32_t stages_base = smem_addr(stages);
     bool ok = true;
 
-    for (int i = warp; i < ir.n_stage; i += NW) {
+    const int grp = warp / DSPLIT;             // consumer group: stages grp, grp + NP, ...
+    const int half = warp - grp * DSPLIT;      // which DH columns of O this warp accumulates
+    const uint32_t v_half = static_cast<uint32_t>(half * (DH / 64) * G::REGION_BYTES);
+    for (int i = grp; i < ir.n_stage; i += NP) {
         const int s = i % S;
         if (!wait_stage<S>(full, i)) {
             ok = false;
@@ -295,10 +308,11 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
         // O += P V
 #pragma unroll
         for (int k2 = 0; k2 < 2; ++k2) {
-            static_for<0, D / 16>([&](auto jp_) {
-                constexpr int jp = decltype(jp_)::value;
+            static_for<0, DH / 16>([&](auto jp_) {
+                constexpr int jp = decltype(jp_)::value;  // 16-column group of this warp's half
                 uint32_t b0, b1, b2, b3;
-                ldmatrix_x4_trans(vbase + (jp >> 2) * G::REGION_BYTES + vb_row[k2] + vb_x[jp & 3], b0, b1, b2, b3);
+                ldmatrix_x4_trans(vbase + v_half + (jp >> 2) * G::REGION_BYTES + vb_row[k2] + vb_x[jp & 3], b0, b1, b2,
+                                  b3);
                 mma_16816<BF16>(o[2 * jp], ph[k2], b0, b1);
                 mma_16816<BF16>(o[2 * jp], pl[k2], b0, b1);
                 mma_16816<BF16>(o[2 * jp + 1], ph[k2], b2, b3);
@@ -320,22 +334,23 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
     named_barrier(1, NW * 32);  // every consumer is done with the stage buffers
     // The reduction (launched as a programmatic dependent) may start its launch now.
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    float* sm_m = reinterpret_cast<float*>(stages);  // [NW][RC]
-    float* sm_l = sm_m + NW * RC;                     // [NW][RC]
-    float* sm_o = sm_l + NW * RC;                     // [NW][RC][D]
-    if (tq == 0) {
-        sm_m[warp * RC + g] = mrow[0];
-        sm_m[warp * RC + g + 8] = mrow[1];
-        sm_l[warp * RC + g] = lrow[0];
-        sm_l[warp * RC + g + 8] = lrow[1];
+    float* sm_m = reinterpret_cast<float*>(stages);  // [NP][RC]
+    float* sm_l = sm_m + NP * RC;                     // [NP][RC]
+    float* sm_o = sm_l + NP * RC;                     // [NP][RC][D]
+    if (tq == 0 && half == 0) {  // the warps of a group hold the same m and l
+        sm_m[grp * RC + g] = mrow[0];
+        sm_m[grp * RC + g + 8] = mrow[1];
+        sm_l[grp * RC + g] = lrow[0];
+        sm_l[grp * RC + g + 8] = lrow[1];
     }
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-        *reinterpret_cast<float2*>(sm_o + (warp * RC + g) * D + 8 * n + 2 * tq) = make_float2(o[n][0], o[n][1]);
-        *reinterpret_cast<float2*>(sm_o + (warp * RC + g + 8) * D + 8 * n + 2 * tq) = make_float2(o[n][2], o[n][3]);
+        *reinterpret_cast<float2*>(sm_o + (grp * RC + g) * D + half * DH + 8 * n + 2 * tq) = make_float2(o[n][0], o[n][1]);
+        *reinterpret_cast<float2*>(sm_o + (grp * RC + g + 8) * D + half * DH + 8 * n + 2 * tq) =
+            make_float2(o[n][2], o[n][3]);
     }
     named_barrier(1, NW * 32);
-    merge_and_store<NW, RC, D>(p, it, kvh, row0, sm_m, sm_l, sm_o);
+    merge_and_store<NP, RC, D, NW * 32>(p, it, kvh, row0, sm_m, sm_l, sm_o);
 }
 
 template <int D, bool BF16>

@@ -102,12 +102,9 @@ def test_auto_plan_balances_ragged_batches():
 
 def test_path_selection():
     assert fd.fdec_plan_get_info(_plan([100], path=fd.FDEC_PATH_SIMT))["path"] == fd.FDEC_PATH_SIMT
-    for d in (64, 128, 192, 256):
+    for d in (64, 128, 192, 256, 512):
         assert fd.fdec_plan_get_info(_plan([100], head_dim=d))["path"] == fd.FDEC_PATH_MMA
-    assert fd.fdec_plan_get_info(_plan([100], head_dim=512))["path"] == fd.FDEC_PATH_SIMT
-    with pytest.raises(fd.FdecError) as ei:
-        _plan([100], head_dim=512, path=fd.FDEC_PATH_MMA)
-    assert ei.value.status_name == "FDEC_ERR_UNSUPPORTED"
+        assert fd.fdec_plan_get_info(_plan([100], head_dim=d, path=fd.FDEC_PATH_SIMT))["path"] == fd.FDEC_PATH_SIMT
     with pytest.raises(fd.FdecError) as ei:
         _plan([100], head_dim=64, path=fd.FDEC_PATH_TC)
     assert ei.value.status_name == "FDEC_ERR_UNSUPPORTED"
@@ -135,9 +132,12 @@ def test_row_groups_cover_all_query_rows():
     p = _plan([8200] * 4, q_len=8, num_qo_heads=32, num_kv_heads=8, causal=True)
     info = fd.fdec_plan_get_info(p)
     assert info["rows_per_group"] * info["row_groups"] >= 32
-    p = _plan([1000], num_qo_heads=16, num_kv_heads=8, head_dim=512, q_len=3)
+    p = _plan([1000], num_qo_heads=16, num_kv_heads=8, head_dim=512, q_len=3, path=fd.FDEC_PATH_SIMT)
     info = fd.fdec_plan_get_info(p)
     assert info["rows_per_group"] <= 4 and info["rows_per_group"] * info["row_groups"] >= 6
+    p = _plan([1000], num_qo_heads=16, num_kv_heads=8, head_dim=512, q_len=3)  # tensor cores: one 16-row group
+    info = fd.fdec_plan_get_info(p)
+    assert info["rows_per_group"] == 16 and info["row_groups"] == 1
 
 
 @pytest.mark.parametrize("kw,status", [

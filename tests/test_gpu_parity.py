@@ -183,19 +183,22 @@ def test_tcgen05_and_mma_kernels_agree_on_the_prefill_chunk():
     assert float((l_tc - l_mma).abs().max()) <= 2 * 1e-4
 
 
+@pytest.mark.parametrize("head_dim", [256, 512])
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("page_size", [4, 16, 64])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_head_dim_256_on_both_kernels(path, page_size, dtype):
-    # 3 q positions x 6 heads per KV head = 18 rows: two 16-row groups on the tensor-core kernel
-    w = W.make(3, 3, 12, 2, 256, page_size, [7, 400, 1500], dtype=dtype, device="cuda", seed=page_size + 256,
-               causal=True, nan_guard=True, pool_pages=2 * (1500 // page_size + 8), peaked=True)
+def test_large_head_dims_on_both_kernels(head_dim, path, page_size, dtype):
+    # 3 q positions x 6 heads per KV head = 18 rows: two 16-row groups on the tensor-core kernel;
+    # head_dim 512 splits O between the two warps of each consumer group
+    w = W.make(3, 3, 12, 2, head_dim, page_size, [7, 400, 1500], dtype=dtype, device="cuda",
+               seed=page_size + head_dim, causal=True, nan_guard=True, pool_pages=2 * (1500 // page_size + 8),
+               peaked=True)
     out, lse, pd = gpu_run(w, path=path, blocks_per_split=2)
     assert pd.info["path"] == path
     torch.cuda.synchronize()
     assert pd.device_errors() == 0 and torch.isfinite(out).all()
     ro, rl = oracle_run(w.to("cpu"))
-    assert_parity(out.cpu(), lse.cpu(), ro, rl, f"D256 path {path} page {page_size} {dtype}")
+    assert_parity(out.cpu(), lse.cpu(), ro, rl, f"D{head_dim} path {path} page {page_size} {dtype}")
 
 
 # ------------------------------------------------------------------ plans and reductions
