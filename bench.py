@@ -253,6 +253,31 @@ def _config_points(dev, calls, hbm_peak):
         del pd, run, w
         torch.cuda.empty_cache()
 
+    # Paged append (the cache's write side): one new token per sequence (a decode
+    # step) and a 512-token chunk per sequence (a prefill chunk), 64 sequences of
+    # 4096-token capacity, 8 KV heads, D 128.  Bytes = new K and V rows read + written.
+    wa = W.make(64, 1, 32, 8, 128, 16, [4096] * 64, dtype="bf16", device=dev, seed=11)
+    table = torch.as_tensor(wa.page_table, device=dev)
+    app = {}
+    for n_per in (1, 512):
+        n = 64 * n_per
+        k_new = torch.randn(n, 8, 128, device=dev).to(torch.bfloat16)
+        v_new = torch.randn(n, 8, 128, device=dev).to(torch.bfloat16)
+        bi = torch.arange(64, dtype=torch.int32, device=dev).repeat_interleave(n_per)
+        pos = (torch.arange(n_per, dtype=torch.int32, device=dev) + 3000).repeat(64)
+
+        def run_append(k_new=k_new, v_new=v_new, bi=bi, pos=pos):
+            fd.fdec_append(k_new, v_new, bi, pos, wa.k, wa.v, table, 16)
+
+        run_append()
+        med, mn = _time_calls(torch, run_append, calls, flush)
+        nbytes = 2 * 2 * n * 8 * 128 * 2
+        app[f"tokens_per_seq_{n_per}"] = {"us_per_call": round(med, 2), "us_min": round(mn, 2), "bytes": nbytes,
+                                          "GB_per_s": round(nbytes / (med * 1e-6) / 1e9, 1)}
+    points["paged_append"] = app
+    del wa, table
+    torch.cuda.empty_cache()
+
     # Graph-replayed long-context points where launch latency matters.
     graph = {}
     for L in (1900, 2000, 2100, 3000, 4800):

@@ -188,6 +188,35 @@ fdec_status fdec_run(fdec_plan_t plan, const void* q, int64_t q_stride_tok, int6
 fdec_status fdec_merge_states(const float* o, const float* lse, int n_states, int rows,
                               int head_dim, float* o_out, float* lse_out, cudaStream_t stream);
 
+/*
+ * Paged KV append, the write side of the cache (FlashInfer PR "Stop declaring
+ * the paged KV cache mutated on read-only attention ops", append notes: the
+ * append op genuinely writes the cache; K and V are best given as separate
+ * storage).  For each new token i of n_tokens, with b = batch_indices[i] and
+ * position t = positions[i] (its index within sequence b):
+ *   page = page_table[b * page_table_stride + t / page_size], slot = t % page_size,
+ *   K[page, h, slot, :] = k_new[i, h, :] and V[page, h, slot, :] = v_new[i, h, :]
+ * for every KV head h.  Nothing else of K or V is written.
+ *   k_new, v_new: 16-bit device [n_tokens][num_kv_heads][head_dim] with token
+ *      stride new_stride_tok and head stride new_stride_head (elements; unit
+ *      dim stride; 16-byte aligned rows).
+ *   batch_indices, positions: int32 device [n_tokens].
+ *   k, v: the cache pools (fdec_kv_desc, same rules as fdec_run).
+ *   page_table: int32 device [batch][page_table_stride], as for fdec_run.
+ *   device_errors: optional uint32 device word; a page id outside the pool sets
+ *      FDEC_DEVERR_PAGE_ID, and a position outside [0, page_table_stride *
+ *      page_size) or a sequence outside [0, batch) sets FDEC_DEVERR_SEQ_LEN;
+ *      that token is skipped.
+ * Errors: FDEC_ERR_INVALID_ARG (null pointers, counts), FDEC_ERR_UNSUPPORTED
+ * (head_dim, page_size), FDEC_ERR_LAYOUT (alignment and stride rules).
+ * Tokens must not repeat a (sequence, position) (the order of two writes to
+ * one slot is unspecified).  One kernel launch, no allocation; capturable.
+ */
+fdec_status fdec_append(const void* k_new, const void* v_new, int64_t new_stride_tok, int64_t new_stride_head,
+                        const int32_t* batch_indices, const int32_t* positions, int n_tokens, int num_kv_heads,
+                        int head_dim, int page_size, fdec_kv_desc k, fdec_kv_desc v, const int32_t* page_table,
+                        int batch, int64_t page_table_stride, uint32_t* device_errors, cudaStream_t stream);
+
 /* Release a plan (NULL is a no-op). */
 fdec_status fdec_plan_destroy(fdec_plan_t plan);
 

@@ -9,7 +9,8 @@ The arithmetic lives in ``oracle.c`` (plain C, OpenMP over output rows); this
 module only compiles it with gcc and marshals numpy arrays through ctypes.
 What it computes is stated at the top of ``oracle.c``: softmax(q K^T * scale) V
 and its log-sum-exp over the tokens gathered through the page table, and the
-log-sum-exp merge of normalised attention states.
+log-sum-exp merge of normalised attention states.  ``append_paged`` (the write
+side of the cache, a plain scatter) is written here in Python.
 """
 from __future__ import annotations
 
@@ -177,3 +178,31 @@ def merge_states(o, lse):
     if st != 0:
         raise ValueError(f"oracle_merge_states failed with status {st}")
     return o_out, lse_out
+
+
+def append_paged(k_new, v_new, batch_indices, positions, k_view, v_view, page_table, page_size: int) -> int:
+    """Paged KV append, by definition (FlashInfer PR "Stop declaring the paged KV
+    cache mutated on read-only attention ops", append notes: append writes the
+    cache): new token i of sequence b = batch_indices[i] at position
+    t = positions[i] goes to page = page_table[b][t // page_size], slot
+    t % page_size, for every KV head:  K[page, h, slot, :] = k_new[i, h, :] and
+    V likewise.  A token whose sequence, position or page id is out of range is
+    skipped; the returned flags are those of the library (1 = page id,
+    2 = sequence / position).  Plain Python over the tokens on CPU tensors
+    (k_view / v_view are written in place through their strides)."""
+    table = np.asarray(page_table)
+    flags = 0
+    n_pages_k, n_pages_v = k_view.shape[0], v_view.shape[0]
+    for i in range(k_new.shape[0]):
+        b, t = int(batch_indices[i]), int(positions[i])
+        if b < 0 or b >= table.shape[0] or t < 0 or t // page_size >= table.shape[1]:
+            flags |= 2
+            continue
+        page = int(table[b, t // page_size])
+        if page < 0 or page >= n_pages_k or page >= n_pages_v:
+            flags |= 1
+            continue
+        slot = t % page_size
+        k_view[page, :, slot, :] = k_new[i]
+        v_view[page, :, slot, :] = v_new[i]
+    return flags

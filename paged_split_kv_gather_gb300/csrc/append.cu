@@ -1,0 +1,60 @@
+// append.cu -- paged KV append: scatter new tokens' K and V rows into the pages
+// the page table names (the write side of the cache).
+//
+// One thread per 16-byte chunk of a (token, KV head) row, for K and V; grid-
+// stride loop.  Reads of the new rows are coalesced; each chunk lands at
+// base + page * stride_page + head * stride_head + slot * stride_token.
+// HBM-bound: 2 x n_tokens x Hk x D x 2 bytes read and as many written.
+#include <cstdint>
+
+#include "../../include/fdec.h"
+#include "fdec_internal.h"
+
+namespace fdec {
+
+__global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+    const int chunks_row = p.head_dim / 8;
+    const int64_t per_token = static_cast<int64_t>(p.hk) * chunks_row;
+    const int64_t total = static_cast<int64_t>(p.n_tokens) * per_token;
+    const int page_mask = (1 << p.page_shift) - 1;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < 2 * total;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const bool is_v = idx >= total;
+        const int64_t j = is_v ? idx - total : idx;
+        const int i = static_cast<int>(j / per_token);
+        const int rem = static_cast<int>(j - static_cast<int64_t>(i) * per_token);
+        const int h = rem / chunks_row;
+        const int c = rem - h * chunks_row;
+        const int b = __ldg(p.batch_indices + i);
+        const int t = __ldg(p.positions + i);
+        const int pi = t >> p.page_shift;
+        if (t < 0 || pi >= p.pt_stride || b < 0 || b >= p.batch) {
+            if (c == 0 && h == 0 && !is_v && p.err != nullptr) atomicOr(p.err, FDEC_DEVERR_SEQ_LEN);
+            continue;
+        }
+        const int page = __ldg(p.page_table + static_cast<int64_t>(b) * p.pt_stride + pi);
+        if (page < 0 || page >= p.k_pages || page >= p.v_pages) {  // the token is skipped for K and V alike
+            if (c == 0 && h == 0 && !is_v && p.err != nullptr) atomicOr(p.err, FDEC_DEVERR_PAGE_ID);
+            continue;
+        }
+        const uint16_t* src = (is_v ? p.v_new : p.k_new) + static_cast<int64_t>(i) * p.new_st +
+                              static_cast<int64_t>(h) * p.new_sh + c * 8;
+        uint16_t* dst = (is_v ? p.v_base : p.k_base) +
+                        static_cast<int64_t>(page) * (is_v ? p.v_sp : p.k_sp) +
+                        static_cast<int64_t>(h) * (is_v ? p.v_sh : p.k_sh) +
+                        static_cast<int64_t>(t & page_mask) * (is_v ? p.v_st : p.k_st) + c * 8;
+        *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
+    }
+}
+
+cudaError_t launch_append(const AppendParams& p, int num_sms, cudaStream_t s) {
+    const int64_t total = 2LL * p.n_tokens * p.hk * (p.head_dim / 8);
+    if (total == 0) return cudaSuccess;
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * 8;
+    if (blocks > cap) blocks = cap;
+    append_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace fdec
