@@ -48,13 +48,15 @@ def _bind(path: str):
     lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_bf16_to_double.restype = ctypes.c_double
     lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_e4m3_to_double.restype = ctypes.c_double
+    lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
     lib.oracle_paged_attention.restype = I
     lib.oracle_paged_attention.argtypes = (
         [P, I64, I64, I64]
         + [P, I64, I64, I64, I64, I64]
         + [P, I64, I64, I64, I64, I64]
         + [P, I64, P]
-        + [I, I, I, I, I, I, I, I, ctypes.c_double, P, I64, P, P, I]
+        + [I, I, I, I, I, I, I, I, ctypes.c_double, I, ctypes.c_double, ctypes.c_double, P, I64, P, P, I]
     )
     lib.oracle_merge_states.restype = I
     lib.oracle_merge_states.argtypes = [P, P, I, I64, I, P, P]
@@ -105,16 +107,23 @@ def bf16_to_double(bits: int) -> float:
     return _load().oracle_bf16_to_double(int(bits) & 0xFFFF)
 
 
+def e4m3_to_double(bits: int) -> float:
+    return _load().oracle_e4m3_to_double(int(bits) & 0xFF)
+
+
 class Pool:
-    """A K or V pool as flat 16-bit storage plus element offset, page count and strides.
+    """A K or V pool as flat storage plus element offset, page count and strides.
 
     Element (page, head, slot, dim) is at ``offset + page*stride_page +
-    head*stride_head + slot*stride_token + dim``.
+    head*stride_head + slot*stride_token + dim``.  The storage is 16-bit (the
+    query's type) or, for a quantised cache, uint8 holding E4M3 codes.
     """
 
     def __init__(self, storage, offset: int, num_pages: int, stride_page: int,
                  stride_head: int, stride_token: int):
-        self.storage = _u16(storage)
+        a = np.asarray(storage)
+        self.fp8 = a.dtype == np.uint8
+        self.storage = np.ascontiguousarray(a).reshape(-1) if self.fp8 else _u16(storage)
         self.offset = int(offset)
         self.num_pages = int(num_pages)
         self.stride_page = int(stride_page)
@@ -125,13 +134,19 @@ class Pool:
 def paged_attention(q_storage, q_offset: int, q_stride_tok: int, q_stride_head: int,
                     k: Pool, v: Pool, page_table, seq_lens, *, q_len: int, num_qo_heads: int,
                     num_kv_heads: int, head_dim: int, page_size: int, is_bf16: bool,
-                    causal: bool, scale: float, rows=None, n_threads: int = 0):
+                    causal: bool, scale: float, rows=None, n_threads: int = 0, k_scale: float = 1.0,
+                    v_scale: float = 1.0):
     """Return (out, lse) in float64.
+
+    K and V are k_scale and v_scale times their stored values (decoded from
+    16-bit, or from E4M3 when the pools hold uint8 codes).
 
     Without ``rows``: out has shape [batch, q_len, Hq, D] and lse [batch, q_len, Hq].
     With ``rows`` (flat indices (b*q_len + i)*Hq + h): out is [len(rows), D], lse [len(rows)].
     """
     lib = _load()
+    if k.fp8 != v.fp8:
+        raise ValueError("K and V pools must have the same storage type")
     qs = _u16(q_storage)
     table = np.ascontiguousarray(page_table, dtype=np.int32)
     if table.ndim != 2:
@@ -152,7 +167,7 @@ def paged_attention(q_storage, q_offset: int, q_stride_tok: int, q_stride_head: 
         v.storage.ctypes.data, v.offset, v.num_pages, v.stride_page, v.stride_head, v.stride_token,
         table.ctypes.data, table.shape[1], lens.ctypes.data,
         batch, q_len, num_qo_heads, num_kv_heads, head_dim, page_size, int(bool(is_bf16)),
-        int(bool(causal)), float(scale),
+        int(bool(causal)), float(scale), int(k.fp8), float(k_scale), float(v_scale),
         None if rows_arr is None else rows_arr.ctypes.data, n_rows,
         out.ctypes.data, lse.ctypes.data, int(n_threads))
     if st != 0:

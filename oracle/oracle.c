@@ -36,6 +36,13 @@
  *
  * 16-bit storage is decoded to double exactly, from the IEEE 754 binary16
  * definition and from the bfloat16 definition (the top half of a binary32).
+ *
+ * Quantised caches: K and V may instead be stored as 8-bit E4M3 floating point
+ * (the fp8 caches of the FlashInfer PR's AITER paged-attention notes, which
+ * carry a k_scale and a v_scale).  Then the key and value of a token are
+ *   K_t = k_scale * e4m3(K_stored),   V_t = v_scale * e4m3(V_stored)
+ * and everything above applies unchanged to these K_t, V_t.  For 16-bit caches
+ * the same scales apply (1 gives the plain definition).
  */
 #include <math.h>
 #include <stdint.h>
@@ -77,7 +84,31 @@ double oracle_bf16_to_double(uint16_t bits) {
     return sign ? -mag : mag;
 }
 
+/* OCP 8-bit floating point E4M3 ("e4m3fn"): 1 sign bit, 4 exponent bits
+ * (bias 7), 3 fraction bits; exponent 0 is subnormal; there is no infinity and
+ * only S.1111.111 is NaN, so the largest magnitude is 1.75 * 2^8 = 448. */
+double oracle_e4m3_to_double(uint8_t bits) {
+    int sign = (bits >> 7) & 1;
+    int expo = (bits >> 3) & 0xf;
+    int frac = bits & 0x7;
+    double mag;
+    if (expo == 0xf && frac == 0x7) {
+        mag = NAN;
+    } else if (expo == 0) {
+        mag = ldexp((double)frac, -9);              /* frac/8 * 2^-6 */
+    } else {
+        mag = ldexp((double)(8 + frac), expo - 10); /* (1 + frac/8) * 2^(expo-7) */
+    }
+    return sign ? -mag : mag;
+}
+
 typedef double (*decode_fn)(uint16_t);
+
+/* Element idx of a K or V pool: 16-bit (decoded by dec) or E4M3. */
+static double kv_elem(const void* pool, int64_t idx, int kv_fp8, decode_fn dec) {
+    if (kv_fp8) return oracle_e4m3_to_double(((const uint8_t*)pool)[idx]);
+    return dec(((const uint16_t*)pool)[idx]);
+}
 
 /* Return codes. */
 #define ORACLE_OK 0
@@ -86,11 +117,11 @@ typedef double (*decode_fn)(uint16_t);
 
 int oracle_paged_attention(
     const uint16_t* q, int64_t q_off, int64_t q_stride_tok, int64_t q_stride_head,
-    const uint16_t* k, int64_t k_off, int64_t k_pages, int64_t k_sp, int64_t k_sh, int64_t k_st,
-    const uint16_t* v, int64_t v_off, int64_t v_pages, int64_t v_sp, int64_t v_sh, int64_t v_st,
+    const void* k, int64_t k_off, int64_t k_pages, int64_t k_sp, int64_t k_sh, int64_t k_st,
+    const void* v, int64_t v_off, int64_t v_pages, int64_t v_sp, int64_t v_sh, int64_t v_st,
     const int32_t* table, int64_t table_stride, const int32_t* seq_lens,
     int batch, int q_len, int hq, int hk, int d, int page_size, int is_bf16, int causal,
-    double scale, const int64_t* rows, int64_t n_rows, double* out, double* lse, int n_threads)
+    double scale, int kv_fp8, double k_scale, double v_scale, const int64_t* rows, int64_t n_rows, double* out, double* lse, int n_threads)
 {
     if (batch < 0 || q_len < 1 || hq < 1 || hk < 1 || hq % hk != 0 || d < 1 || page_size < 1)
         return ORACLE_BAD_ARG;
@@ -150,9 +181,9 @@ int oracle_paged_attention(
                     z[t] = -INFINITY;
                     continue;
                 }
-                const uint16_t* kp = k + k_off + page * k_sp + (int64_t)kvh * k_sh + slot * k_st;
+                const int64_t kp = k_off + page * k_sp + (int64_t)kvh * k_sh + slot * k_st;
                 double s = 0.0;
-                for (int e = 0; e < d; ++e) s += qd[e] * dec(kp[e]);
+                for (int e = 0; e < d; ++e) s += qd[e] * (k_scale * kv_elem(k, kp + e, kv_fp8, dec));
                 z[t] = scale * s;
                 if (z[t] > zmax) zmax = z[t];
             }
@@ -164,10 +195,10 @@ int oracle_paged_attention(
                 const int64_t page = table[(int64_t)b * table_stride + t / page_size];
                 if (page < 0 || page >= k_pages || page >= v_pages) continue;
                 const int64_t slot = t % page_size;
-                const uint16_t* vp = v + v_off + page * v_sp + (int64_t)kvh * v_sh + slot * v_st;
+                const int64_t vp = v_off + page * v_sp + (int64_t)kvh * v_sh + slot * v_st;
                 const double w = exp(z[t] - zmax);
                 denom += w;
-                for (int e = 0; e < d; ++e) acc[e] += w * dec(vp[e]);
+                for (int e = 0; e < d; ++e) acc[e] += w * (v_scale * kv_elem(v, vp + e, kv_fp8, dec));
             }
             if (n_vis == 0 || denom == 0.0) {
                 for (int e = 0; e < d; ++e) o_row[e] = 0.0;

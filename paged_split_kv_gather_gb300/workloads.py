@@ -17,7 +17,9 @@ Recipe (all draws seeded):
     that token's logit by about +8 for every head of the group; the sum is
     rounded to the storage dtype, and both sides read the stored values;
   * "peaked": q multiplied by 8 (exact in 16-bit), so the softmax is sharp and
-    a misread key or value moves the output well past the tolerance.
+    a misread key or value moves the output well past the tolerance;
+  * quantised caches (kv_dtype "fp8"): K and V drawn the same way and rounded
+    to 8-bit E4M3 (torch.float8_e4m3fn), q stays 16-bit.
 
 The five named workloads follow the shapes of the pages' workloads: a tiny
 decode, a batched GQA decode at exactly 32 blocks of 64 tokens, the 32q/4kv/128
@@ -38,8 +40,8 @@ LONG_CONTEXT_LENGTHS = (1900, 2000, 2100, 3000, 4800, 32768, 131072, 262144)
 RAGGED_HEAD_DIMS = (192, 256, 512)
 MULTI_TOKEN_Q_LENS = (4, 8, 2048)
 
-_TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16}
-_NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0}
+_TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16, "fp8": torch.float8_e4m3fn}
+_NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0, "fp8": 0x7F}
 
 
 @dataclass
@@ -63,6 +65,11 @@ class Workload:
     v: torch.Tensor               # [pages, Hk, P, D] view
     layout: str = "hnd"
     keep: List[torch.Tensor] = field(default_factory=list)
+    kv_dtype: str = ""            # "" = the q dtype; "fp8" = E4M3 K/V codes
+
+    @property
+    def kv_fp8(self) -> bool:
+        return self.kv_dtype == "fp8"
 
     @property
     def group(self) -> int:
@@ -70,8 +77,9 @@ class Workload:
 
     @property
     def kv_bytes(self) -> int:
-        """Algorithmic K+V bytes one call reads: sum_b L_b * Hk * D * 2 (K and V) * 2 bytes."""
-        return int(np.sum(self.seq_lens.astype(np.int64))) * self.num_kv_heads * self.head_dim * 4
+        """Algorithmic K+V bytes one call reads: sum_b L_b * Hk * D * 2 (K and V) * element bytes."""
+        eb = 1 if self.kv_fp8 else 2
+        return int(np.sum(self.seq_lens.astype(np.int64))) * self.num_kv_heads * self.head_dim * 2 * eb
 
     def to(self, device) -> "Workload":
         """Copy every tensor to ``device`` keeping views and strides (storage is copied whole)."""
@@ -88,7 +96,7 @@ class Workload:
         return Workload(self.name, self.dtype, self.batch, self.q_len, self.num_qo_heads,
                         self.num_kv_heads, self.head_dim, self.page_size, self.causal, self.scale,
                         self.seq_lens.copy(), self.page_table.copy(), move(self.q), move(self.k),
-                        move(self.v), self.layout, list(memo.values()))
+                        move(self.v), self.layout, list(memo.values()), self.kv_dtype)
 
 
 def _flat_storage(t: torch.Tensor) -> torch.Tensor:
@@ -171,13 +179,15 @@ def make(batch: int, q_len: int, num_qo_heads: int, num_kv_heads: int, head_dim:
          page_size: int, seq_lens, *, dtype: str = "bf16", layout: str = "hnd",
          causal: bool = False, seed: int = 0, device="cpu", pool_pages: Optional[int] = None,
          q_layout: str = "packed", peaked: bool = False, spikes: float = 0.0,
-         nan_guard: bool = False, name: str = "custom", scale: Optional[float] = None) -> Workload:
+         nan_guard: bool = False, name: str = "custom", scale: Optional[float] = None,
+         kv_dtype: str = "") -> Workload:
     """General seeded workload.
 
     q_layout: "packed" [B,Q,Hq,D]; "fused_qkv" (head slice of a [B*Q, Hq+2Hk, D] tensor);
     "head_major" (a [Hq, B*Q, D] tensor viewed as [B,Q,Hq,D]).
     nan_guard: fill every K/V element that must never be read (slots past L in a
     sequence's last page, and pages no sequence references) with NaN.
+    kv_dtype: "" (K/V in the q dtype) or "fp8" (E4M3 K/V codes).
     """
     rng = np.random.Generator(np.random.PCG64(seed))
     lens = np.asarray(seq_lens, dtype=np.int64).reshape(-1)
@@ -208,15 +218,16 @@ def make(batch: int, q_len: int, num_qo_heads: int, num_kv_heads: int, head_dim:
     if peaked:
         q.mul_(8)
 
-    k, v, keep = _alloc_pool(pool, hk, page_size, d, layout, gen, device, dtype)
+    kvd = kv_dtype or dtype
+    k, v, keep = _alloc_pool(pool, hk, page_size, d, layout, gen, device, kvd)
 
     if spikes > 0:
         _add_spikes(rng, k, q, table, lens, page_size, sc, spikes, hq // hk)
     if nan_guard:
-        _nan_fill_unread(k, v, table, lens, page_size, dtype)
+        _nan_fill_unread(k, v, table, lens, page_size, kvd)
 
     return Workload(name, dtype, batch, q_len, hq, hk, d, page_size, causal, sc,
-                    lens.astype(np.int32), table, q, k, v, layout, q_keep + keep)
+                    lens.astype(np.int32), table, q, k, v, layout, q_keep + keep, kv_dtype)
 
 
 def _add_spikes(rng, k, q, table, lens, page_size, scale, frac, g):
@@ -238,13 +249,14 @@ def _add_spikes(rng, k, q, table, lens, page_size, scale, frac, g):
 
 
 def _nan_fill_unread(k, v, table, lens, page_size, dtype):
-    nan = torch.tensor(_NAN_BITS[dtype], dtype=torch.int32).to(torch.int16).item()
+    raw_dtype = torch.uint8 if dtype == "fp8" else torch.int16
+    nan = torch.tensor(_NAN_BITS[dtype], dtype=torch.int32).to(raw_dtype).item()
     used = np.zeros(k.shape[0], dtype=bool)
     for b in range(table.shape[0]):
         n = max(1, -(-int(lens[b]) // page_size))
         used[table[b, :n]] = True
     for pool in (k, v):
-        raw = pool.view(torch.int16)
+        raw = pool.view(raw_dtype)
         unused = torch.as_tensor(np.nonzero(~used)[0], device=pool.device)
         if unused.numel():
             raw[unused] = nan

@@ -9,8 +9,11 @@ from paged_split_kv_gather_gb300.workloads import Workload, q_token_stride, stor
 
 
 def np_storage(t: torch.Tensor):
-    """(uint16 numpy array over t's whole CPU storage, element offset)."""
+    """(numpy array over t's whole CPU storage, element offset): uint16 for 16-bit
+    tensors, uint8 (E4M3 codes) for float8_e4m3fn."""
     flat, off, _ = storage_view(t)
+    if t.dtype == torch.float8_e4m3fn:
+        return flat.view(torch.uint8).numpy(), off
     return flat.view(torch.int16).numpy().view(np.uint16), off
 
 
@@ -19,7 +22,7 @@ def oracle_pool(t: torch.Tensor) -> oracle.Pool:
     return oracle.Pool(arr, off, t.shape[0], t.stride(0), t.stride(1), t.stride(2))
 
 
-def oracle_run(w: Workload, rows=None, n_threads: int = 0, seq_lens=None):
+def oracle_run(w: Workload, rows=None, n_threads: int = 0, seq_lens=None, k_scale=1.0, v_scale=1.0):
     """Oracle (out, lse) for a CPU workload."""
     assert w.q.device.type == "cpu"
     q_arr, q_off = np_storage(w.q)
@@ -29,7 +32,7 @@ def oracle_run(w: Workload, rows=None, n_threads: int = 0, seq_lens=None):
         w.page_table, lens, q_len=w.q_len, num_qo_heads=w.num_qo_heads,
         num_kv_heads=w.num_kv_heads, head_dim=w.head_dim, page_size=w.page_size,
         is_bf16=(w.dtype == "bf16"), causal=w.causal, scale=w.scale, rows=rows,
-        n_threads=n_threads)
+        n_threads=n_threads, k_scale=k_scale, v_scale=v_scale)
 
 
 def gather_tokens(w: Workload, pool: torch.Tensor, b: int, kvh: int, n: int) -> np.ndarray:

@@ -4,7 +4,7 @@ Each case plants one mistake in a copy of oracle/oracle.c (on the CPU),
 builds it, routes the oracle through it and runs the pin suite: at least one
 pin has to fail.  This shows the pins constrain every step of the definition
 (gather address, GQA head map, scale, causal alignment, normalisation, the
-log-sum-exp, the state merge and the 16-bit decoders).
+log-sum-exp, the state merge, the 16-bit and E4M3 decoders and the K/V scales).
 """
 import os
 import subprocess
@@ -12,6 +12,7 @@ import subprocess
 import pytest
 
 import oracle
+from tests import test_oracle_fp8 as pins_fp8
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -29,6 +30,10 @@ MUTATIONS = {
     "merge_weight_wrong_reference": ("exp(lse[(int64_t)s * rows + r] - total)", "exp(lse[(int64_t)s * rows + r] - m)"),
     "bf16_bias_off_by_one": ("expo - 134", "expo - 133"),
     "f16_subnormal_scale": ("ldexp((double)frac, -24)", "ldexp((double)frac, -25)"),
+    "e4m3_bias_off_by_one": ("ldexp((double)(8 + frac), expo - 10)", "ldexp((double)(8 + frac), expo - 9)"),
+    "e4m3_subnormal_scale": ("ldexp((double)frac, -9)", "ldexp((double)frac, -10)"),
+    "k_scale_dropped": ("(k_scale * kv_elem(k, kp + e", "(kv_elem(k, kp + e"),
+    "v_scale_dropped": ("(v_scale * kv_elem(v, vp + e", "(kv_elem(v, vp + e"),
     "last_token_dropped": ("n_vis = L;                              /* tokens", "n_vis = L - 1;                              /* tokens"),
 }
 
@@ -36,18 +41,21 @@ MUTATIONS = {
 def _pin_checks():
     """(name, callable) for every pin, with parametrised pins expanded."""
     checks = []
-    for name in dir(pins):
-        if not name.startswith("test_"):
-            continue
-        fn = getattr(pins, name)
-        marks = getattr(fn, "pytestmark", [])
-        params = [m for m in marks if m.name == "parametrize"]
-        if not params:
-            checks.append((name, fn))
-            continue
-        argname, values = params[0].args[0], params[0].args[1]
-        for k, v in enumerate(values):
-            checks.append((f"{name}[{k}]", lambda fn=fn, a=argname, v=v: fn(**{a: v})))
+    for mod in (pins, pins_fp8):
+        for name in dir(mod):
+            if not name.startswith("test_"):
+                continue
+            fn = getattr(mod, name)
+            marks = getattr(fn, "pytestmark", [])
+            params = [m for m in marks if m.name == "parametrize"]
+            if not params:
+                checks.append((name, fn))
+                continue
+            argnames = [a.strip() for a in params[0].args[0].split(",")]
+            for k, v in enumerate(params[0].args[1]):
+                vals = v if len(argnames) > 1 else (v,)
+                kwargs = dict(zip(argnames, vals))
+                checks.append((f"{name}[{k}]", lambda fn=fn, kw=kwargs: fn(**kw)))
     return checks
 
 
