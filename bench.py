@@ -207,6 +207,36 @@ def _time_flush_graph(torch, reps, flush):
     return best / reps
 
 
+def _e4m3_point(dev, calls, hbm_peak, flush):
+    """Quantised cache: the long-context shape (262144 tokens, 32/4 heads, D 128, page 64)
+    over E4M3 codes with a k_scale and a v_scale; kv_bytes counts the 1-byte codes."""
+    import torch
+
+    import paged_split_kv_gather_gb300 as fd
+    from paged_split_kv_gather_gb300 import workloads as W
+
+    w = W.long_context(262144, device=dev, kv_dtype="fp8")
+    pd = fd.PagedDecode(w.seq_lens, 1, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
+                        device=dev, kv_dtype="fp8")
+    table = torch.as_tensor(w.page_table, device=dev)
+    lens = torch.as_tensor(w.seq_lens, device=dev)
+    out = torch.empty((1, 1, w.num_qo_heads, w.head_dim), device=dev)
+    lse = torch.empty((1, 1, w.num_qo_heads), device=dev)
+
+    def run():
+        pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale, k_scale=0.5, v_scale=2.0)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    med, mn = _time_calls(torch, run, calls, flush)
+    gbs = w.kv_bytes / (med * 1e-6) / 1e9
+    return {"us_per_call": round(med, 2), "us_min": round(mn, 2), "kv_bytes": int(w.kv_bytes),
+            "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / hbm_peak, 4), "path": int(pd.info["path"]),
+            "launches": int(pd.info["launches"]), "max_splits": int(pd.info["max_splits"]),
+            "scales": {"k_scale": 0.5, "v_scale": 2.0}}
+
+
 def _config_points(dev, calls, hbm_peak):
     """The other workloads' µs/call and GB/s (tiny decode, batched GQA decode, the
     ragged serving batch at head_dim 192/256/512), a no-cliff sweep of the long-context
@@ -219,8 +249,10 @@ def _config_points(dev, calls, hbm_peak):
 
     flush = L2Flush(torch, dev)
 
-    def runner(w, capacities=None, **plan_opts):
+    def runner(w, capacities=None, run_kw=None, **plan_opts):
         caps = w.seq_lens if capacities is None else capacities
+        if w.kv_dtype:
+            plan_opts.setdefault("kv_dtype", w.kv_dtype)
         pd = fd.PagedDecode(caps, w.q_len, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
                             w.causal, device=dev, **plan_opts)
         table = torch.as_tensor(w.page_table, device=dev)
@@ -229,7 +261,7 @@ def _config_points(dev, calls, hbm_peak):
         lse = torch.empty((w.batch, w.q_len, w.num_qo_heads), device=dev)
 
         def run():
-            pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale)
+            pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale, **(run_kw or {}))
 
         for _ in range(3):
             run()
@@ -276,6 +308,9 @@ def _config_points(dev, calls, hbm_peak):
                                           "GB_per_s": round(nbytes / (med * 1e-6) / 1e9, 1)}
     points["paged_append"] = app
     del wa, table
+    torch.cuda.empty_cache()
+
+    points["long_context_e4m3_L262144"] = _e4m3_point(dev, calls, hbm_peak, flush)
     torch.cuda.empty_cache()
 
     # Graph-replayed long-context points where launch latency matters.
@@ -455,6 +490,16 @@ def _run_fdec(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
+    if args.only_e4m3:
+        # The quantised-cache long-context point alone (profiling the E4M3 kernel); not a bench line.
+        peak, _ = _peaks()
+        pt = _e4m3_point(dev, args.sweep_calls, peak, L2Flush(torch, dev))
+        if rank == 0:
+            print(json.dumps({"long_context_e4m3_L262144": pt}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
     if args.only_dense:
         # The multi-token points alone (for profiling the tcgen05 kernel); not a bench line.
         peak, _ = _peaks()
@@ -796,6 +841,8 @@ def main():
     ap.add_argument("--only-dense", action="store_true",
                     help="run only the multi-token points and print them (profiling; no bench line)")
     ap.add_argument("--dense-q", type=int, nargs="+", default=[4, 8, 2048], help="q_len of the multi-token points")
+    ap.add_argument("--only-e4m3", action="store_true",
+                    help="run only the E4M3 (fp8) long-context point and print it (profiling; no bench line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=120.0)

@@ -27,8 +27,8 @@
  *     first commit: a lazily allocated untracked tensor broke CUDA-graph pools.)
  *   - K, V and q are only read, never written (same PR, second commit: the
  *     read-only ops must not declare or perform writes to the cache).
- *   - Element strides are in elements of the 16-bit storage type; the
- *     innermost (head_dim) stride is always 1.
+ *   - Element strides are in elements of the storage type (16-bit, or one
+ *     byte for E4M3 caches); the innermost (head_dim) stride is always 1.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).
  */
 #ifndef FDEC_H
@@ -71,8 +71,9 @@ typedef enum { FDEC_F16 = 0, FDEC_BF16 = 1 } fdec_dtype;
  * the K/V forms of the FlashInfer PR's "Architecture / design notes" table.
  * K and V may differ in strides and page count; only indexed pages are read
  * (same PR, first commit: a shorter V pool).  base must be 16-byte aligned and
- * every stride a multiple of 8 elements (16 bytes), so that each token row
- * starts on a 16-byte boundary; otherwise fdec_run returns FDEC_ERR_LAYOUT.
+ * every stride a multiple of 16 bytes (8 elements of a 16-bit cache, 16 of an
+ * E4M3 cache), so that each token row starts on a 16-byte boundary; otherwise
+ * fdec_run returns FDEC_ERR_LAYOUT.
  */
 typedef struct {
     const void* base;
@@ -96,6 +97,17 @@ typedef struct fdec_plan_s* fdec_plan_t;
  */
 enum { FDEC_PATH_AUTO = 0, FDEC_PATH_SIMT = 1, FDEC_PATH_MMA = 2, FDEC_PATH_TC = 3 };
 
+/*
+ * K/V storage types.  SAME: K and V are 16-bit, of the query's dtype.  E4M3:
+ * quantised caches of 8-bit OCP E4M3 codes (the fp8 caches of the FlashInfer
+ * PR's AITER paged-attention notes, with a k_scale and a v_scale): the key and
+ * value of a token are k_scale x the decoded K code and v_scale x the decoded V
+ * code (scales given to fdec_run_scaled).  E4M3 caches run on the MMA path with
+ * head_dim 128 or 256; the codes are staged as they are stored and widened to
+ * 16 bits in shared memory, so no dequantised copy of the cache exists anywhere.
+ */
+enum { FDEC_KV_SAME = 0, FDEC_KV_E4M3 = 1 };
+
 /* Plan options; pass NULL for the defaults (all fields 0). */
 typedef struct {
     int blocks_per_split;  /* 64-token blocks per split; 0 = auto; 1 = one partial per block */
@@ -104,6 +116,7 @@ typedef struct {
                               where built, else SIMT), _SIMT, _MMA (every head_dim),
                               _TC (head_dim 128) */
     int num_sms;           /* 0 = query the current device; > 0 plans without a device */
+    int kv_dtype;          /* FDEC_KV_SAME (0) or FDEC_KV_E4M3 (head_dim 128 / 256; path AUTO or MMA) */
 } fdec_plan_opts;
 
 /* What a plan decided (for logging, tests and benchmarks). */
@@ -174,6 +187,22 @@ fdec_status fdec_run(fdec_plan_t plan, const void* q, int64_t q_stride_tok, int6
                      fdec_kv_desc k, fdec_kv_desc v, const int32_t* page_table,
                      int64_t page_table_stride, const int32_t* seq_lens_dev, float scale,
                      float* out, float* lse, void* workspace, cudaStream_t stream);
+
+/*
+ * fdec_run for scaled caches: K_t = k_scale x stored K_t and V_t = v_scale x
+ * stored V_t (E4M3 caches, see FDEC_KV_E4M3; any cache may carry scales).  So
+ * z_t = scale x k_scale x q . K_stored_t and out = v_scale x (the attention of
+ * the stored values); lse does not depend on v_scale.  The scales are host
+ * values: nothing is read from or allocated on the device for them, so a
+ * captured graph holds them as launch arguments (the FlashInfer PR's first
+ * commit: a lazily allocated unit-scale tensor broke graph pools).  Both must
+ * be finite (FDEC_ERR_INVALID_ARG).  fdec_run is this call with 1 and 1.
+ */
+fdec_status fdec_run_scaled(fdec_plan_t plan, const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                            fdec_kv_desc k, fdec_kv_desc v, const int32_t* page_table,
+                            int64_t page_table_stride, const int32_t* seq_lens_dev, float scale,
+                            float k_scale, float v_scale, float* out, float* lse, void* workspace,
+                            cudaStream_t stream);
 
 /*
  * Merge n_states normalised attention states (as fdec_run writes them) over

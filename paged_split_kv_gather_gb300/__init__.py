@@ -22,6 +22,7 @@ __all__ = [
     "fdec_plan_set_split_event", "fdec_read_device_errors", "fdec_last_error", "fdec_version",
     "fdec_run_static_workspace", "fdec_append", "kv_desc", "library_path", "PagedDecode", "EXPORTED_SYMBOLS",
     "FDEC_F16", "FDEC_BF16", "FDEC_PATH_AUTO", "FDEC_PATH_SIMT", "FDEC_PATH_MMA", "FDEC_PATH_TC",
+    "FDEC_KV_SAME", "FDEC_KV_E4M3", "fdec_run_scaled",
     "DEVERR_PAGE_ID", "DEVERR_SEQ_LEN", "DEVERR_TIMEOUT",
 ]
 
@@ -30,6 +31,7 @@ _LIB_PATH = os.path.join(_HERE, "libfdec.so")
 
 FDEC_F16, FDEC_BF16 = 0, 1
 FDEC_PATH_AUTO, FDEC_PATH_SIMT, FDEC_PATH_MMA, FDEC_PATH_TC = 0, 1, 2, 3
+FDEC_KV_SAME, FDEC_KV_E4M3 = 0, 1
 DEVERR_PAGE_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 
 STATUS_NAMES = {
@@ -43,6 +45,7 @@ EXPORTED_SYMBOLS = (
     "fdec_plan", "fdec_plan_upload", "fdec_run", "fdec_merge_states", "fdec_plan_destroy",
     "fdec_plan_get_info", "fdec_plan_get_splits", "fdec_plan_set_split_event",
     "fdec_read_device_errors", "fdec_last_error", "fdec_version", "fdec_run_static_workspace", "fdec_append",
+    "fdec_run_scaled",
 )
 
 
@@ -61,7 +64,7 @@ class KVDesc(ctypes.Structure):
 
 class PlanOpts(ctypes.Structure):
     _fields_ = [("blocks_per_split", ctypes.c_int), ("reducer_fanin", ctypes.c_int),
-                ("path", ctypes.c_int), ("num_sms", ctypes.c_int)]
+                ("path", ctypes.c_int), ("num_sms", ctypes.c_int), ("kv_dtype", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -104,6 +107,9 @@ def _load():
         lib.fdec_plan_upload.argtypes = [P, P, P]
         lib.fdec_run.restype = I
         lib.fdec_run.argtypes = [P, P, I64, I64, KVDesc, KVDesc, P, I64, P, ctypes.c_float, P, P, P, P]
+        lib.fdec_run_scaled.restype = I
+        lib.fdec_run_scaled.argtypes = [P, P, I64, I64, KVDesc, KVDesc, P, I64, P, ctypes.c_float, ctypes.c_float,
+                                        ctypes.c_float, P, P, P, P]
         lib.fdec_run_static_workspace.restype = I
         lib.fdec_run_static_workspace.argtypes = [P, P, I64, I64, KVDesc, KVDesc, P, I64, P, ctypes.c_float, P,
                                                   P, P]
@@ -170,10 +176,12 @@ class Plan:
 
 def fdec_plan(seq_lens: Sequence[int], q_len: int, page_size: int, num_qo_heads: int, num_kv_heads: int,
               head_dim: int, dtype: str = "bf16", causal: bool = False, blocks_per_split: int = 0,
-              reducer_fanin: int = 0, path: int = FDEC_PATH_AUTO, num_sms: int = 0) -> Plan:
+              reducer_fanin: int = 0, path: int = FDEC_PATH_AUTO, num_sms: int = 0, kv_dtype: str = "") -> Plan:
+    """kv_dtype: "" (K/V in the q dtype) or "fp8" (E4M3 codes; scales go to fdec_run)."""
     lib = _load()
     lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32).reshape(-1))
-    opts = PlanOpts(blocks_per_split, reducer_fanin, path, num_sms)
+    kvd = {"": FDEC_KV_SAME, "fp8": FDEC_KV_E4M3}[kv_dtype]
+    opts = PlanOpts(blocks_per_split, reducer_fanin, path, num_sms, kvd)
     handle = ctypes.c_void_p()
     ws = ctypes.c_size_t()
     dt = {"f16": FDEC_F16, "bf16": FDEC_BF16}[dtype]
@@ -181,7 +189,7 @@ def fdec_plan(seq_lens: Sequence[int], q_len: int, page_size: int, num_qo_heads:
                          head_dim, dt, int(bool(causal)), ctypes.byref(opts), ctypes.byref(handle),
                          ctypes.byref(ws)))
     meta = dict(q_len=q_len, page_size=page_size, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
-                head_dim=head_dim, dtype=dtype, causal=causal, capacity=lens.copy())
+                head_dim=head_dim, dtype=dtype, causal=causal, capacity=lens.copy(), kv_dtype=kv_dtype)
     return Plan(handle.value, ws.value, lens.shape[0], meta)
 
 
@@ -257,10 +265,37 @@ def fdec_run(plan: Plan, q, k, v, page_table, seq_lens, out, lse, workspace, sca
     if page_table.stride(1) != 1:
         raise ValueError("page_table rows must be contiguous")
     sc = 1.0 / math.sqrt(plan.meta["head_dim"]) if scale is None else float(scale)
+    _check_kv_type(plan, k, v)
     _check(_load().fdec_run(plan.handle, q.data_ptr(), tok, head, kd, vd, page_table.data_ptr(),
                             page_table.stride(0), seq_lens.data_ptr(), sc, out.data_ptr(),
                             None if lse is None else lse.data_ptr(), workspace.data_ptr(),
                             _stream_handle(stream)))
+
+
+def _check_kv_type(plan: Plan, k, v) -> None:
+    """K/V tensors must hold the element type the plan was made for (1-byte E4M3 codes or 16-bit)."""
+    want = 1 if plan.meta.get("kv_dtype") == "fp8" else 2
+    for t in (k, v):
+        if not isinstance(t, KVDesc) and t.element_size() != want:
+            raise ValueError(f"this plan reads {want}-byte K/V elements, got {t.dtype}")
+
+
+def fdec_run_scaled(plan: Plan, q, k, v, page_table, seq_lens, out, lse, workspace, scale: Optional[float] = None,
+                    k_scale: float = 1.0, v_scale: float = 1.0, stream=None) -> None:
+    """fdec_run over a scaled cache: K = k_scale x stored K, V = v_scale x stored V (host floats)."""
+    kd = k if isinstance(k, KVDesc) else kv_desc(k)
+    vd = v if isinstance(v, KVDesc) else kv_desc(v)
+    if not out.is_contiguous() or (lse is not None and not lse.is_contiguous()):
+        raise ValueError("out and lse must be contiguous")
+    tok, head = _q_strides(q)
+    if page_table.stride(1) != 1:
+        raise ValueError("page_table rows must be contiguous")
+    sc = 1.0 / math.sqrt(plan.meta["head_dim"]) if scale is None else float(scale)
+    _check_kv_type(plan, k, v)
+    _check(_load().fdec_run_scaled(plan.handle, q.data_ptr(), tok, head, kd, vd, page_table.data_ptr(),
+                                   page_table.stride(0), seq_lens.data_ptr(), sc, float(k_scale), float(v_scale),
+                                   out.data_ptr(), None if lse is None else lse.data_ptr(), workspace.data_ptr(),
+                                   _stream_handle(stream)))
 
 
 def fdec_run_static_workspace(plan: Plan, q, k, v, page_table, seq_lens, out, lse, scale: Optional[float] = None,
@@ -274,6 +309,7 @@ def fdec_run_static_workspace(plan: Plan, q, k, v, page_table, seq_lens, out, ls
     if page_table.stride(1) != 1:
         raise ValueError("page_table rows must be contiguous")
     sc = 1.0 / math.sqrt(plan.meta["head_dim"]) if scale is None else float(scale)
+    _check_kv_type(plan, k, v)
     _check(_load().fdec_run_static_workspace(plan.handle, q.data_ptr(), tok, head, kd, vd, page_table.data_ptr(),
                                              page_table.stride(0), seq_lens.data_ptr(), sc, out.data_ptr(),
                                              None if lse is None else lse.data_ptr(), _stream_handle(stream)))
@@ -319,8 +355,13 @@ class PagedDecode:
                                      device=device or "cuda")
         fdec_plan_upload(self.plan, self.workspace, stream)
 
-    def run(self, q, k, v, page_table, seq_lens, out, lse=None, scale=None, stream=None):
-        fdec_run(self.plan, q, k, v, page_table, seq_lens, out, lse, self.workspace, scale, stream)
+    def run(self, q, k, v, page_table, seq_lens, out, lse=None, scale=None, stream=None, k_scale=None,
+            v_scale=None):
+        if k_scale is None and v_scale is None:
+            fdec_run(self.plan, q, k, v, page_table, seq_lens, out, lse, self.workspace, scale, stream)
+        else:
+            fdec_run_scaled(self.plan, q, k, v, page_table, seq_lens, out, lse, self.workspace, scale,
+                            1.0 if k_scale is None else k_scale, 1.0 if v_scale is None else v_scale, stream)
 
     def device_errors(self, clear=True, stream=None) -> int:
         return fdec_read_device_errors(self.plan, self.workspace, clear, stream)

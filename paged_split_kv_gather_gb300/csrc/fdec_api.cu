@@ -117,6 +117,7 @@ struct fdec_plan_s {
     int batch = 0, q_len = 1, page_size = 1, page_shift = 0;
     int hq = 0, hk = 0, head_dim = 0, group = 1, rows = 1;
     fdec_dtype dtype = FDEC_BF16;
+    bool kv8 = false;  // K/V stored as E4M3 codes
     int causal = 0;
     int path = FDEC_PATH_SIMT;
     int rc = 1, row_groups = 1;
@@ -220,7 +221,8 @@ cudaError_t dispatch_split(const fdec_plan_s* p, const SplitParams& sp, dim3 gri
     const CUtensorMap& tk = p->tmap_k;
     const CUtensorMap& tv = p->tmap_v;
     if (p->path == FDEC_PATH_TC) return launch_split_tc(sp, tk, tv, p->rc / kTcRows, bf16, grid, stream, launch);
-    if (p->path == FDEC_PATH_MMA) return launch_split_mma(sp, tk, tv, p->head_dim, bf16, grid, stream, launch);
+    if (p->path == FDEC_PATH_MMA)
+        return launch_split_mma(sp, tk, tv, p->head_dim, bf16, p->kv8, grid, stream, launch);
     switch (p->head_dim) {
         case 64: return launch_split_d64(sp, tk, tv, p->rc, bf16, grid, stream, launch);
         case 128: return launch_split_d128(sp, tk, tv, p->rc, bf16, grid, stream, launch);
@@ -248,30 +250,31 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // A 4-D tensor map over one K or V pool: dims (head_dim, and the slot, head and
-// page dims ordered by increasing stride), box = 64 dims x box_rows slots, 128-byte
+// page dims ordered by increasing stride), box = 128 bytes of a row (64 16-bit
+// elements or 128 E4M3 codes; eb = element bytes) x box_rows slots, 128-byte
 // swizzle.  pos[role] receives the coordinate position of slot (0), head (1), page (2).
 fdec_status encode_kv_map(CUtensorMap* map, const fdec_kv_desc& d, int head_dim, int page_size, int hk,
-                          int box_rows, int pos[3]) {
+                          int box_rows, int pos[3], int eb) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr) return fail(FDEC_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     struct Dim {
         uint64_t size, stride;
         int role;
-    } dims[3] = {{static_cast<uint64_t>(page_size), static_cast<uint64_t>(d.stride_token) * 2, 0},
-                 {static_cast<uint64_t>(hk), static_cast<uint64_t>(d.stride_head) * 2, 1},
-                 {static_cast<uint64_t>(d.num_pages), static_cast<uint64_t>(d.stride_page) * 2, 2}};
+    } dims[3] = {{static_cast<uint64_t>(page_size), static_cast<uint64_t>(d.stride_token) * eb, 0},
+                 {static_cast<uint64_t>(hk), static_cast<uint64_t>(d.stride_head) * eb, 1},
+                 {static_cast<uint64_t>(d.num_pages), static_cast<uint64_t>(d.stride_page) * eb, 2}};
     for (Dim& x : dims)
         if (x.size == 1 && x.stride == 0) x.stride = 16;  // any stride works for a single index
     std::stable_sort(dims, dims + 3, [](const Dim& a, const Dim& b) { return a.stride < b.stride; });
     cuuint64_t gdim[4] = {static_cast<cuuint64_t>(head_dim), dims[0].size, dims[1].size, dims[2].size};
     cuuint64_t gstride[3] = {dims[0].stride, dims[1].stride, dims[2].stride};
-    cuuint32_t box[4] = {64, 1, 1, 1};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), 1, 1, 1};
     cuuint32_t estride[4] = {1, 1, 1, 1};
     for (int i = 0; i < 3; ++i) {
         pos[dims[i].role] = i + 1;
         if (dims[i].role == 0) box[i + 1] = static_cast<cuuint32_t>(box_rows);
     }
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(d.base), gdim, gstride, box, estride,
+    CUresult r = enc(map, eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(d.base), gdim, gstride, box, estride,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -329,6 +332,13 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
         return fail(FDEC_ERR_INVALID_ARG, "invalid plan options");
     if (o.path != FDEC_PATH_AUTO && o.path != FDEC_PATH_SIMT && o.path != FDEC_PATH_MMA && o.path != FDEC_PATH_TC)
         return fail(FDEC_ERR_INVALID_ARG, "invalid path option");
+    if (o.kv_dtype != FDEC_KV_SAME && o.kv_dtype != FDEC_KV_E4M3)
+        return fail(FDEC_ERR_INVALID_ARG, "kv_dtype must be FDEC_KV_SAME or FDEC_KV_E4M3");
+    const bool kv8 = o.kv_dtype == FDEC_KV_E4M3;
+    if (kv8 && !split_mma_kv8_supported(head_dim))
+        return fail(FDEC_ERR_UNSUPPORTED, "E4M3 caches support head_dim 128 and 256");
+    if (kv8 && o.path != FDEC_PATH_AUTO && o.path != FDEC_PATH_MMA)
+        return fail(FDEC_ERR_UNSUPPORTED, "E4M3 caches run on the MMA path only");
     const bool mma_ok = head_dim_supported(head_dim);  // every supported head_dim
     const bool tc_ok = head_dim == 128;
     if (o.path == FDEC_PATH_MMA && !mma_ok)
@@ -363,12 +373,15 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
     p->group = num_qo_heads / num_kv_heads;
     p->rows = static_cast<int>(rows_ll);
     p->dtype = dtype;
+    p->kv8 = kv8;
     p->causal = (causal != 0 && q_len > 1) ? 1 : 0;
     // Tensor cores by default where the kernel exists (see split_mma_kernel.cuh for
     // why); the fp32 SIMT kernel on request and for head_dim 256 / 512.
     // The tcgen05 kernel once the rows need more than one 16-row group of the
     // warp-level kernel (which would stream K/V once per group).
-    if (o.path == FDEC_PATH_AUTO)
+    if (kv8)
+        p->path = FDEC_PATH_MMA;
+    else if (o.path == FDEC_PATH_AUTO)
         p->path = (tc_ok && p->rows > kMmaRows) ? FDEC_PATH_TC : (mma_ok ? FDEC_PATH_MMA : FDEC_PATH_SIMT);
     else
         p->path = o.path;
@@ -384,8 +397,8 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
         threads = split_tc_threads(tiles);
     } else if (p->path == FDEC_PATH_MMA) {
         p->rc = kMmaRows;
-        smem = split_mma_smem_bytes(head_dim);
-        threads = split_mma_threads(head_dim);
+        smem = split_mma_smem_bytes(head_dim, kv8);
+        threads = split_mma_threads(head_dim, kv8);
     } else {
         p->rc = std::min(next_pow2(p->rows), split_max_rc(head_dim));
         smem = split_smem_bytes(head_dim, p->rc);
@@ -406,9 +419,11 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
     }
     const int copies = p->hk * p->row_groups;
     const int slots = num_sms * p->ctas_per_sm;
-    // A block unit streams 64 tokens of K and V (64 x D x 4 bytes) at 1/slots of the machine's bandwidth.
+    // A block unit streams 64 tokens of K and V (64 x D x 2 x element bytes) at 1/slots of the
+    // machine's bandwidth.
+    const double kv_bytes_per_token = head_dim * 2.0 * (kv8 ? 1.0 : 2.0);
     const double partial_cost = 2.0 * p->hk * static_cast<double>(p->rows) * (4.0 * head_dim + 8.0) /
-                                (64.0 * head_dim * 4.0 * slots);
+                                (64.0 * kv_bytes_per_token * slots);
     p->blocks_per_split = o.blocks_per_split > 0 ? o.blocks_per_split
                                                  : choose_blocks_per_split(nblocks, copies, slots, partial_cost);
     const int C = p->blocks_per_split;
@@ -585,6 +600,14 @@ fdec_status fdec_run(fdec_plan_t p, const void* q, int64_t q_stride_tok, int64_t
                      fdec_kv_desc v, const int32_t* page_table, int64_t page_table_stride,
                      const int32_t* seq_lens_dev, float scale, float* out, float* lse, void* workspace,
                      cudaStream_t stream) {
+    return fdec_run_scaled(p, q, q_stride_tok, q_stride_head, k, v, page_table, page_table_stride, seq_lens_dev, scale,
+                           1.f, 1.f, out, lse, workspace, stream);
+}
+
+fdec_status fdec_run_scaled(fdec_plan_t p, const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                            fdec_kv_desc k, fdec_kv_desc v, const int32_t* page_table, int64_t page_table_stride,
+                            const int32_t* seq_lens_dev, float scale, float k_scale, float v_scale, float* out,
+                            float* lse, void* workspace, cudaStream_t stream) {
     if (p == nullptr) return fail(FDEC_ERR_INVALID_ARG, "null plan");
     if (q == nullptr || k.base == nullptr || v.base == nullptr || page_table == nullptr || seq_lens_dev == nullptr ||
         out == nullptr)
@@ -593,13 +616,18 @@ fdec_status fdec_run(fdec_plan_t p, const void* q, int64_t q_stride_tok, int64_t
     if (k.num_pages > INT32_MAX || v.num_pages > INT32_MAX) return fail(FDEC_ERR_INVALID_ARG, "too many pages");
     if (page_table_stride < p->max_pages_needed)
         return fail(FDEC_ERR_CAPACITY, "page_table_stride is smaller than ceil(capacity / page_size)");
-    if (!std::isfinite(scale)) return fail(FDEC_ERR_INVALID_ARG, "scale must be finite");
+    if (!std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale) ||
+        !std::isfinite(scale * k_scale * 1.4426950408889634074f))
+        return fail(FDEC_ERR_INVALID_ARG, "scale, k_scale and v_scale must be finite");
+    const int eb = p->kv8 ? 1 : 2;  // bytes per stored K/V element
+    const int64_t stride_unit = 16 / eb;
     const fdec_kv_desc* descs[2] = {&k, &v};
     for (const fdec_kv_desc* d : descs) {
         if (reinterpret_cast<uintptr_t>(d->base) % 16 != 0)
             return fail(FDEC_ERR_LAYOUT, "K/V base must be 16-byte aligned");
-        if (d->stride_page % 8 != 0 || d->stride_head % 8 != 0 || d->stride_token % 8 != 0)
-            return fail(FDEC_ERR_LAYOUT, "K/V strides must be multiples of 8 elements (16 bytes)");
+        if (d->stride_page % stride_unit != 0 || d->stride_head % stride_unit != 0 ||
+            d->stride_token % stride_unit != 0)
+            return fail(FDEC_ERR_LAYOUT, "K/V strides must be multiples of 16 bytes");
         if (d->stride_page < 0 || d->stride_head < 0 || d->stride_token < 0)
             return fail(FDEC_ERR_LAYOUT, "negative K/V stride");
     }
@@ -611,8 +639,9 @@ fdec_status fdec_run(fdec_plan_t p, const void* q, int64_t q_stride_tok, int64_t
 
     if (p->page_size >= 8 && !(p->maps_valid && same_desc(p->map_k, k) && same_desc(p->map_v, v))) {
         const int box_rows = std::min(p->page_size, p->path == FDEC_PATH_TC ? kTcStageTokens : kStageTokens);
-        fdec_status st = encode_kv_map(&p->tmap_k, k, p->head_dim, p->page_size, p->hk, box_rows, p->k_pos);
-        if (st == FDEC_OK) st = encode_kv_map(&p->tmap_v, v, p->head_dim, p->page_size, p->hk, box_rows, p->v_pos);
+        fdec_status st = encode_kv_map(&p->tmap_k, k, p->head_dim, p->page_size, p->hk, box_rows, p->k_pos, eb);
+        if (st == FDEC_OK)
+            st = encode_kv_map(&p->tmap_v, v, p->head_dim, p->page_size, p->hk, box_rows, p->v_pos, eb);
         if (st != FDEC_OK) {
             p->maps_valid = false;
             return st;
@@ -628,14 +657,14 @@ fdec_status fdec_run(fdec_plan_t p, const void* q, int64_t q_stride_tok, int64_t
     sp.q_stride_head = q_stride_head;
     sp.k_base = static_cast<const uint8_t*>(k.base);
     sp.k_pages = k.num_pages;
-    sp.k_sp = k.stride_page * 2;
-    sp.k_sh = k.stride_head * 2;
-    sp.k_st = k.stride_token * 2;
+    sp.k_sp = k.stride_page * eb;
+    sp.k_sh = k.stride_head * eb;
+    sp.k_st = k.stride_token * eb;
     sp.v_base = static_cast<const uint8_t*>(v.base);
     sp.v_pages = v.num_pages;
-    sp.v_sp = v.stride_page * 2;
-    sp.v_sh = v.stride_head * 2;
-    sp.v_st = v.stride_token * 2;
+    sp.v_sp = v.stride_page * eb;
+    sp.v_sh = v.stride_head * eb;
+    sp.v_st = v.stride_token * eb;
     sp.page_table = page_table;
     sp.pt_stride = page_table_stride;
     sp.seq_lens = seq_lens_dev;
@@ -653,7 +682,8 @@ fdec_status fdec_run(fdec_plan_t p, const void* q, int64_t q_stride_tok, int64_t
     sp.rows = p->rows;
     sp.page_shift = p->page_shift;
     sp.causal = p->causal;
-    sp.scale_log2 = scale * 1.4426950408889634074f;
+    sp.scale_log2 = scale * k_scale * 1.4426950408889634074f;
+    sp.v_scale = v_scale;
     sp.k_pos_slot = p->k_pos[0];
     sp.k_pos_head = p->k_pos[1];
     sp.k_pos_page = p->k_pos[2];

@@ -54,7 +54,8 @@ struct SplitParams {
     float* lse;                // [B*Q*Hq] or null
     unsigned* err;
     int q_len, hq, hk, group, rows, page_shift, causal;
-    float scale_log2;          // scale * log2(e): logits are kept in log2 units
+    float scale_log2;          // scale * k_scale * log2(e): logits are kept in log2 units
+    float v_scale;             // value scale (quantised caches; 1 otherwise), applied to O
     // Coordinate position (1..3) of the slot, head and page dims in each tensor map.
     int k_pos_slot, k_pos_head, k_pos_page;
     int v_pos_slot, v_pos_head, v_pos_page;
@@ -89,11 +90,13 @@ cudaError_t launch_split_d256(const SplitParams& p, const CUtensorMap& tk, const
 cudaError_t launch_split_d512(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int rc,
                                bool bf16, dim3 grid, cudaStream_t s, bool launch);
 
-// The tensor-core split kernel (head_dim 64, 128, 192, 256, 512; query rows in groups of 16).
+// The tensor-core split kernel (head_dim 64, 128, 192, 256, 512; query rows in
+// groups of 16).  kv8: K/V stored as E4M3 codes (head_dim 128 and 256).
 cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int head_dim,
-                             bool bf16, dim3 grid, cudaStream_t s, bool launch);
-size_t split_mma_smem_bytes(int head_dim);
-int split_mma_threads(int head_dim);
+                             bool bf16, bool kv8, dim3 grid, cudaStream_t s, bool launch);
+size_t split_mma_smem_bytes(int head_dim, bool kv8);
+int split_mma_threads(int head_dim, bool kv8);
+inline bool split_mma_kv8_supported(int head_dim) { return head_dim == 128 || head_dim == 256; }
 constexpr int kMmaRows = 16;
 
 // The tcgen05 dense-query split kernel (head_dim 128; `tiles` (1 or 2) 128-row

@@ -3,7 +3,8 @@
 // zeroing of a partial stage's tail, and the epilogue that merges the consumer
 // warps' (m, l, o) states and writes a partial or the final out / lse.
 //
-// Stage layout (per K and per V): D/64 regions of [32 rows][128 bytes]; the
+// Stage layout (per K and per V): D x (element bytes) / 128 regions of
+// [32 rows][128 bytes] (D/64 for 16-bit storage, D/128 for E4M3 codes); the
 // 16-byte chunk c of row r sits at chunk position c ^ (r & 7) (TMA SWIZZLE_128B).
 // Stage i completes barrier full[i % 2S] (phase i / 2S) and is released on
 // empty[i % S]; see the consumer loops for why 2S full barriers are needed.
@@ -26,10 +27,11 @@ __device__ __forceinline__ void static_for(F&& f) {
     }
 }
 
-template <int D, int TOK = kStageTokens>
+template <int D, int TOK = kStageTokens, int EB = 2>
 struct StageGeom {
     static constexpr int TOKENS = TOK;                         // token rows per stage
-    static constexpr int REGIONS = D / 64;
+    static constexpr int ROW_BYTES = D * EB;                   // one token's K (or V) row
+    static constexpr int REGIONS = ROW_BYTES / 128;
     static constexpr int REGION_BYTES = TOK * 128;             // TOK rows x 128 B
     static constexpr int HALF_BYTES = REGIONS * REGION_BYTES;  // K (or V) of one stage
     static constexpr int STAGE_BYTES = 2 * HALF_BYTES;         // K regions then V regions
@@ -123,12 +125,14 @@ __device__ __forceinline__ void init_stage_barriers(uint64_t* full, uint64_t* em
 }
 
 // The producer warp: fills stage i (TOK tokens) into slot i % S once the slot is released.
-template <int D, int S, int TOK = kStageTokens>
+// EB: bytes per stored K/V element (2: 16-bit, 1: E4M3 codes).
+template <int D, int S, int TOK = kStageTokens, int EB = 2>
 __device__ __forceinline__ void produce_stages(const SplitParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv, uint64_t* full,
                                uint64_t* empty, uint8_t* stages, int b, int kvh, const ItemRange& ir,
                                bool tma_mode) {
-    using G = StageGeom<D, TOK>;
+    using G = StageGeom<D, TOK, EB>;
     static_assert(TOK % 32 == 0 && TOK <= 256, "stage rows");
+    static_assert(G::ROW_BYTES % 128 == 0, "rows of whole 128-byte regions");
     const int lane = threadIdx.x & 31;
     const int tok_begin = ir.tok_begin;
     const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride;
@@ -153,7 +157,7 @@ __device__ __forceinline__ void produce_stages(const SplitParams& p, const CUten
         const int tok_end = ir.tok_end, n_stage = ir.n_stage;
         if (n_stage == 0) return;
         const int n_box = (tok_end - tok_begin + BR - 1) / BR;
-        const uint32_t box_bytes = static_cast<uint32_t>(BR) * 2u * (2u * D);  // K and V
+        const uint32_t box_bytes = static_cast<uint32_t>(BR) * 2u * G::ROW_BYTES;  // K and V
         int group = 0;
         for (int i = 0; i < n_stage; ++i) {
             const int s = i % S;
@@ -192,9 +196,10 @@ __device__ __forceinline__ void produce_stages(const SplitParams& p, const CUten
                               v3 = coord(3, p.v_pos_slot, p.v_pos_head);
 #pragma unroll
                     for (int r = 0; r < G::REGIONS; ++r) {
-                        tma_load_4d(smem_addr(kdst + r * G::REGION_BYTES), tmk, r * 64, k1, k2, k3, fbar);
-                        tma_load_4d(smem_addr(kdst + G::HALF_BYTES + r * G::REGION_BYTES), tmv, r * 64, v1, v2, v3,
-                                    fbar);
+                        // x = the region's first element: 128 bytes per region, a multiple of 16 bytes
+                        tma_load_4d(smem_addr(kdst + r * G::REGION_BYTES), tmk, r * (128 / EB), k1, k2, k3, fbar);
+                        tma_load_4d(smem_addr(kdst + G::HALF_BYTES + r * G::REGION_BYTES), tmv, r * (128 / EB), v1,
+                                    v2, v3, fbar);
                     }
                 }
             }
@@ -204,7 +209,7 @@ __device__ __forceinline__ void produce_stages(const SplitParams& p, const CUten
         // Small pages: 16-byte cp.async per (row, chunk) into the swizzled layout.
         const int tok_end = ir.tok_end, n_stage = ir.n_stage;
         if (n_stage == 0) return;
-        constexpr int CHUNKS = D / 8;
+        constexpr int CHUNKS = G::ROW_BYTES / 16;
         for (int i = 0; i < n_stage; ++i) {
             const int s = i % S;
             if (i >= S) {
@@ -284,6 +289,8 @@ __device__ __forceinline__ void zero_v_tail(uint8_t* stage, int nv, int tid = th
 // sm_m [NW][RC], sm_l [NW][RC], sm_o [NW][RC][D] and passed a barrier: merge the
 // NW states by log-sum-exp (m in log2 units) and write the split's partial or,
 // when one split covers the sequence, out = O / L and lse = ln 2 * (M + log2 L).
+// O is scaled by v_scale (the value scale of a quantised cache, 1 otherwise): the
+// LSE merge is linear in O, so partials may carry it.
 // NTHREADS consumer threads (from thread 0) share the work.
 template <int NW, int RC, int D, int NTHREADS = NW * 32>
 __device__ __forceinline__ void merge_and_store(const SplitParams& p, const WorkItem& it, int kvh, int row0,
@@ -310,11 +317,11 @@ __device__ __forceinline__ void merge_and_store(const SplitParams& p, const Work
             const int qi = row / p.group;
             const int h = kvh * p.group + (row - qi * p.group);
             const int64_t orow = static_cast<int64_t>(it.seq * p.q_len + qi) * p.hq + h;
-            p.out[orow * D + d] = Ls > 0.f ? O / Ls : 0.f;
+            p.out[orow * D + d] = Ls > 0.f ? O / Ls * p.v_scale : 0.f;
             if (d == 0 && p.lse != nullptr) p.lse[orow] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
         } else {
             const int64_t prow = (static_cast<int64_t>(it.slot) * p.hk + kvh) * p.rows + row;
-            p.part_o[prow * D + d] = O;
+            p.part_o[prow * D + d] = O * p.v_scale;
             if (d == 0) p.part_ml[prow] = make_float2(M, Ls);
         }
     }

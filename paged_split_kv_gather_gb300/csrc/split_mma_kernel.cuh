@@ -26,15 +26,31 @@
 // time per stage and SM at 6.8 TB/s for a group of 8 query heads.  The fragment
 // layouts of m16n8k16 keep Q and P in registers, leaving ~260 wavefronts per stage
 // (the K and V reads and the TMA writes).
+//
+// Quantised caches (KV8: K and V stored as 8-bit E4M3 codes, head_dim 128 and
+// 256): the producer stages the codes (half the bytes of a 16-bit cache), and
+// the consumer warp that takes a stage first converts it into its own f16 tile
+// in the same swizzled layout (one hardware conversion per pair of codes; every
+// E4M3 value is exact in f16), releases the stage to the producer, and runs the
+// unchanged contractions on the tile in f16.  A bf16 query is brought to f16 by
+// scaling each query row by a power of two that puts its largest magnitude in
+// f16's top binade [2^14, 2^15): exact for every element within 2^38 of the row's
+// largest, and the factor is taken back out of the row's logit scale.  The
+// cache's k_scale is folded into the logit scale and v_scale into the epilogue.
 #pragma once
+
+#include <type_traits>
+
+#include <cuda_fp8.h>
 
 #include "split_common.cuh"
 
 namespace fdec {
 
-template <int D>
+template <int D, bool KV8 = false>
 struct MmaLayout {
-    using G = StageGeom<D>;
+    using G = StageGeom<D>;                                   // 16-bit tile: what the consumers read
+    using GS = StageGeom<D, kStageTokens, KV8 ? 1 : 2>;       // what the producer stages
     static constexpr int RC = 16;                 // query rows per M tile
     static constexpr int BAR_BYTES = 512;
     static constexpr int Q_BYTES = RC * D * 2;    // 16-bit q rows
@@ -44,7 +60,9 @@ struct MmaLayout {
     // memory and four warps (3 consumers + the producer), 255 registers each.
     // head_dim 256 fits three stages and two consumers per CTA; head_dim 512
     // runs one CTA per SM (stages of 64 KB).
-    static constexpr int CTAS_PER_SM = D <= 256 ? 2 : 1;
+    // E4M3 caches: each consumer group also owns a 16-bit tile (16 KB at head_dim
+    // 128, which still fits two CTAs per SM; 32 KB at 256, one CTA).
+    static constexpr int CTAS_PER_SM = KV8 ? (D <= 128 ? 2 : 1) : (D <= 256 ? 2 : 1);
     // head_dim 512: the O accumulators of all 512 columns would need 256
     // registers, so two consumer warps share each stage, both computing S and
     // each accumulating P V for one half of the columns (DH).
@@ -55,17 +73,82 @@ struct MmaLayout {
     // memory (ldmatrix) at every k-step instead.
     static constexpr bool Q_IN_REGS = D <= 192;
     static constexpr int BUDGET = 232448 / CTAS_PER_SM - 1024;
-    static constexpr int FIXED = BAR_BYTES + Q_BYTES + ALIGN_SLACK;
-    static constexpr int S_FIT = (BUDGET - FIXED) / G::STAGE_BYTES;
+    static constexpr int NP_MAX = 3;
+    static constexpr int TILE_BYTES = KV8 ? NP_MAX * G::STAGE_BYTES : 0;  // after the stage ring
+    static constexpr int FIXED = BAR_BYTES + Q_BYTES + ALIGN_SLACK + TILE_BYTES;
+    static constexpr int S_FIT = (BUDGET - FIXED) / GS::STAGE_BYTES;
     static constexpr int S = S_FIT > 16 ? 16 : S_FIT;
-    static constexpr int NP = (S - 1) < 3 ? (S - 1) : 3;  // consumer groups (stages in flight at once)
+    static constexpr int NP = (S - 1) < NP_MAX ? (S - 1) : NP_MAX;  // consumer groups (stages in flight at once)
     static constexpr int NW = NP * DSPLIT;                 // consumer warps
     static constexpr int THREADS = (NW + 1) * 32;
-    static constexpr int SMEM = FIXED + S * G::STAGE_BYTES;
+    static constexpr int SMEM = FIXED + S * GS::STAGE_BYTES;
     static_assert(S >= NP + 1, "stage ring too small");
+    static_assert(!KV8 || (DSPLIT == 1 && NP == NP_MAX), "E4M3 caches: one warp per stage, a tile per group");
+    static_assert(!KV8 || 3 * S * 8 <= 256, "E4M3 caches keep the query row maxima at byte 256 of the barrier area");
     static_assert(3 * S * 8 <= BAR_BYTES, "barrier area too small");
-    static_assert(NP * RC * (D + 2) * 4 <= S * G::STAGE_BYTES, "merge scratch must fit the stage area");
+    static_assert(NP * RC * (D + 2) * 4 <= S * GS::STAGE_BYTES + TILE_BYTES, "merge scratch must fit the stage area");
 };
+
+// Four E4M3 codes (w's bytes, lowest first) -> two packed f16 pairs (exact; the
+// lower code of each pair lands in the lower half).
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& p01, uint32_t& p23) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(p01), "=r"(p23)
+        : "r"(w));
+}
+
+// One warp converts a staged E4M3 stage (K then V; D/128 regions of [32 rows][128 B]
+// each, chunk c of row r at c ^ (r & 7)) into an f16 tile of the layout the
+// consumers read (D/64 regions).  A code chunk holds dims 16c .. 16c+15 of its
+// region, i.e. 16-bit chunks 2c and 2c+1 of region 2 r8 + c / 4.  Shared memory
+// serves 16-byte accesses eight lanes at a time, so each group of eight lanes
+// takes two adjacent rows (one even, one odd) and complementary halves of their
+// chunks: its eight loads and each of its two sets of eight stores then fall on
+// eight different 16-byte bank groups (no conflict).  Lane l handles chunk
+// c8 = (l & 3) + 4 ((l >> 2 ^ l >> 3) & 1) of rows 2 (l >> 4) + ((l >> 2) & 1) + 4 k,
+// k = 0 .. 7, of every region of K and V; its swizzle offsets depend on k only
+// through k & 1.
+template <int D>
+__device__ __forceinline__ void convert_stage_e4m3(const uint8_t* src, uint8_t* dst, int lane) {
+    using G = StageGeom<D>;
+    using G8 = StageGeom<D, kStageTokens, 1>;
+    static_assert(kStageTokens == 32, "eight rows of four per lane group below");
+    const int odd = (lane >> 2) & 1;
+    const int c8 = (lane & 3) + 4 * (odd ^ ((lane >> 3) & 1));
+    const int row0 = 2 * (lane >> 4) + odd;  // rows row0 + 4 k
+    const int c16 = (c8 & 3) * 2;
+    uint32_t s_off[2], d_lo[2], d_hi[2];  // by k & 1: (row0 + 4 k) & 7 = (row0 & 7) ^ (4 (k & 1))
+#pragma unroll
+    for (int par = 0; par < 2; ++par) {
+        const int r7 = (row0 + 4 * par) & 7;
+        s_off[par] = static_cast<uint32_t>(row0 * 128 + ((c8 ^ r7) << 4));
+        d_lo[par] = static_cast<uint32_t>((c8 >> 2) * G::REGION_BYTES + row0 * 128 + ((c16 ^ r7) << 4));
+        d_hi[par] = static_cast<uint32_t>((c8 >> 2) * G::REGION_BYTES + row0 * 128 + (((c16 + 1) ^ r7) << 4));
+    }
+#pragma unroll 1
+    for (int hv = 0; hv < 2; ++hv) {        // K, then V
+#pragma unroll
+        for (int r8 = 0; r8 < G8::REGIONS; ++r8) {
+            const uint8_t* sreg = src + hv * G8::HALF_BYTES + r8 * G8::REGION_BYTES;
+            uint8_t* dreg = dst + hv * G::HALF_BYTES + 2 * r8 * G::REGION_BYTES;
+            uint4 x[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                x[k] = *reinterpret_cast<const uint4*>(sreg + s_off[k & 1] + k * 512);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                uint4 lo, hi;
+                e4m3x4_to_f16(x[k].x, lo.x, lo.y);
+                e4m3x4_to_f16(x[k].y, lo.z, lo.w);
+                e4m3x4_to_f16(x[k].z, hi.x, hi.y);
+                e4m3x4_to_f16(x[k].w, hi.z, hi.w);
+                *reinterpret_cast<uint4*>(dreg + d_lo[k & 1] + k * 512) = lo;
+                *reinterpret_cast<uint4*>(dreg + d_hi[k & 1] + k * 512) = hi;
+            }
+        }
+    }
+}
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -98,6 +181,12 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
     }
 }
 
+// (x, y) rounded to a packed f16 pair, x in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float x, float y) {
+    const __half2 h = __floats2half2_rn(x, y);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // Round (x, y) to a packed 16-bit pair (x in the low half), and the residual pair.
 template <bool BF16>
 __device__ __forceinline__ void split_pair(float x, float y, uint32_t& hi, uint32_t& lo) {
@@ -114,12 +203,24 @@ __device__ __forceinline__ void split_pair(float x, float y, uint32_t& hi, uint3
     }
 }
 
-template <int D, bool BF16>
-__global__ void __launch_bounds__(MmaLayout<D>::THREADS, MmaLayout<D>::CTAS_PER_SM)
+// A bf16 query row with largest magnitude bits `mbits` (bf16 pattern without the
+// sign) is scaled by 2^sh, sh = 14 - floor(log2 max), so that the largest lands in
+// [2^14, 2^15) (f16's top binade); sh is kept in [-126, 126] so 2^sh and 2^-sh are
+// normal floats.  forward: 2^sh (applied to q), else 2^-sh (applied to its logits).
+__device__ __forceinline__ float q_row_factor(uint32_t mbits, bool forward) {
+    int sh = 0;
+    if (mbits != 0) sh = 14 - (static_cast<int>((mbits >> 7) & 0xFF) - 127);
+    sh = max(-126, min(126, sh));
+    return __int_as_float((127 + (forward ? sh : -sh)) << 23);
+}
+
+template <int D, bool BF16, bool KV8>
+__global__ void __launch_bounds__(MmaLayout<D, KV8>::THREADS, MmaLayout<D, KV8>::CTAS_PER_SM)
 split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
                  const __grid_constant__ CUtensorMap tmv) {
-    using Lay = MmaLayout<D>;
+    using Lay = MmaLayout<D, KV8>;
     using G = StageGeom<D>;
+    using GS = typename Lay::GS;
     constexpr int NW = Lay::NW;
     constexpr int S = Lay::S;
     constexpr int RC = Lay::RC;
@@ -128,6 +229,11 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
     constexpr int DH = Lay::DH;
     constexpr int KSTEPS = D / 16;       // k-steps of S = Q K^T
     constexpr int NT = DH / 8;           // n-tiles of this warp's O
+    constexpr bool MB = KV8 ? false : BF16;  // operand type of the MMAs (f16 over E4M3 caches)
+    constexpr bool QSCALE = KV8 && BF16;     // bf16 query rows rescaled into f16
+    constexpr bool P1 = KV8;                 // one f16 P (11 bits) instead of a 16-bit hi + lo pair
+    constexpr float kP1Scale = 128.f;        // 2^7
+    const float o_out = P1 ? 1.f / kP1Scale : 1.f;
 
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -139,6 +245,7 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
         const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
         stages = smem + Lay::BAR_BYTES + Lay::Q_BYTES + pad;
     }
+    uint8_t* tiles = stages + S * GS::STAGE_BYTES;  // KV8: one 16-bit tile per consumer group
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -157,18 +264,53 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
             prefetch_tmap(&tmk);
             prefetch_tmap(&tmv);
         }
-        produce_stages<D, S>(p, &tmk, &tmv, full, empty, stages, b, kvh, ir, tma_mode);
+        produce_stages<D, S, kStageTokens, KV8 ? 1 : 2>(p, &tmk, &tmv, full, empty, stages, b, kvh, ir, tma_mode);
         return;
     }
     if (threadIdx.x == 0) report_item_range(p, ir);
     // The group's query rows, as stored (16-bit, [RC][D]); rows past the group are zero.
+    // QSCALE: bf16 rows -> f16 rows times 2^sh(row), sh from the row's largest magnitude.
+    uint32_t* q_rmax = reinterpret_cast<uint32_t*>(smem + 256);  // [RC] largest |q| (bf16 bits)
     {
         QChunks<RC, D, NW * 32> qc;
         qc.load(p, b, kvh, row0, threadIdx.x);
+        if constexpr (QSCALE) {
+            if (threadIdx.x < RC) q_rmax[threadIdx.x] = 0u;
+            named_barrier(1, NW * 32);
 #pragma unroll
-        for (int i = 0; i < qc.PER; ++i) {
-            const int idx = qc.chunk(threadIdx.x, i);
-            if (idx < qc.CH) *reinterpret_cast<uint4*>(q_s + idx * 8) = qc.v[i];
+            for (int i = 0; i < qc.PER; ++i) {
+                const int idx = qc.chunk(threadIdx.x, i);
+                if (idx < qc.CH) {
+                    const uint32_t w[4] = {qc.v[i].x, qc.v[i].y, qc.v[i].z, qc.v[i].w};
+                    uint32_t mx = 0;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) mx = max(mx, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
+                    atomicMax(&q_rmax[idx / (D / 8)], mx);  // bf16 magnitudes order as integers
+                }
+            }
+            named_barrier(1, NW * 32);
+#pragma unroll
+            for (int i = 0; i < qc.PER; ++i) {
+                const int idx = qc.chunk(threadIdx.x, i);
+                if (idx < qc.CH) {
+                    const float f = q_row_factor(q_rmax[idx / (D / 8)], true);
+                    const uint32_t w[4] = {qc.v[i].x, qc.v[i].y, qc.v[i].z, qc.v[i].w};
+                    uint32_t h[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 v = unpack2<true>(w[e]);
+                        const __half2 hv = __floats2half2_rn(v.x * f, v.y * f);
+                        h[e] = *reinterpret_cast<const uint32_t*>(&hv);
+                    }
+                    *reinterpret_cast<uint4*>(q_s + idx * 8) = make_uint4(h[0], h[1], h[2], h[3]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < qc.PER; ++i) {
+                const int idx = qc.chunk(threadIdx.x, i);
+                if (idx < qc.CH) *reinterpret_cast<uint4*>(q_s + idx * 8) = qc.v[i];
+            }
         }
     }
     named_barrier(1, NW * 32);
@@ -211,7 +353,12 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
         const int qi = (row0 + g + 8 * h) / p.group;
         lim[h] = p.causal ? (ir.L - p.q_len + qi) : (ir.L - 1);
     }
-    const uint32_t stages_base = smem_addr(stages);
+    // Logit scale of rows g and g + 8 (QSCALE: the row factor taken back out).
+    float sl[2] = {p.scale_log2, p.scale_log2};
+    if constexpr (QSCALE) {
+        sl[0] = p.scale_log2 * q_row_factor(q_rmax[g], false);
+        sl[1] = p.scale_log2 * q_row_factor(q_rmax[g + 8], false);
+    }
     bool ok = true;
 
     const int grp = warp / DSPLIT;             // consumer group: stages grp, grp + NP, ...
@@ -225,9 +372,19 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
         }
         const int t0 = ir.tok_begin + i * kStageTokens;
         const int nv = min(kStageTokens, ir.tok_end - t0);
-        const uint32_t kbase = stages_base + s * G::STAGE_BYTES;
+        uint8_t* tile;
+        if constexpr (KV8) {
+            // codes -> this group's 16-bit tile; the stage goes back to the producer at once
+            tile = tiles + grp * G::STAGE_BYTES;
+            convert_stage_e4m3<D>(stages + s * GS::STAGE_BYTES, tile, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+        } else {
+            tile = stages + s * G::STAGE_BYTES;
+        }
+        const uint32_t kbase = smem_addr(tile);
         const uint32_t vbase = kbase + G::HALF_BYTES;
-        if (nv < kStageTokens) zero_v_tail<D>(stages + s * G::STAGE_BYTES, nv);
+        if (nv < kStageTokens) zero_v_tail<D>(tile, nv);
 
         // S = Q K^T for the stage's 32 tokens (4 n-tiles of 8)
         float sc[4][4];
@@ -241,8 +398,8 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
             for (int pr = 0; pr < 2; ++pr) {
                 uint32_t b0, b1, b2, b3;
                 ldmatrix_x4(kbase + (kk >> 2) * G::REGION_BYTES + kb_row[pr] + kb_x[kk & 3], b0, b1, b2, b3);
-                mma_16816<BF16>(sc[2 * pr], qa[qk], b0, b1);
-                mma_16816<BF16>(sc[2 * pr + 1], qa[qk], b2, b3);
+                mma_16816<MB>(sc[2 * pr], qa[qk], b0, b1);
+                mma_16816<MB>(sc[2 * pr + 1], qa[qk], b2, b3);
             }
         });
 
@@ -256,7 +413,7 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int tok = 8 * n + 2 * tq + (e & 1);
-                float z = sc[n][e] * p.scale_log2;
+                float z = sc[n][e] * sl[e >> 1];
                 if (tok >= ((e >> 1) ? vis1 : vis0)) z = -INFINITY;
                 sc[n][e] = z;
                 if (e >> 1)
@@ -296,14 +453,23 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
             lrow[0] += sc[n][0] + sc[n][1];
             lrow[1] += sc[n][2] + sc[n][3];
         }
-        // P as A fragments of two k-steps of 16 tokens, split into high and residual parts
+        // P as A fragments of two k-steps of 16 tokens: split into high and residual
+        // parts, or (P1) one f16 value scaled by 2^7 (p <= 2^8 by the lazy rescale, so
+        // p 2^7 <= 2^15 fits f16, and small p stay normal); O then carries 2^7.
         uint32_t ph[2][4], pl[2][4];
 #pragma unroll
         for (int k2 = 0; k2 < 2; ++k2) {
-            split_pair<BF16>(sc[2 * k2][0], sc[2 * k2][1], ph[k2][0], pl[k2][0]);
-            split_pair<BF16>(sc[2 * k2][2], sc[2 * k2][3], ph[k2][1], pl[k2][1]);
-            split_pair<BF16>(sc[2 * k2 + 1][0], sc[2 * k2 + 1][1], ph[k2][2], pl[k2][2]);
-            split_pair<BF16>(sc[2 * k2 + 1][2], sc[2 * k2 + 1][3], ph[k2][3], pl[k2][3]);
+            if constexpr (P1) {
+                ph[k2][0] = pack_f16x2(sc[2 * k2][0] * kP1Scale, sc[2 * k2][1] * kP1Scale);
+                ph[k2][1] = pack_f16x2(sc[2 * k2][2] * kP1Scale, sc[2 * k2][3] * kP1Scale);
+                ph[k2][2] = pack_f16x2(sc[2 * k2 + 1][0] * kP1Scale, sc[2 * k2 + 1][1] * kP1Scale);
+                ph[k2][3] = pack_f16x2(sc[2 * k2 + 1][2] * kP1Scale, sc[2 * k2 + 1][3] * kP1Scale);
+            } else {
+                split_pair<MB>(sc[2 * k2][0], sc[2 * k2][1], ph[k2][0], pl[k2][0]);
+                split_pair<MB>(sc[2 * k2][2], sc[2 * k2][3], ph[k2][1], pl[k2][1]);
+                split_pair<MB>(sc[2 * k2 + 1][0], sc[2 * k2 + 1][1], ph[k2][2], pl[k2][2]);
+                split_pair<MB>(sc[2 * k2 + 1][2], sc[2 * k2 + 1][3], ph[k2][3], pl[k2][3]);
+            }
         }
         // O += P V
 #pragma unroll
@@ -313,15 +479,19 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
                 uint32_t b0, b1, b2, b3;
                 ldmatrix_x4_trans(vbase + v_half + (jp >> 2) * G::REGION_BYTES + vb_row[k2] + vb_x[jp & 3], b0, b1, b2,
                                   b3);
-                mma_16816<BF16>(o[2 * jp], ph[k2], b0, b1);
-                mma_16816<BF16>(o[2 * jp], pl[k2], b0, b1);
-                mma_16816<BF16>(o[2 * jp + 1], ph[k2], b2, b3);
-                mma_16816<BF16>(o[2 * jp + 1], pl[k2], b2, b3);
+                mma_16816<MB>(o[2 * jp], ph[k2], b0, b1);
+                if constexpr (!P1) mma_16816<MB>(o[2 * jp], pl[k2], b0, b1);
+                mma_16816<MB>(o[2 * jp + 1], ph[k2], b2, b3);
+                if constexpr (!P1) mma_16816<MB>(o[2 * jp + 1], pl[k2], b2, b3);
             });
         }
-        if (nv < kStageTokens) fence_proxy_async_shared();  // generic zeroing before the slot's next TMA write
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+        if constexpr (KV8) {
+            __syncwarp();  // every lane's reads of the tile precede its next conversion
+        } else {
+            if (nv < kStageTokens) fence_proxy_async_shared();  // generic zeroing before the slot's next TMA write
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+        }
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -345,29 +515,31 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
     }
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-        *reinterpret_cast<float2*>(sm_o + (grp * RC + g) * D + half * DH + 8 * n + 2 * tq) = make_float2(o[n][0], o[n][1]);
+        *reinterpret_cast<float2*>(sm_o + (grp * RC + g) * D + half * DH + 8 * n + 2 * tq) =
+            make_float2(o[n][0] * o_out, o[n][1] * o_out);
         *reinterpret_cast<float2*>(sm_o + (grp * RC + g + 8) * D + half * DH + 8 * n + 2 * tq) =
-            make_float2(o[n][2], o[n][3]);
+            make_float2(o[n][2] * o_out, o[n][3] * o_out);
     }
     named_barrier(1, NW * 32);
     merge_and_store<NP, RC, D, NW * 32>(p, it, kvh, row0, sm_m, sm_l, sm_o);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool KV8 = false>
 cudaError_t launch_split_mma_one(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
                                  cudaStream_t stream, bool launch) {
-    using Lay = MmaLayout<D>;
+    using Lay = MmaLayout<D, KV8>;
     static unsigned long long attr_done = 0;  // one bit per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-        e = cudaFuncSetAttribute(split_mma_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::SMEM);
+        e = cudaFuncSetAttribute(split_mma_kernel<D, BF16, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Lay::SMEM);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_RELEASE);
     }
     if (!launch) return cudaSuccess;
-    split_mma_kernel<D, BF16><<<grid, Lay::THREADS, Lay::SMEM, stream>>>(p, tk, tv);
+    split_mma_kernel<D, BF16, KV8><<<grid, Lay::THREADS, Lay::SMEM, stream>>>(p, tk, tv);
     return cudaGetLastError();
 }
 

@@ -414,7 +414,7 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
                 tmem_wait_ld();
                 if (row < p.rows) {
                     float* dst = it.slot < 0 ? p.out + orow * D + c0 : p.part_o + prow * D + c0;
-                    const float f = it.slot < 0 ? inv : 1.f;
+                    const float f = (it.slot < 0 ? inv : 1.f) * p.v_scale;
 #pragma unroll
                     for (int c = 0; c < 32; c += 4)
                         *reinterpret_cast<float4*>(dst + c) =

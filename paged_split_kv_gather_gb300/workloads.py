@@ -244,8 +244,11 @@ def _add_spikes(rng, k, q, table, lens, page_size, scale, frac, g):
         for kvh in range(hk):
             qbar = q[b, :, kvh * g:(kvh + 1) * g].float().mean(dim=(0, 1))
             alpha = 8.0 / (scale * float(qbar.pow(2).sum()))
-            rows = k[pages, kvh, slots].float() + alpha * qbar
-            k[pages, kvh, slots] = rows.to(k.dtype)
+            rows = (k[pages, kvh, slots].float() + alpha * qbar).to(k.dtype)
+            if k.element_size() == 1:  # write E4M3 codes through a byte view
+                k.view(torch.uint8)[pages, kvh, slots] = rows.view(torch.uint8)
+            else:
+                k[pages, kvh, slots] = rows
 
 
 def _nan_fill_unread(k, v, table, lens, page_size, dtype):

@@ -77,11 +77,14 @@ OUT_TOL = 2e-3   # max over rows of ||out - ref||_inf / ||ref||_inf
 LSE_TOL = 1e-4   # max |lse - ref|
 
 
-def gpu_run(w: Workload, capacities=None, seq_lens=None, stream=None, **plan_opts):
-    """Plan, upload and run the library on a CUDA workload; returns (out, lse, PagedDecode)."""
+def gpu_run(w: Workload, capacities=None, seq_lens=None, stream=None, k_scale=None, v_scale=None, **plan_opts):
+    """Plan, upload and run the library on a CUDA workload; returns (out, lse, PagedDecode).
+    With k_scale / v_scale the scaled entry point runs."""
     import paged_split_kv_gather_gb300 as fd
 
     dev = w.q.device
+    if w.kv_dtype:
+        plan_opts.setdefault("kv_dtype", w.kv_dtype)
     caps = w.seq_lens if capacities is None else capacities
     pd = fd.PagedDecode(caps, w.q_len, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
                         w.causal, device=dev, stream=stream, **plan_opts)
@@ -91,9 +94,9 @@ def gpu_run(w: Workload, capacities=None, seq_lens=None, stream=None, **plan_opt
     lens = torch.as_tensor(w.seq_lens if seq_lens is None else seq_lens, dtype=torch.int32, device=dev)
     # every storage the workload holds (q and the K/V pools) must come back bit-identical
     before = [t.clone() for t in w.keep]
-    pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale, stream=stream)
+    pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale, stream=stream, k_scale=k_scale, v_scale=v_scale)
     for a, b in zip(before, w.keep):
-        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), "an input buffer changed"
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), "an input buffer changed"
     return out, lse, pd
 
 

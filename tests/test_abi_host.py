@@ -240,3 +240,52 @@ def test_binding_refuses_views_without_a_unit_dim_stride():
     q = torch.zeros(2, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fd._q_strides(q.transpose(2, 3).contiguous().transpose(2, 3))
+
+
+def test_e4m3_cache_plans_on_the_mma_path_only():
+    for d in (128, 256):
+        info = fd.fdec_plan_get_info(_plan([1000], head_dim=d, kv_dtype="fp8"))
+        assert info["path"] == fd.FDEC_PATH_MMA
+    # rows above 16 stay on the 16-row kernel (row groups) for E4M3 caches
+    info = fd.fdec_plan_get_info(_plan([8200] * 4, q_len=8, causal=True, kv_dtype="fp8"))
+    assert info["path"] == fd.FDEC_PATH_MMA and info["row_groups"] == 2
+    for kw in (dict(head_dim=64), dict(head_dim=192), dict(head_dim=512), dict(path=fd.FDEC_PATH_TC),
+               dict(path=fd.FDEC_PATH_SIMT)):
+        with pytest.raises(fd.FdecError) as ei:
+            _plan([1000], kv_dtype="fp8", **kw)
+        assert ei.value.status_name == "FDEC_ERR_UNSUPPORTED"
+
+
+def _run_scaled_raw(plan, k, v, k_scale=1.0, v_scale=1.0):
+    lib = fd._load()
+    st = lib.fdec_run_scaled(plan.handle, 0x10000, 128, 128 * 8, k, v, 0x40000, 256, 0x50000, ctypes.c_float(0.1),
+                             ctypes.c_float(k_scale), ctypes.c_float(v_scale), 0x20000, None, 0x30000, None)
+    return fd.STATUS_NAMES[st]
+
+
+def test_e4m3_strides_are_checked_in_bytes_and_scales_must_be_finite():
+    plan = _plan([2048], num_qo_heads=8, num_kv_heads=1, head_dim=128, kv_dtype="fp8")
+    good = fd.KVDesc(0x100000, 10, 16 * 128, 0, 128)
+    assert _run_scaled_raw(plan, good, good) == "FDEC_ERR_WORKSPACE"  # valid, never uploaded
+    # 8 elements is 16 bytes of a 16-bit cache but only 8 bytes of codes
+    assert _run_scaled_raw(plan, good, fd.KVDesc(0x100000, 10, 16 * 128 + 8, 0, 128)) == "FDEC_ERR_LAYOUT"
+    assert _run_scaled_raw(plan, good, fd.KVDesc(0x100000, 10, 16 * 128 + 16, 0, 128)) == "FDEC_ERR_WORKSPACE"
+    for ks, vs in ((float("inf"), 1.0), (1.0, float("nan")), (-float("inf"), 1.0)):
+        assert _run_scaled_raw(plan, good, good, ks, vs) == "FDEC_ERR_INVALID_ARG"
+
+
+def test_binding_refuses_k_v_of_the_wrong_element_size():
+    import torch
+
+    plan = _plan([64], num_qo_heads=8, num_kv_heads=1, head_dim=128, kv_dtype="fp8")
+    k16 = torch.zeros(4, 1, 16, 128, dtype=torch.bfloat16)
+    k8 = torch.zeros(4, 1, 16, 128, dtype=torch.float8_e4m3fn)
+    q = torch.zeros(1, 1, 8, 128, dtype=torch.bfloat16)
+    out = torch.zeros(1, 1, 8, 128)
+    with pytest.raises(ValueError):
+        fd.fdec_run_scaled(plan, q, k16, k16, torch.zeros(1, 4, dtype=torch.int32), torch.zeros(1, dtype=torch.int32),
+                           out, None, torch.zeros(256, dtype=torch.uint8), k_scale=0.5)
+    plan16 = _plan([64], num_qo_heads=8, num_kv_heads=1, head_dim=128)
+    with pytest.raises(ValueError):
+        fd.fdec_run(plan16, q, k8, k8, torch.zeros(1, 4, dtype=torch.int32), torch.zeros(1, dtype=torch.int32),
+                    out, None, torch.zeros(256, dtype=torch.uint8))
