@@ -246,6 +246,17 @@ fdec_status fdec_append(const void* k_new, const void* v_new, int64_t new_stride
                         int head_dim, int page_size, fdec_kv_desc k, fdec_kv_desc v, const int32_t* page_table,
                         int batch, int64_t page_table_stride, uint32_t* device_errors, cudaStream_t stream);
 
+/*
+ * fdec_append for E4M3 caches (FDEC_KV_E4M3): k_new / v_new hold E4M3 codes,
+ * one byte per element, and are copied into the code pools unchanged (the
+ * caller quantises with its k_scale / v_scale; the library never re-rounds).
+ * Strides are in bytes and must be multiples of 16; otherwise as fdec_append.
+ */
+fdec_status fdec_append_e4m3(const void* k_new, const void* v_new, int64_t new_stride_tok, int64_t new_stride_head,
+                             const int32_t* batch_indices, const int32_t* positions, int n_tokens, int num_kv_heads,
+                             int head_dim, int page_size, fdec_kv_desc k, fdec_kv_desc v, const int32_t* page_table,
+                             int batch, int64_t page_table_stride, uint32_t* device_errors, cudaStream_t stream);
+
 /* Release a plan (NULL is a no-op). */
 fdec_status fdec_plan_destroy(fdec_plan_t plan);
 

@@ -22,7 +22,7 @@ __all__ = [
     "fdec_plan_set_split_event", "fdec_read_device_errors", "fdec_last_error", "fdec_version",
     "fdec_run_static_workspace", "fdec_append", "kv_desc", "library_path", "PagedDecode", "EXPORTED_SYMBOLS",
     "FDEC_F16", "FDEC_BF16", "FDEC_PATH_AUTO", "FDEC_PATH_SIMT", "FDEC_PATH_MMA", "FDEC_PATH_TC",
-    "FDEC_KV_SAME", "FDEC_KV_E4M3", "fdec_run_scaled",
+    "FDEC_KV_SAME", "FDEC_KV_E4M3", "fdec_run_scaled", "fdec_append_e4m3",
     "DEVERR_PAGE_ID", "DEVERR_SEQ_LEN", "DEVERR_TIMEOUT",
 ]
 
@@ -45,7 +45,7 @@ EXPORTED_SYMBOLS = (
     "fdec_plan", "fdec_plan_upload", "fdec_run", "fdec_merge_states", "fdec_plan_destroy",
     "fdec_plan_get_info", "fdec_plan_get_splits", "fdec_plan_set_split_event",
     "fdec_read_device_errors", "fdec_last_error", "fdec_version", "fdec_run_static_workspace", "fdec_append",
-    "fdec_run_scaled",
+    "fdec_run_scaled", "fdec_append_e4m3",
 )
 
 
@@ -117,6 +117,8 @@ def _load():
         lib.fdec_merge_states.argtypes = [P, P, I, I, I, P, P, P]
         lib.fdec_append.restype = I
         lib.fdec_append.argtypes = [P, P, I64, I64, P, P, I, I, I, I, KVDesc, KVDesc, P, I, I64, P, P]
+        lib.fdec_append_e4m3.restype = I
+        lib.fdec_append_e4m3.argtypes = [P, P, I64, I64, P, P, I, I, I, I, KVDesc, KVDesc, P, I, I64, P, P]
         lib.fdec_plan_destroy.restype = I
         lib.fdec_plan_destroy.argtypes = [P]
         lib.fdec_plan_get_info.restype = I
@@ -315,21 +317,38 @@ def fdec_run_static_workspace(plan: Plan, q, k, v, page_table, seq_lens, out, ls
                                              None if lse is None else lse.data_ptr(), _stream_handle(stream)))
 
 
+def _append(entry, elem_bytes, k_new, v_new, batch_indices, positions, k, v, page_table, page_size, device_errors,
+            stream):
+    if k_new.dim() != 3 or v_new.shape != k_new.shape or k_new.stride(2) != 1 or v_new.stride(2) != 1:
+        raise ValueError("k_new and v_new must be [n, Hk, D] with a unit dim stride")
+    if k_new.stride() != v_new.stride():
+        raise ValueError("k_new and v_new must have the same strides")
+    for t in (k_new, v_new, k, v):
+        if t.element_size() != elem_bytes:
+            raise ValueError(f"expected {elem_bytes}-byte elements, got {t.dtype}")
+    n, hk, d = k_new.shape
+    _check(entry(k_new.data_ptr(), v_new.data_ptr(), k_new.stride(0), k_new.stride(1), batch_indices.data_ptr(),
+                 positions.data_ptr(), n, hk, d, page_size, kv_desc(k), kv_desc(v), page_table.data_ptr(),
+                 page_table.shape[0], page_table.stride(0),
+                 None if device_errors is None else device_errors.data_ptr(), _stream_handle(stream)))
+
+
 def fdec_append(k_new, v_new, batch_indices, positions, k, v, page_table, page_size: int, device_errors=None,
                 stream=None) -> None:
     """Write new tokens into the paged cache: k_new / v_new [n, Hk, D] (16-bit, unit
     dim stride), batch_indices / positions int32 [n] (device); k / v the cache
     views [page, kv_head, slot, dim]; page_table int32 [batch, stride];
     device_errors an optional int32/uint32 device tensor of one element."""
-    if k_new.dim() != 3 or v_new.shape != k_new.shape or k_new.stride(2) != 1 or v_new.stride(2) != 1:
-        raise ValueError("k_new and v_new must be [n, Hk, D] with a unit dim stride")
-    if k_new.stride() != v_new.stride():
-        raise ValueError("k_new and v_new must have the same strides")
-    n, hk, d = k_new.shape
-    _check(_load().fdec_append(k_new.data_ptr(), v_new.data_ptr(), k_new.stride(0), k_new.stride(1),
-                               batch_indices.data_ptr(), positions.data_ptr(), n, hk, d, page_size, kv_desc(k),
-                               kv_desc(v), page_table.data_ptr(), page_table.shape[0], page_table.stride(0),
-                               None if device_errors is None else device_errors.data_ptr(), _stream_handle(stream)))
+    _append(_load().fdec_append, 2, k_new, v_new, batch_indices, positions, k, v, page_table, page_size,
+            device_errors, stream)
+
+
+def fdec_append_e4m3(k_new, v_new, batch_indices, positions, k, v, page_table, page_size: int, device_errors=None,
+                     stream=None) -> None:
+    """fdec_append for E4M3 caches: k_new / v_new and the pools hold 1-byte codes
+    (torch.float8_e4m3fn or uint8), copied unchanged."""
+    _append(_load().fdec_append_e4m3, 1, k_new, v_new, batch_indices, positions, k, v, page_table, page_size,
+            device_errors, stream)
 
 
 def fdec_merge_states(o, lse, o_out, lse_out=None, stream=None) -> None:

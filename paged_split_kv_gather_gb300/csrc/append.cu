@@ -1,10 +1,14 @@
 // append.cu -- paged KV append: scatter new tokens' K and V rows into the pages
-// the page table names (the write side of the cache).
+// the page table names (the write side of the cache), for 16-bit caches and for
+// E4M3 code caches alike (rows are moved as bytes).
 //
-// One thread per 16-byte chunk of a (token, KV head) row, for K and V; grid-
-// stride loop.  Reads of the new rows are coalesced; each chunk lands at
-// base + page * stride_page + head * stride_head + slot * stride_token.
-// HBM-bound: 2 x n_tokens x Hk x D x 2 bytes read and as many written.
+// One thread per 16-byte chunk of a (token, KV head) row, K chunks then V
+// chunks; grid-stride over at most eight CTAs of 256 threads per SM.  Reads of
+// the new rows are coalesced; each chunk lands at base + page * stride_page +
+// head * stride_head + slot * stride_token of its pool.  HBM-bound: the new rows
+// are read once and written once.  (Measured: four chunks per thread with all
+// loads issued first, on an uncapped grid, was slower: 59.4 against 57.3 us for
+// 268 MB, 9.2 against 6.1 us for one token per sequence.)
 #include <cstdint>
 
 #include "../../include/fdec.h"
@@ -12,8 +16,10 @@
 
 namespace fdec {
 
-__global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
-    const int chunks_row = p.head_dim / 8;
+constexpr int kAppendThreads = 256;
+
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendParams p) {
+    const int chunks_row = p.row_bytes / 16;
     const int64_t per_token = static_cast<int64_t>(p.hk) * chunks_row;
     const int64_t total = static_cast<int64_t>(p.n_tokens) * per_token;
     const int page_mask = (1 << p.page_shift) - 1;
@@ -37,23 +43,31 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
             if (c == 0 && h == 0 && !is_v && p.err != nullptr) atomicOr(p.err, FDEC_DEVERR_PAGE_ID);
             continue;
         }
-        const uint16_t* src = (is_v ? p.v_new : p.k_new) + static_cast<int64_t>(i) * p.new_st +
-                              static_cast<int64_t>(h) * p.new_sh + c * 8;
-        uint16_t* dst = (is_v ? p.v_base : p.k_base) +
-                        static_cast<int64_t>(page) * (is_v ? p.v_sp : p.k_sp) +
-                        static_cast<int64_t>(h) * (is_v ? p.v_sh : p.k_sh) +
-                        static_cast<int64_t>(t & page_mask) * (is_v ? p.v_st : p.k_st) + c * 8;
+        const uint8_t* src = (is_v ? p.v_new : p.k_new) + static_cast<int64_t>(i) * p.new_st +
+                             static_cast<int64_t>(h) * p.new_sh + c * 16;
+        uint8_t* dst = (is_v ? p.v_base : p.k_base) + static_cast<int64_t>(page) * (is_v ? p.v_sp : p.k_sp) +
+                       static_cast<int64_t>(h) * (is_v ? p.v_sh : p.k_sh) +
+                       static_cast<int64_t>(t & page_mask) * (is_v ? p.v_st : p.k_st) + c * 16;
         *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
     }
 }
 
-cudaError_t launch_append(const AppendParams& p, int num_sms, cudaStream_t s) {
-    const int64_t total = 2LL * p.n_tokens * p.hk * (p.head_dim / 8);
+cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
+    static int sms[64] = {0};  // SM count per device, queried once
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int n_sms = dev < 64 ? sms[dev] : 0;
+    if (n_sms == 0) {
+        e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) sms[dev] = n_sms;
+    }
+    const int64_t total = 2LL * p.n_tokens * p.hk * (p.row_bytes / 16);
     if (total == 0) return cudaSuccess;
-    int64_t blocks = (total + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * 8;
-    if (blocks > cap) blocks = cap;
-    append_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
+    int64_t blocks = (total + kAppendThreads - 1) / kAppendThreads;
+    if (blocks > static_cast<int64_t>(n_sms) * 8) blocks = static_cast<int64_t>(n_sms) * 8;
+    append_kernel<<<static_cast<unsigned>(blocks), kAppendThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

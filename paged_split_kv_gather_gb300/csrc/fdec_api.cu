@@ -728,10 +728,16 @@ fdec_status fdec_run_scaled(fdec_plan_t p, const void* q, int64_t q_stride_tok, 
     return FDEC_OK;
 }
 
-fdec_status fdec_append(const void* k_new, const void* v_new, int64_t new_stride_tok, int64_t new_stride_head,
+}  // extern "C"
+
+namespace {
+
+// Both appends: K/V elements of eb bytes (2: the 16-bit cache types, 1: E4M3 codes).
+fdec_status append_impl(const void* k_new, const void* v_new, int64_t new_stride_tok, int64_t new_stride_head,
                         const int32_t* batch_indices, const int32_t* positions, int n_tokens, int num_kv_heads,
-                        int head_dim, int page_size, fdec_kv_desc k, fdec_kv_desc v, const int32_t* page_table,
-                        int batch, int64_t page_table_stride, uint32_t* device_errors, cudaStream_t stream) {
+                        int head_dim, int page_size, const fdec_kv_desc& k, const fdec_kv_desc& v,
+                        const int32_t* page_table, int batch, int64_t page_table_stride, uint32_t* device_errors,
+                        cudaStream_t stream, int eb) {
     g_last_error.clear();
     if (n_tokens < 0 || num_kv_heads < 1 || batch < 1 || page_table_stride < 1)
         return fail(FDEC_ERR_INVALID_ARG, "need n_tokens >= 0, num_kv_heads >= 1, batch >= 1, page_table_stride >= 1");
@@ -746,55 +752,68 @@ fdec_status fdec_append(const void* k_new, const void* v_new, int64_t new_stride
         return fail(FDEC_ERR_INVALID_ARG, "null pointer");
     if (k.num_pages < 1 || v.num_pages < 1 || k.num_pages > INT32_MAX || v.num_pages > INT32_MAX)
         return fail(FDEC_ERR_INVALID_ARG, "K and V pools need 1 .. 2^31-1 pages");
+    const int64_t unit = 16 / eb;  // elements per 16 bytes
     const fdec_kv_desc* descs[2] = {&k, &v};
     for (const fdec_kv_desc* d : descs) {
         if (reinterpret_cast<uintptr_t>(d->base) % 16 != 0)
             return fail(FDEC_ERR_LAYOUT, "K/V base must be 16-byte aligned");
-        if (d->stride_page % 8 != 0 || d->stride_head % 8 != 0 || d->stride_token % 8 != 0 || d->stride_page < 0 ||
-            d->stride_head < 0 || d->stride_token < 0)
-            return fail(FDEC_ERR_LAYOUT, "K/V strides must be non-negative multiples of 8 elements (16 bytes)");
+        if (d->stride_page % unit != 0 || d->stride_head % unit != 0 || d->stride_token % unit != 0 ||
+            d->stride_page < 0 || d->stride_head < 0 || d->stride_token < 0)
+            return fail(FDEC_ERR_LAYOUT, "K/V strides must be non-negative multiples of 16 bytes");
     }
     if (reinterpret_cast<uintptr_t>(k_new) % 16 != 0 || reinterpret_cast<uintptr_t>(v_new) % 16 != 0 ||
-        new_stride_tok % 8 != 0 || new_stride_head % 8 != 0 || new_stride_tok < 0 || new_stride_head < 0)
-        return fail(FDEC_ERR_LAYOUT, "new K/V rows must start on 16-byte boundaries (strides multiples of 8)");
-    static int sms[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
-    if (dev < 64 && sms[dev] == 0) {
-        int n = 0;
-        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return fail_cuda(e, "querying the SM count");
-        sms[dev] = n;
-    }
+        new_stride_tok % unit != 0 || new_stride_head % unit != 0 || new_stride_tok < 0 || new_stride_head < 0)
+        return fail(FDEC_ERR_LAYOUT, "new K/V rows must start on 16-byte boundaries");
     AppendParams ap;
-    ap.k_new = static_cast<const uint16_t*>(k_new);
-    ap.v_new = static_cast<const uint16_t*>(v_new);
-    ap.new_st = new_stride_tok;
-    ap.new_sh = new_stride_head;
+    ap.k_new = static_cast<const uint8_t*>(k_new);
+    ap.v_new = static_cast<const uint8_t*>(v_new);
+    ap.new_st = new_stride_tok * eb;
+    ap.new_sh = new_stride_head * eb;
     ap.batch_indices = batch_indices;
     ap.positions = positions;
     ap.page_table = page_table;
     ap.pt_stride = page_table_stride;
-    ap.k_base = static_cast<uint16_t*>(const_cast<void*>(k.base));
+    ap.k_base = static_cast<uint8_t*>(const_cast<void*>(k.base));
     ap.k_pages = k.num_pages;
-    ap.k_sp = k.stride_page;
-    ap.k_sh = k.stride_head;
-    ap.k_st = k.stride_token;
-    ap.v_base = static_cast<uint16_t*>(const_cast<void*>(v.base));
+    ap.k_sp = k.stride_page * eb;
+    ap.k_sh = k.stride_head * eb;
+    ap.k_st = k.stride_token * eb;
+    ap.v_base = static_cast<uint8_t*>(const_cast<void*>(v.base));
     ap.v_pages = v.num_pages;
-    ap.v_sp = v.stride_page;
-    ap.v_sh = v.stride_head;
-    ap.v_st = v.stride_token;
+    ap.v_sp = v.stride_page * eb;
+    ap.v_sh = v.stride_head * eb;
+    ap.v_st = v.stride_token * eb;
     ap.err = device_errors;
     ap.n_tokens = n_tokens;
     ap.batch = batch;
     ap.hk = num_kv_heads;
-    ap.head_dim = head_dim;
+    ap.row_bytes = head_dim * eb;
     ap.page_shift = pshift;
-    e = launch_append(ap, dev < 64 ? sms[dev] : 0, stream);
+    const cudaError_t e = launch_append(ap, stream);
     if (e != cudaSuccess) return fail_cuda(e, "launching the append");
     return FDEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fdec_status fdec_append(const void* k_new, const void* v_new, int64_t new_stride_tok, int64_t new_stride_head,
+                        const int32_t* batch_indices, const int32_t* positions, int n_tokens, int num_kv_heads,
+                        int head_dim, int page_size, fdec_kv_desc k, fdec_kv_desc v, const int32_t* page_table,
+                        int batch, int64_t page_table_stride, uint32_t* device_errors, cudaStream_t stream) {
+    return append_impl(k_new, v_new, new_stride_tok, new_stride_head, batch_indices, positions, n_tokens,
+                       num_kv_heads, head_dim, page_size, k, v, page_table, batch, page_table_stride, device_errors,
+                       stream, 2);
+}
+
+fdec_status fdec_append_e4m3(const void* k_new, const void* v_new, int64_t new_stride_tok, int64_t new_stride_head,
+                             const int32_t* batch_indices, const int32_t* positions, int n_tokens, int num_kv_heads,
+                             int head_dim, int page_size, fdec_kv_desc k, fdec_kv_desc v, const int32_t* page_table,
+                             int batch, int64_t page_table_stride, uint32_t* device_errors, cudaStream_t stream) {
+    return append_impl(k_new, v_new, new_stride_tok, new_stride_head, batch_indices, positions, n_tokens,
+                       num_kv_heads, head_dim, page_size, k, v, page_table, batch, page_table_stride, device_errors,
+                       stream, 1);
 }
 
 fdec_status fdec_merge_states(const float* o, const float* lse, int n_states, int rows, int head_dim, float* o_out,

@@ -117,23 +117,24 @@ int split_max_rc(int head_dim);
 int reduce_warps_per_unit(int max_count);
 cudaError_t launch_reduce(const ReduceParams& p, int num_tasks, cudaStream_t s);
 
-// Paged KV append (fdec_append).  Strides in elements.
+// Paged KV append (fdec_append, fdec_append_e4m3).  Strides in bytes; every row
+// is row_bytes long (a multiple of 16) and starts on a 16-byte boundary.
 struct AppendParams {
-    const uint16_t* k_new;
-    const uint16_t* v_new;
+    const uint8_t* k_new;
+    const uint8_t* v_new;
     int64_t new_st, new_sh;
     const int32_t* batch_indices;
     const int32_t* positions;
     const int32_t* page_table;
     int64_t pt_stride;
-    uint16_t* k_base;
+    uint8_t* k_base;
     int64_t k_pages, k_sp, k_sh, k_st;
-    uint16_t* v_base;
+    uint8_t* v_base;
     int64_t v_pages, v_sp, v_sh, v_st;
     unsigned* err;
-    int n_tokens, batch, hk, head_dim, page_shift;
+    int n_tokens, batch, hk, row_bytes, page_shift;
 };
-cudaError_t launch_append(const AppendParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 // One task given by value (p.tasks must be null): used by fdec_merge_states.
 cudaError_t launch_reduce_single(const ReduceParams& p, ReduceTask task, cudaStream_t s);
 

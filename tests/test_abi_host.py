@@ -26,7 +26,7 @@ def built_library():
 def declared_entry_points():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(fdec_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(fdec_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declarations_match_binding_list():

@@ -131,3 +131,68 @@ def test_append_rejects_bad_arguments_on_the_host():
     assert fd.STATUS_NAMES[lib.fdec_append(None, p, 64, 64, p, p, 1, 1, 64, 16, kd, kd, p, 1, 4, None, None)] == \
         "FDEC_ERR_INVALID_ARG"
     assert fd.STATUS_NAMES[lib.fdec_append(p, p, 64, 64, p, p, 0, 1, 64, 16, kd, kd, p, 1, 4, None, None)] == "FDEC_OK"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("layout,page_size", [("hnd", 16), ("interleaved", 64), ("nhd", 1)])
+def test_e4m3_append_matches_the_oracle_scatter_bit_for_bit(layout, page_size):
+    caps = [300, 1000, 64]
+    w = W.make(3, 1, 16, 4, 128, page_size, caps, dtype="bf16", kv_dtype="fp8", device="cuda", seed=page_size,
+               layout=layout)
+    lens = [250, 900, 10]
+    k16, v16, bi, pos = _new_tokens(w, lens, 40 if page_size > 1 else 7, seed=page_size + 1)
+    k_new, v_new = k16.float().to(torch.float8_e4m3fn), v16.float().to(torch.float8_e4m3fn)
+    cpu = w.to("cpu")
+    assert oracle.append_paged(k_new, v_new, bi, pos, cpu.k, cpu.v, cpu.page_table, page_size) == 0
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fd.fdec_append_e4m3(k_new.cuda(), v_new.cuda(), torch.as_tensor(bi, device="cuda"),
+                        torch.as_tensor(pos, device="cuda"), w.k, w.v, torch.as_tensor(w.page_table, device="cuda"),
+                        page_size, device_errors=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for got, ref in zip(w.keep, cpu.keep):
+        assert torch.equal(got.reshape(-1).cpu().view(torch.uint8), ref.reshape(-1).view(torch.uint8))
+
+
+@pytest.mark.gpu
+def test_e4m3_append_then_decode_matches_the_oracle():
+    caps = [700, 2100, 129]
+    w = W.make(3, 1, 32, 8, 128, 16, caps, dtype="bf16", kv_dtype="fp8", device="cuda", seed=9, peaked=True)
+    lens = [600, 2000, 100]
+    k16, v16, bi, pos = _new_tokens(w, lens, 29, seed=9)
+    k_new, v_new = k16.float().to(torch.float8_e4m3fn), v16.float().to(torch.float8_e4m3fn)
+    table = torch.as_tensor(w.page_table, device="cuda")
+    fd.fdec_append_e4m3(k_new.cuda(), v_new.cuda(), torch.as_tensor(bi, device="cuda"),
+                        torch.as_tensor(pos, device="cuda"), w.k, w.v, table, 16)
+    new_lens = np.array(lens, dtype=np.int32) + 29
+    pd = fd.PagedDecode(caps, 1, 16, 32, 8, 128, "bf16", device="cuda", kv_dtype="fp8")
+    out = torch.empty(3, 1, 32, 128, device="cuda")
+    lse = torch.empty(3, 1, 32, device="cuda")
+    pd.run(w.q, w.k, w.v, table, torch.as_tensor(new_lens, device="cuda"), out, lse, scale=w.scale,
+           k_scale=0.7, v_scale=1.3)
+    torch.cuda.synchronize()
+    assert pd.device_errors() == 0
+    ro, rl = oracle_run(w.to("cpu"), seq_lens=new_lens, k_scale=0.7, v_scale=1.3)
+    assert_parity(out.cpu(), lse.cpu(), ro, rl, "e4m3 append then decode")
+
+
+def test_e4m3_append_checks_byte_strides_and_element_sizes():
+    lib = fd._load()
+    p = 0x200000
+    good = fd.KVDesc(0x100000, 4, 4 * 16 * 128, 16 * 128, 128)
+    # 8-element strides are 16 bytes of a 16-bit cache but 8 bytes of codes
+    assert fd.STATUS_NAMES[lib.fdec_append_e4m3(p, p, 128, 8, p, p, 1, 1, 128, 16, good, good, p, 1, 4, None,
+                                                None)] == "FDEC_ERR_LAYOUT"
+    bad = fd.KVDesc(0x100000, 4, 4 * 16 * 128, 16 * 128, 136)
+    assert fd.STATUS_NAMES[lib.fdec_append_e4m3(p, p, 128, 128, p, p, 1, 1, 128, 16, good, bad, p, 1, 4, None,
+                                                None)] == "FDEC_ERR_LAYOUT"
+    odd16 = fd.KVDesc(0x100000, 4, 4 * 16 * 128, 16 * 128, 132)  # 132 x 2 bytes is not a multiple of 16
+    assert fd.STATUS_NAMES[lib.fdec_append(p, p, 128, 8, p, p, 1, 1, 128, 16, good, odd16, p, 1, 4, None,
+                                           None)] == "FDEC_ERR_LAYOUT"
+    k16 = torch.zeros(2, 1, 128, dtype=torch.bfloat16)
+    pool8 = torch.zeros(4, 1, 16, 128, dtype=torch.float8_e4m3fn)
+    idx = torch.zeros(2, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        fd.fdec_append_e4m3(k16, k16, idx, idx, pool8, pool8, torch.zeros(1, 4, dtype=torch.int32), 16)
+    with pytest.raises(ValueError):
+        fd.fdec_append(k16, k16, idx, idx, pool8, pool8, torch.zeros(1, 4, dtype=torch.int32), 16)

@@ -89,3 +89,34 @@ def test_captured_decode_loop_with_growing_lengths_equals_eager():
             ro, rl = oracle_run(w_cpu, seq_lens=cur)
             assert_parity(out.cpu(), lse.cpu(), ro, rl, f"graph step {step}")
     assert pd.device_errors() == 0
+
+
+def test_first_call_with_an_e4m3_cache_and_scales_is_captured():
+    """The pages' capture failure came from a lazily allocated unit-scale tensor for
+    fp8 caches; here the scales are launch arguments, so the very first scaled call
+    over an E4M3 cache captures and replays exactly."""
+    code = textwrap.dedent("""
+        import torch
+        import paged_split_kv_gather_gb300 as fd
+        from paged_split_kv_gather_gb300 import workloads as W
+        w = W.long_context(3000, device="cuda", kv_dtype="fp8")
+        table = torch.as_tensor(w.page_table, device="cuda")
+        lens = torch.as_tensor(w.seq_lens, device="cuda")
+        out = torch.zeros(1, 1, 32, 128, device="cuda"); lse = torch.zeros(1, 1, 32, device="cuda")
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            pd = fd.PagedDecode(w.seq_lens, 1, 64, 32, 4, 128, "bf16", stream=s, kv_dtype="fp8")
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale, stream=s, k_scale=0.5, v_scale=3.0)
+        torch.cuda.synchronize()
+        assert torch.all(out == 0)
+        g.replay(); torch.cuda.synchronize()
+        ref = torch.empty_like(out); rl = torch.empty_like(lse)
+        pd.run(w.q, w.k, w.v, table, lens, ref, rl, scale=w.scale, k_scale=0.5, v_scale=3.0)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref) and torch.equal(lse, rl)
+        print("CAPTURED_E4M3_OK")
+    """)
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert "CAPTURED_E4M3_OK" in r.stdout, r.stdout + r.stderr
