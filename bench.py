@@ -249,7 +249,7 @@ def _config_points(dev, calls, hbm_peak):
 
     flush = L2Flush(torch, dev)
 
-    def runner(w, capacities=None, run_kw=None, **plan_opts):
+    def runner(w, capacities=None, **plan_opts):
         caps = w.seq_lens if capacities is None else capacities
         if w.kv_dtype:
             plan_opts.setdefault("kv_dtype", w.kv_dtype)
@@ -261,7 +261,7 @@ def _config_points(dev, calls, hbm_peak):
         lse = torch.empty((w.batch, w.q_len, w.num_qo_heads), device=dev)
 
         def run():
-            pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale, **(run_kw or {}))
+            pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale)
 
         for _ in range(3):
             run()

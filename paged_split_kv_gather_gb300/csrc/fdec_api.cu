@@ -375,10 +375,11 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
     p->dtype = dtype;
     p->kv8 = kv8;
     p->causal = (causal != 0 && q_len > 1) ? 1 : 0;
-    // Tensor cores by default where the kernel exists (see split_mma_kernel.cuh for
-    // why); the fp32 SIMT kernel on request and for head_dim 256 / 512.
-    // The tcgen05 kernel once the rows need more than one 16-row group of the
-    // warp-level kernel (which would stream K/V once per group).
+    // The warp-level tensor-core kernel by default (every head_dim; see
+    // split_mma_kernel.cuh for why tensor cores pay off even when bandwidth-bound);
+    // the tcgen05 kernel once the rows need more than one 16-row group (the 16-row
+    // kernel would stream K/V once per group); E4M3 caches always on the former;
+    // the fp32 SIMT kernel only on request.
     if (kv8)
         p->path = FDEC_PATH_MMA;
     else if (o.path == FDEC_PATH_AUTO)
