@@ -272,9 +272,9 @@ __device__ __forceinline__ bool wait_stage(uint64_t* full, int i) {
 // A partial (last) stage: rows past the sequence end hold whatever the page
 // held; zero its V rows [nv, TOK) so that a fixed-size p.V loop adds 0 * 0.
 // `threads` consecutive threads (from `tid` 0) share the work.
-template <int D, int TOK = kStageTokens>
+template <int D, int TOK = kStageTokens, int EB = 2>
 __device__ __forceinline__ void zero_v_tail(uint8_t* stage, int nv, int tid = threadIdx.x & 31, int threads = 32) {
-    using G = StageGeom<D, TOK>;
+    using G = StageGeom<D, TOK, EB>;
     uint8_t* vrows = stage + G::HALF_BYTES;
     for (int idx = tid; idx < (TOK - nv) * G::REGIONS * 8; idx += threads) {
         const int row = nv + idx / (G::REGIONS * 8);

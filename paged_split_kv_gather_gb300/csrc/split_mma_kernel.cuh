@@ -28,15 +28,24 @@
 // (the K and V reads and the TMA writes).
 //
 // Quantised caches (KV8: K and V stored as 8-bit E4M3 codes, head_dim 128 and
-// 256): the producer stages the codes (half the bytes of a 16-bit cache), and
-// the consumer warp that takes a stage first converts it into its own f16 tile
-// in the same swizzled layout (one hardware conversion per pair of codes; every
-// E4M3 value is exact in f16), releases the stage to the producer, and runs the
-// unchanged contractions on the tile in f16.  A bf16 query is brought to f16 by
-// scaling each query row by a power of two that puts its largest magnitude in
-// f16's top binade [2^14, 2^15): exact for every element within 2^38 of the row's
-// largest, and the factor is taken back out of the row's logit scale.  The
-// cache's k_scale is folded into the logit scale and v_scale into the epilogue.
+// 256): the producer stages the codes (half the bytes of a 16-bit cache) and the
+// consumers build f16 MMA fragments straight from them (every E4M3 value is
+// exact in f16; one hardware conversion per pair of codes):
+//   K: ldmatrix on the code rows hands lane l four consecutive codes of token
+//      l / 4 (dims 16c + 4 (l % 4) .. + 3 of chunk c).  The k order inside each
+//      16-dim step is permuted so that these are exactly the lane's B fragment
+//      (k slots 2t, 2t+1 <- dims 4t, 4t+1 and 2t+8, 2t+9 <- 4t+2, 4t+3), and Q's A
+//      fragments are read from shared memory in the same order.  A dot product
+//      does not depend on the order of its terms.
+//   V: ldmatrix.trans on the code rows hands lane l the codes of tokens 2t, 2t+1
+//      for dims 2g, 2g+1 (g = l / 4); one byte permutation pairs them by dim, so
+//      each register yields the B fragments of two n-tiles: the even dims and the
+//      odd dims of a 16-dim chunk.  The epilogue puts O's columns back in order.
+// A bf16 query is brought to f16 by scaling each query row by a power of two
+// that puts its largest magnitude in f16's top binade [2^14, 2^15): exact for
+// every element within 2^38 of the row's largest, and the factor is taken back
+// out of the row's logit scale.  P is one f16 value scaled by 2^7.  The cache's
+// k_scale is folded into the logit scale and v_scale into the epilogue.
 #pragma once
 
 #include <type_traits>
@@ -60,9 +69,7 @@ struct MmaLayout {
     // memory and four warps (3 consumers + the producer), 255 registers each.
     // head_dim 256 fits three stages and two consumers per CTA; head_dim 512
     // runs one CTA per SM (stages of 64 KB).
-    // E4M3 caches: each consumer group also owns a 16-bit tile (16 KB at head_dim
-    // 128, which still fits two CTAs per SM; 32 KB at 256, one CTA).
-    static constexpr int CTAS_PER_SM = KV8 ? (D <= 128 ? 2 : 1) : (D <= 256 ? 2 : 1);
+    static constexpr int CTAS_PER_SM = (KV8 && D <= 128) ? 3 : (D <= 256 ? 2 : 1);
     // head_dim 512: the O accumulators of all 512 columns would need 256
     // registers, so two consumer warps share each stage, both computing S and
     // each accumulating P V for one half of the columns (DH).
@@ -74,8 +81,7 @@ struct MmaLayout {
     static constexpr bool Q_IN_REGS = D <= 192;
     static constexpr int BUDGET = 232448 / CTAS_PER_SM - 1024;
     static constexpr int NP_MAX = 3;
-    static constexpr int TILE_BYTES = KV8 ? NP_MAX * G::STAGE_BYTES : 0;  // after the stage ring
-    static constexpr int FIXED = BAR_BYTES + Q_BYTES + ALIGN_SLACK + TILE_BYTES;
+    static constexpr int FIXED = BAR_BYTES + Q_BYTES + ALIGN_SLACK;
     static constexpr int S_FIT = (BUDGET - FIXED) / GS::STAGE_BYTES;
     static constexpr int S = S_FIT > 16 ? 16 : S_FIT;
     static constexpr int NP = (S - 1) < NP_MAX ? (S - 1) : NP_MAX;  // consumer groups (stages in flight at once)
@@ -83,10 +89,10 @@ struct MmaLayout {
     static constexpr int THREADS = (NW + 1) * 32;
     static constexpr int SMEM = FIXED + S * GS::STAGE_BYTES;
     static_assert(S >= NP + 1, "stage ring too small");
-    static_assert(!KV8 || (DSPLIT == 1 && NP == NP_MAX), "E4M3 caches: one warp per stage, a tile per group");
-    static_assert(!KV8 || 3 * S * 8 <= 256, "E4M3 caches keep the query row maxima at byte 256 of the barrier area");
-    static_assert(3 * S * 8 <= BAR_BYTES, "barrier area too small");
-    static_assert(NP * RC * (D + 2) * 4 <= S * GS::STAGE_BYTES + TILE_BYTES, "merge scratch must fit the stage area");
+    static_assert(!KV8 || DSPLIT == 1, "E4M3 caches: one warp per stage");
+    static constexpr int QMAX_OFFSET = BAR_BYTES - RC * 4;  // E4M3 caches: query row maxima
+    static_assert(3 * S * 8 <= QMAX_OFFSET, "barrier area too small");
+    static_assert(NP * RC * (D + 2) * 4 <= S * GS::STAGE_BYTES, "merge scratch must fit the stage area");
 };
 
 // Four E4M3 codes (w's bytes, lowest first) -> two packed f16 pairs (exact; the
@@ -96,58 +102,6 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& p01, uint32_
         "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
         : "=r"(p01), "=r"(p23)
         : "r"(w));
-}
-
-// One warp converts a staged E4M3 stage (K then V; D/128 regions of [32 rows][128 B]
-// each, chunk c of row r at c ^ (r & 7)) into an f16 tile of the layout the
-// consumers read (D/64 regions).  A code chunk holds dims 16c .. 16c+15 of its
-// region, i.e. 16-bit chunks 2c and 2c+1 of region 2 r8 + c / 4.  Shared memory
-// serves 16-byte accesses eight lanes at a time, so each group of eight lanes
-// takes two adjacent rows (one even, one odd) and complementary halves of their
-// chunks: its eight loads and each of its two sets of eight stores then fall on
-// eight different 16-byte bank groups (no conflict).  Lane l handles chunk
-// c8 = (l & 3) + 4 ((l >> 2 ^ l >> 3) & 1) of rows 2 (l >> 4) + ((l >> 2) & 1) + 4 k,
-// k = 0 .. 7, of every region of K and V; its swizzle offsets depend on k only
-// through k & 1.
-template <int D>
-__device__ __forceinline__ void convert_stage_e4m3(const uint8_t* src, uint8_t* dst, int lane) {
-    using G = StageGeom<D>;
-    using G8 = StageGeom<D, kStageTokens, 1>;
-    static_assert(kStageTokens == 32, "eight rows of four per lane group below");
-    const int odd = (lane >> 2) & 1;
-    const int c8 = (lane & 3) + 4 * (odd ^ ((lane >> 3) & 1));
-    const int row0 = 2 * (lane >> 4) + odd;  // rows row0 + 4 k
-    const int c16 = (c8 & 3) * 2;
-    uint32_t s_off[2], d_lo[2], d_hi[2];  // by k & 1: (row0 + 4 k) & 7 = (row0 & 7) ^ (4 (k & 1))
-#pragma unroll
-    for (int par = 0; par < 2; ++par) {
-        const int r7 = (row0 + 4 * par) & 7;
-        s_off[par] = static_cast<uint32_t>(row0 * 128 + ((c8 ^ r7) << 4));
-        d_lo[par] = static_cast<uint32_t>((c8 >> 2) * G::REGION_BYTES + row0 * 128 + ((c16 ^ r7) << 4));
-        d_hi[par] = static_cast<uint32_t>((c8 >> 2) * G::REGION_BYTES + row0 * 128 + (((c16 + 1) ^ r7) << 4));
-    }
-#pragma unroll 1
-    for (int hv = 0; hv < 2; ++hv) {        // K, then V
-#pragma unroll
-        for (int r8 = 0; r8 < G8::REGIONS; ++r8) {
-            const uint8_t* sreg = src + hv * G8::HALF_BYTES + r8 * G8::REGION_BYTES;
-            uint8_t* dreg = dst + hv * G::HALF_BYTES + 2 * r8 * G::REGION_BYTES;
-            uint4 x[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                x[k] = *reinterpret_cast<const uint4*>(sreg + s_off[k & 1] + k * 512);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                uint4 lo, hi;
-                e4m3x4_to_f16(x[k].x, lo.x, lo.y);
-                e4m3x4_to_f16(x[k].y, lo.z, lo.w);
-                e4m3x4_to_f16(x[k].z, hi.x, hi.y);
-                e4m3x4_to_f16(x[k].w, hi.z, hi.w);
-                *reinterpret_cast<uint4*>(dreg + d_lo[k & 1] + k * 512) = lo;
-                *reinterpret_cast<uint4*>(dreg + d_hi[k & 1] + k * 512) = hi;
-            }
-        }
-    }
 }
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -245,7 +199,6 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
         const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
         stages = smem + Lay::BAR_BYTES + Lay::Q_BYTES + pad;
     }
-    uint8_t* tiles = stages + S * GS::STAGE_BYTES;  // KV8: one 16-bit tile per consumer group
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -270,7 +223,7 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
     if (threadIdx.x == 0) report_item_range(p, ir);
     // The group's query rows, as stored (16-bit, [RC][D]); rows past the group are zero.
     // QSCALE: bf16 rows -> f16 rows times 2^sh(row), sh from the row's largest magnitude.
-    uint32_t* q_rmax = reinterpret_cast<uint32_t*>(smem + 256);  // [RC] largest |q| (bf16 bits)
+    uint32_t* q_rmax = reinterpret_cast<uint32_t*>(smem + Lay::QMAX_OFFSET);  // [RC] largest |q| (bf16 bits)
     {
         QChunks<RC, D, NW * 32> qc;
         qc.load(p, b, kvh, row0, threadIdx.x);
@@ -323,12 +276,34 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
     constexpr int QREGS = Lay::Q_IN_REGS ? KSTEPS : 1;
     uint32_t qa[QREGS][4];
     const uint32_t q_lane = smem_addr(q_s) + ((mi & 1) * 8 + (lane & 7)) * (D * 2) + (mi >> 1) * 16;
+    // KV8: A fragments in the permuted k order of the code fragments (dims 16 kk + 4 tq .. + 3
+    // of rows g and g + 8: k slots 2tq, 2tq+1 and 2tq+8, 2tq+9).
+    auto load_q8 = [&](int kk, uint32_t(&a)[4]) {
+        const uint2 r0 = *reinterpret_cast<const uint2*>(q_s + g * D + 16 * kk + 4 * tq);
+        const uint2 r1 = *reinterpret_cast<const uint2*>(q_s + (g + 8) * D + 16 * kk + 4 * tq);
+        a[0] = r0.x;
+        a[1] = r1.x;
+        a[2] = r0.y;
+        a[3] = r1.y;
+    };
     if constexpr (Lay::Q_IN_REGS) {
         static_for<0, KSTEPS>([&](auto kk_) {
             constexpr int kk = decltype(kk_)::value;
-            ldmatrix_x4(q_lane + 2 * kk * 16, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+            if constexpr (KV8)
+                load_q8(kk, qa[kk]);
+            else
+                ldmatrix_x4(q_lane + 2 * kk * 16, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
         });
     }
+    // KV8 ldmatrix addresses in a code stage (32 token rows of D/128 regions of 128 bytes;
+    // chunk c of row r at c ^ (r & 7)).  K: lane l addresses token l (matrix = n-tile l / 8).
+    // V: lane l addresses token 16 k2 + 8 ((l >> 3) & 1) + (l & 7) of chunk c + (l >> 4).
+    const uint32_t k8_row = static_cast<uint32_t>(lane * 128);
+    const uint32_t k8_x = static_cast<uint32_t>((lane & 7) << 4);
+    uint32_t v8_row[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) v8_row[j] = static_cast<uint32_t>((16 * j + 8 * ((lane >> 3) & 1) + (lane & 7)) * 128);
+    const uint32_t v8_x = static_cast<uint32_t>((((lane >> 4) & 1) ^ (lane & 7)) << 4);
     // ldmatrix row addresses within a stage (swizzled: chunk c of row r at c ^ (r & 7)).
     uint32_t kb_row[2], kb_x[4], vb_row[2], vb_x[4];
 #pragma unroll
@@ -372,19 +347,10 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
         }
         const int t0 = ir.tok_begin + i * kStageTokens;
         const int nv = min(kStageTokens, ir.tok_end - t0);
-        uint8_t* tile;
-        if constexpr (KV8) {
-            // codes -> this group's 16-bit tile; the stage goes back to the producer at once
-            tile = tiles + grp * G::STAGE_BYTES;
-            convert_stage_e4m3<D>(stages + s * GS::STAGE_BYTES, tile, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
-        } else {
-            tile = stages + s * G::STAGE_BYTES;
-        }
-        const uint32_t kbase = smem_addr(tile);
-        const uint32_t vbase = kbase + G::HALF_BYTES;
-        if (nv < kStageTokens) zero_v_tail<D>(tile, nv);
+        uint8_t* stage = stages + s * GS::STAGE_BYTES;
+        const uint32_t kbase = smem_addr(stage);
+        const uint32_t vbase = kbase + GS::HALF_BYTES;
+        if (nv < kStageTokens) zero_v_tail<D, kStageTokens, KV8 ? 1 : 2>(stage, nv);
 
         // S = Q K^T for the stage's 32 tokens (4 n-tiles of 8)
         float sc[4][4];
@@ -393,13 +359,27 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
         static_for<0, KSTEPS>([&](auto kk_) {
             constexpr int kk = decltype(kk_)::value;
             constexpr int qk = Lay::Q_IN_REGS ? kk : 0;
-            if constexpr (!Lay::Q_IN_REGS) ldmatrix_x4(q_lane + 2 * kk * 16, qa[0][0], qa[0][1], qa[0][2], qa[0][3]);
+            if constexpr (KV8) {
+                if constexpr (!Lay::Q_IN_REGS) load_q8(kk, qa[0]);
+                uint32_t r[4];
+                ldmatrix_x4(kbase + (kk >> 3) * GS::REGION_BYTES + k8_row + ((static_cast<uint32_t>(kk & 7) << 4) ^ k8_x),
+                            r[0], r[1], r[2], r[3]);
 #pragma unroll
-            for (int pr = 0; pr < 2; ++pr) {
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4(kbase + (kk >> 2) * G::REGION_BYTES + kb_row[pr] + kb_x[kk & 3], b0, b1, b2, b3);
-                mma_16816<MB>(sc[2 * pr], qa[qk], b0, b1);
-                mma_16816<MB>(sc[2 * pr + 1], qa[qk], b2, b3);
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t b0, b1;
+                    e4m3x4_to_f16(r[j], b0, b1);
+                    mma_16816<false>(sc[j], qa[qk], b0, b1);
+                }
+            } else {
+                if constexpr (!Lay::Q_IN_REGS)
+                    ldmatrix_x4(q_lane + 2 * kk * 16, qa[0][0], qa[0][1], qa[0][2], qa[0][3]);
+#pragma unroll
+                for (int pr = 0; pr < 2; ++pr) {
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4(kbase + (kk >> 2) * G::REGION_BYTES + kb_row[pr] + kb_x[kk & 3], b0, b1, b2, b3);
+                    mma_16816<MB>(sc[2 * pr], qa[qk], b0, b1);
+                    mma_16816<MB>(sc[2 * pr + 1], qa[qk], b2, b3);
+                }
             }
         });
 
@@ -474,24 +454,38 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
         // O += P V
 #pragma unroll
         for (int k2 = 0; k2 < 2; ++k2) {
-            static_for<0, DH / 16>([&](auto jp_) {
-                constexpr int jp = decltype(jp_)::value;  // 16-column group of this warp's half
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4_trans(vbase + v_half + (jp >> 2) * G::REGION_BYTES + vb_row[k2] + vb_x[jp & 3], b0, b1, b2,
-                                  b3);
-                mma_16816<MB>(o[2 * jp], ph[k2], b0, b1);
-                if constexpr (!P1) mma_16816<MB>(o[2 * jp], pl[k2], b0, b1);
-                mma_16816<MB>(o[2 * jp + 1], ph[k2], b2, b3);
-                if constexpr (!P1) mma_16816<MB>(o[2 * jp + 1], pl[k2], b2, b3);
-            });
+            if constexpr (KV8) {
+                // chunks c, c + 1 (16 dims each): o[2c] / o[2c+1] hold the even / odd dims of chunk c
+                static_for<0, D / 32>([&](auto cp_) {
+                    constexpr int c = 2 * decltype(cp_)::value;
+                    uint32_t r[4];
+                    ldmatrix_x4_trans(vbase + (c >> 3) * GS::REGION_BYTES + v8_row[k2] +
+                                          ((static_cast<uint32_t>(c & 7) << 4) ^ v8_x),
+                                      r[0], r[1], r[2], r[3]);
+                    uint32_t ev[4], od[4];  // by matrix: (tokens 0-7 | 8-15) x (chunk c | c + 1)
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) e4m3x4_to_f16(__byte_perm(r[m], 0u, 0x3120u), ev[m], od[m]);
+                    mma_16816<false>(o[2 * c], ph[k2], ev[0], ev[1]);
+                    mma_16816<false>(o[2 * c + 1], ph[k2], od[0], od[1]);
+                    mma_16816<false>(o[2 * c + 2], ph[k2], ev[2], ev[3]);
+                    mma_16816<false>(o[2 * c + 3], ph[k2], od[2], od[3]);
+                });
+            } else {
+                static_for<0, DH / 16>([&](auto jp_) {
+                    constexpr int jp = decltype(jp_)::value;  // 16-column group of this warp's half
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4_trans(vbase + v_half + (jp >> 2) * G::REGION_BYTES + vb_row[k2] + vb_x[jp & 3], b0, b1,
+                                      b2, b3);
+                    mma_16816<MB>(o[2 * jp], ph[k2], b0, b1);
+                    if constexpr (!P1) mma_16816<MB>(o[2 * jp], pl[k2], b0, b1);
+                    mma_16816<MB>(o[2 * jp + 1], ph[k2], b2, b3);
+                    if constexpr (!P1) mma_16816<MB>(o[2 * jp + 1], pl[k2], b2, b3);
+                });
+            }
         }
-        if constexpr (KV8) {
-            __syncwarp();  // every lane's reads of the tile precede its next conversion
-        } else {
-            if (nv < kStageTokens) fence_proxy_async_shared();  // generic zeroing before the slot's next TMA write
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
-        }
+        if (nv < kStageTokens) fence_proxy_async_shared();  // generic zeroing before the slot's next TMA write
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -513,8 +507,19 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
         sm_l[grp * RC + g] = lrow[0];
         sm_l[grp * RC + g + 8] = lrow[1];
     }
+    if constexpr (KV8) {
+        // o[2c] / o[2c+1]: dims 16c + 2n / 16c + 2n + 1 of column n: this lane's columns 2tq, 2tq+1
+        // are dims 16c + 4tq + {0, 2} / {1, 3}
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
+        for (int c = 0; c < D / 16; ++c) {
+            *reinterpret_cast<float4*>(sm_o + (grp * RC + g) * D + 16 * c + 4 * tq) =
+                make_float4(o[2 * c][0] * o_out, o[2 * c + 1][0] * o_out, o[2 * c][1] * o_out, o[2 * c + 1][1] * o_out);
+            *reinterpret_cast<float4*>(sm_o + (grp * RC + g + 8) * D + 16 * c + 4 * tq) =
+                make_float4(o[2 * c][2] * o_out, o[2 * c + 1][2] * o_out, o[2 * c][3] * o_out, o[2 * c + 1][3] * o_out);
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < (KV8 ? 0 : NT); ++n) {
         *reinterpret_cast<float2*>(sm_o + (grp * RC + g) * D + half * DH + 8 * n + 2 * tq) =
             make_float2(o[n][0] * o_out, o[n][1] * o_out);
         *reinterpret_cast<float2*>(sm_o + (grp * RC + g + 8) * D + half * DH + 8 * n + 2 * tq) =
