@@ -9,6 +9,7 @@
 // are read once and written once.  (Measured: four chunks per thread with all
 // loads issued first, on an uncapped grid, was slower: 59.4 against 57.3 us for
 // 268 MB, 9.2 against 6.1 us for one token per sequence.)
+#include <atomic>
 #include <cstdint>
 
 #include "../../include/fdec.h"
@@ -53,15 +54,15 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendParams p) 
 }
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
-    static int sms[64] = {0};  // SM count per device, queried once
+    static std::atomic<int> sms[64];  // SM count per device, queried once (0 = not yet)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int n_sms = dev < 64 ? sms[dev] : 0;
+    int n_sms = dev >= 0 && dev < 64 ? sms[dev].load(std::memory_order_relaxed) : 0;
     if (n_sms == 0) {
         e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        if (dev < 64) sms[dev] = n_sms;
+        if (dev >= 0 && dev < 64) sms[dev].store(n_sms, std::memory_order_relaxed);
     }
     const int64_t total = 2LL * p.n_tokens * p.hk * (p.row_bytes / 16);
     if (total == 0) return cudaSuccess;
