@@ -77,7 +77,7 @@ def test_forced_one_block_per_split_uses_two_reduction_passes():
     p = _plan([262144], num_qo_heads=32, num_kv_heads=4, page_size=64, blocks_per_split=1)
     info = fd.fdec_plan_get_info(p)
     assert info["max_splits"] == 4096
-    assert info["reduce_passes"] == 2          # 4096 -> 64 -> 1 with fan-in 64
+    assert info["reduce_passes"] == 2          # 4096 -> 16 -> 1 with the default fan-in 256
     assert info["launches"] == 3
     p = _plan([262144], num_qo_heads=32, num_kv_heads=4, page_size=64, blocks_per_split=1, reducer_fanin=4)
     assert fd.fdec_plan_get_info(p)["reduce_passes"] == 6   # 4096 = 4^6
@@ -289,3 +289,45 @@ def test_binding_refuses_k_v_of_the_wrong_element_size():
     with pytest.raises(ValueError):
         fd.fdec_run(plan16, q, k8, k8, torch.zeros(1, 4, dtype=torch.int32), torch.zeros(1, dtype=torch.int32),
                     out, None, torch.zeros(256, dtype=torch.uint8))
+
+
+def test_plan_invariants_hold_for_random_batches():
+    """Property check of the planner over random batches: split counts follow the
+    chosen blocks per split, items and CTAs cover every (split, KV head, row group),
+    the reduction has exactly the passes a fan-in F tree needs, the path choice
+    follows the row count, and the workspace holds every partial."""
+    hypothesis = pytest.importorskip("hypothesis")
+    st = hypothesis.strategies
+
+    @hypothesis.settings(max_examples=60, deadline=None, derandomize=True)
+    @hypothesis.given(lens=st.lists(st.integers(0, 100000), min_size=1, max_size=12), q_len=st.integers(1, 12),
+                      group=st.sampled_from([1, 2, 4, 8]), hk=st.sampled_from([1, 2, 8]),
+                      d=st.sampled_from([64, 128, 192, 256, 512]), bps=st.integers(0, 40),
+                      fanin=st.sampled_from([0, 2, 3, 16]), kv8=st.booleans())
+    def check(lens, q_len, group, hk, d, bps, fanin, kv8):
+        if kv8 and d not in (128, 256):
+            d = 128
+        p = _plan(lens, q_len=q_len, num_qo_heads=hk * group, num_kv_heads=hk, head_dim=d, blocks_per_split=bps,
+                  reducer_fanin=fanin, kv_dtype="fp8" if kv8 else "", causal=q_len > 1)
+        info = fd.fdec_plan_get_info(p)
+        splits = fd.fdec_plan_get_splits(p).astype(np.int64)
+        C = info["blocks_per_split"]
+        if bps:
+            assert C == bps
+        nb = np.maximum(1, -(-np.asarray(lens, dtype=np.int64) // 64))
+        assert np.array_equal(splits, -(-nb // C))
+        assert info["num_items"] == int(splits.sum()) and info["max_splits"] == int(splits.max())
+        rows = q_len * group
+        want_path = fd.FDEC_PATH_TC if (not kv8 and d == 128 and rows > 16) else fd.FDEC_PATH_MMA
+        assert info["path"] == want_path
+        assert info["row_groups"] == -(-rows // info["rows_per_group"])
+        assert info["num_split_ctas"] == info["num_items"] * hk * info["row_groups"]
+        F = fanin or 256
+        n, passes = int(splits.max()), 0
+        while n > 1:
+            n, passes = -(-n // F), passes + 1
+        assert info["reduce_passes"] == passes and info["launches"] == 1 + passes
+        partial_rows = int(splits[splits > 1].sum()) * hk * rows
+        assert info["workspace_bytes"] >= partial_rows * (4 * d + 8)
+
+    check()
