@@ -30,6 +30,11 @@
  *   - Element strides are in elements of the storage type (16-bit, or one
  *     byte for E4M3 caches); the innermost (head_dim) stride is always 1.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).
+ *   - A plan is not thread-safe: fdec_run caches the tensor maps of the last
+ *     K/V descriptors in the plan, so calls on one plan from several host threads
+ *     must be serialised by the caller (calls on different plans need not be).
+ *     Calls on one plan and workspace from one thread may go to any streams only
+ *     if the caller orders them (they share the workspace's partials).
  */
 #ifndef FDEC_H
 #define FDEC_H

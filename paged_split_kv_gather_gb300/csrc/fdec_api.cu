@@ -609,6 +609,7 @@ fdec_status fdec_run_scaled(fdec_plan_t p, const void* q, int64_t q_stride_tok, 
                             fdec_kv_desc k, fdec_kv_desc v, const int32_t* page_table, int64_t page_table_stride,
                             const int32_t* seq_lens_dev, float scale, float k_scale, float v_scale, float* out,
                             float* lse, void* workspace, cudaStream_t stream) {
+    g_last_error.clear();
     if (p == nullptr) return fail(FDEC_ERR_INVALID_ARG, "null plan");
     if (q == nullptr || k.base == nullptr || v.base == nullptr || page_table == nullptr || seq_lens_dev == nullptr ||
         out == nullptr)
