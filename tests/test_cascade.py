@@ -84,3 +84,42 @@ def test_cascade_matches_the_oracle_on_whole_sequences(hq, hk, d, dtype, suffix_
     assert int(info["path"]) == want_path
     ro, rl = _full_sequence_oracle(w, q, prefix_len, suffix_lens)
     assert_parity(out.cpu(), lse.cpu(), ro, rl, "cascade")
+
+
+def test_cascade_reading_holds_in_the_oracle():
+    """CPU pin of the cascade reading, oracle only: the prefix attended as the
+    non-causal query rows of one call, merged by log-sum-exp with each sequence's
+    own-suffix attention, equals attention over prefix + suffix (to 1e-12)."""
+    import oracle
+
+    prefix_len, suffix_lens = 192, [5, 0, 70]
+    hq, hk, d, P = 8, 2, 64, 16
+    s = len(suffix_lens)
+    w = W.make(s + 1, 1, hq, hk, d, P, [prefix_len, *suffix_lens], dtype="bf16", seed=3, peaked=True)
+    q = (torch.randn((s, 1, hq, d), generator=torch.Generator().manual_seed(4)) * 8).to(torch.bfloat16)
+    pre = dataclasses.replace(w, batch=1, q_len=s, q=q.view(1, s, hq, d), causal=False,
+                              page_table=w.page_table[0:1], seq_lens=np.array([prefix_len], dtype=np.int32))
+    suf = dataclasses.replace(w, batch=s, q_len=1, q=q, page_table=w.page_table[1:],
+                              seq_lens=np.array(suffix_lens, dtype=np.int32))
+    po, pl = oracle_run(pre)
+    so, sl = oracle_run(suf)
+    mo, ml = oracle.merge_states(np.stack([po.reshape(s * hq, d), so.reshape(s * hq, d)]),
+                                 np.stack([pl.reshape(-1), sl.reshape(-1)]))
+    ro, rl = _full_sequence_oracle_cpu(w, q, prefix_len, suffix_lens)
+    assert np.abs(mo - ro.reshape(s * hq, d)).max() < 1e-12
+    assert np.abs(ml - rl.reshape(-1)).max() < 1e-12
+
+
+def _full_sequence_oracle_cpu(w, q, prefix_len, suffix_lens):
+    P = w.page_size
+    s = len(suffix_lens)
+    npre = prefix_len // P
+    width = npre + max(1, -(-max(suffix_lens) // P))
+    table = np.full((s, width), -1, dtype=np.int32)
+    for b, L in enumerate(suffix_lens):
+        table[b, :npre] = w.page_table[0, :npre]
+        own = -(-L // P)
+        table[b, npre:npre + own] = w.page_table[1 + b, :own]
+    full = dataclasses.replace(w, batch=s, q_len=1, q=q, page_table=table,
+                               seq_lens=np.array([prefix_len + L for L in suffix_lens], dtype=np.int32))
+    return oracle_run(full)
