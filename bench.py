@@ -490,6 +490,10 @@ def _run_fdec(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
+    if world > 1:
+        # Several replicas: the headline step, its roofline and end-to-end numbers only.  The
+        # per-workload points characterise one GPU and would hold every GPU for another minute.
+        args.no_sweep = args.no_configs = args.no_dense = True
     if args.only_e4m3:
         # The quantised-cache long-context point alone (profiling the E4M3 kernel); not a bench line.
         peak, _ = _peaks()
