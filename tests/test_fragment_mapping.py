@@ -1,5 +1,7 @@
-"""CPU check of the lane-level data flow the E4M3 decode kernel uses to build f16
-MMA fragments straight from staged codes (split_mma_kernel.cuh, KV8 branches).
+"""CPU check of the lane-level data flow of the warp-level tensor-core decode
+kernel (split_mma_kernel.cuh): the E4M3 path, which builds f16 MMA fragments
+straight from staged codes (KV8 branches), and the 16-bit path's ldmatrix
+addressing of the query rows and the swizzled K/V stages.
 
 The kernel's address and permutation formulas are restated here and run through a
 model of the warp-level instructions, taken from their PTX definitions:
@@ -125,3 +127,79 @@ def test_code_fragments_reproduce_qk_and_pv(d):
             o[g, 16 * c + 4 * t:16 * c + 4 * t + 4] = [e[0], od_[0], e[1], od_[1]]
             o[g + 8, 16 * c + 4 * t:16 * c + 4 * t + 4] = [e[2], od_[2], e[3], od_[3]]
     assert np.allclose(o, p @ _dec(vc), rtol=1e-12, atol=1e-9)
+
+
+def _stage16(vals, d):
+    """[32][d] f16 values -> stage bytes: d/64 regions of [32 rows][128 B], 8-element chunk c at c ^ (r & 7)."""
+    raw = np.ascontiguousarray(vals.astype(np.float16)).view(np.uint8).reshape(32, 2 * d)
+    buf = np.zeros((d // 64) * 4096, dtype=np.uint8)
+    for r in range(32):
+        for c in range(d // 8):
+            off = (c >> 3) * 4096 + r * 128 + (((c & 7) ^ (r & 7)) << 4)
+            buf[off:off + 16] = raw[r, 16 * c:16 * c + 16]
+    return buf
+
+
+def _pairs16(w):  # 4 bytes -> the two f16 values (low half first)
+    v = np.frombuffer(np.ascontiguousarray(w).tobytes(), dtype=np.float16).astype(np.float64)
+    return (v[0], v[1])
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_16bit_fragments_reproduce_qk_and_pv(d):
+    """The same check for the 16-bit cache path: Q fragments by ldmatrix from the query
+    rows, K by ldmatrix and V by ldmatrix.trans from the swizzled stage."""
+    rng = np.random.default_rng(d + 1)
+    k = rng.standard_normal((32, d)).astype(np.float16).astype(np.float64)
+    v = rng.standard_normal((32, d)).astype(np.float16).astype(np.float64)
+    q = rng.standard_normal((16, d)).astype(np.float16).astype(np.float64)
+    p = rng.random((16, 32)).astype(np.float16).astype(np.float64)
+    kbuf, vbuf = _stage16(k, d), _stage16(v, d)
+    qbuf = np.ascontiguousarray(q.astype(np.float16)).view(np.uint8).reshape(-1)  # [16][d] rows, unswizzled
+    lanes = range(32)
+    mi = [lane >> 3 for lane in lanes]
+    q_lane = [((mi[lane] & 1) * 8 + (lane & 7)) * (d * 2) + (mi[lane] >> 1) * 16 for lane in lanes]
+    kb_row = [[(8 * (2 * j + (mi[lane] >> 1)) + (lane & 7)) * 128 for lane in lanes] for j in range(2)]
+    kb_x = [[((2 * j + (mi[lane] & 1)) ^ (lane & 7)) << 4 for lane in lanes] for j in range(4)]
+    vb_row = [[(16 * j + 8 * (mi[lane] & 1) + (lane & 7)) * 128 for lane in lanes] for j in range(2)]
+    vb_x = [[((2 * j + (mi[lane] >> 1)) ^ (lane & 7)) << 4 for lane in lanes] for j in range(4)]
+
+    s_acc = [[np.zeros(4) for _ in range(4)] for _ in range(32)]
+    for kk in range(d // 16):
+        qr = _ldmatrix_x4(qbuf, [q_lane[lane] + 2 * kk * 16 for lane in lanes], trans=False)
+        qa = [tuple(_pairs16(qr[lane][m]) for m in range(4)) for lane in lanes]
+        for pr in range(2):
+            kr = _ldmatrix_x4(kbuf, [(kk >> 2) * 4096 + kb_row[pr][lane] + kb_x[kk & 3][lane] for lane in lanes],
+                              trans=False)
+            for half, (m0, m1) in enumerate(((0, 1), (2, 3))):
+                acc = [s_acc[lane][2 * pr + half] for lane in lanes]
+                _mma(acc, qa, [_pairs16(kr[lane][m0]) for lane in lanes], [_pairs16(kr[lane][m1]) for lane in lanes])
+    s = np.zeros((16, 32))
+    for lane in lanes:
+        g, t = lane // 4, lane % 4
+        for n in range(4):
+            s[g, 8 * n + 2 * t:8 * n + 2 * t + 2] = s_acc[lane][n][:2]
+            s[g + 8, 8 * n + 2 * t:8 * n + 2 * t + 2] = s_acc[lane][n][2:]
+    assert np.allclose(s, q @ k.T, rtol=1e-12, atol=1e-9)
+
+    o_acc = [[np.zeros(4) for _ in range(d // 8)] for _ in range(32)]
+    for k2 in range(2):
+        pa = []
+        for lane in lanes:
+            g, t = lane // 4, lane % 4
+            b = 16 * k2
+            pa.append(((p[g, b + 2 * t], p[g, b + 2 * t + 1]), (p[g + 8, b + 2 * t], p[g + 8, b + 2 * t + 1]),
+                       (p[g, b + 8 + 2 * t], p[g, b + 9 + 2 * t]), (p[g + 8, b + 8 + 2 * t], p[g + 8, b + 9 + 2 * t])))
+        for jp in range(d // 16):
+            vr = _ldmatrix_x4(vbuf, [(jp >> 2) * 4096 + vb_row[k2][lane] + vb_x[jp & 3][lane] for lane in lanes],
+                              trans=True)
+            for half, (m0, m1) in enumerate(((0, 1), (2, 3))):
+                acc = [o_acc[lane][2 * jp + half] for lane in lanes]
+                _mma(acc, pa, [_pairs16(vr[lane][m0]) for lane in lanes], [_pairs16(vr[lane][m1]) for lane in lanes])
+    o = np.zeros((16, d))
+    for lane in lanes:
+        g, t = lane // 4, lane % 4
+        for n in range(d // 8):
+            o[g, 8 * n + 2 * t:8 * n + 2 * t + 2] = o_acc[lane][n][:2]
+            o[g + 8, 8 * n + 2 * t:8 * n + 2 * t + 2] = o_acc[lane][n][2:]
+    assert np.allclose(o, p @ v, rtol=1e-12, atol=1e-9)
