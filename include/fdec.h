@@ -292,15 +292,21 @@ fdec_status fdec_read_device_errors(fdec_plan_t plan, void* workspace, uint32_t*
  * cannot allocate device memory at all, e.g. a plug-in inside a program whose
  * memory pool owns the whole device, or a loop that must never call
  * cudaMalloc because it may synchronise the device.  Inputs and outputs are
- * as for fdec_run; the partials and work lists live in a 16 MiB array built
- * into the library, which every GPU that loads the library keeps until the
- * process exits.  A plan whose workspace_bytes exceeds 16 MiB is rejected
- * with FDEC_ERR_WORKSPACE (use fdec_run with your own workspace).
+ * as for fdec_run, and so is the result: the cache is read unscaled
+ * (k_scale = v_scale = 1), as fdec_run reads it; scaled caches go through
+ * fdec_run_scaled with a workspace.  The partials and work lists live in a
+ * 16 MiB array built into the library, which every GPU that loads the library
+ * keeps until the process exits.  A plan whose workspace_bytes exceeds 16 MiB
+ * is rejected with FDEC_ERR_WORKSPACE (use fdec_run with your own workspace).
  *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *   - Each call copies the plan's work lists into the array on `stream`
- *     (this also clears the device error word); the plan needs no upload.
- *   - The first call on a device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ *   - The plan needs no fdec_plan_upload: every call copies the plan's work
+ *     lists (host memory) into the array with cudaMemcpyAsync on `stream`,
+ *     which also clears the device error word, then launches the kernels.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current and keeps it for the
+ *     process; make that first call before any stream capture begins.  The
+ *     address belongs to the device's primary context: do not call this entry
+ *     point again on a device after cudaDeviceReset of that device.
  *   - All calls share the one array: calls that overlap on the GPU (other
  *     streams, other threads) race and corrupt each other's results.
  *   - Device error bits land in the array and are not reported; use fdec_run

@@ -18,6 +18,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfdec.so")
+# Benchmark helper (end-to-end steps timed from C), linked against LIB; not part of the ABI.
+E2E_SRC = os.path.join(PKG, "e2e", "e2e_loop.cu")
+E2E_LIB = os.path.join(PKG, "libfdec_e2e.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
@@ -73,7 +76,21 @@ def build(force: bool = False, verbose: bool = False, jobs: int = 0) -> str:
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, LIB)
+    _build_e2e(nvcc, force)
     return LIB
+
+
+def _build_e2e(nvcc: str, force: bool) -> None:
+    """libfdec_e2e.so: the C end-to-end loop bench.py times (links libfdec.so via $ORIGIN)."""
+    if (not force and os.path.exists(E2E_LIB) and os.path.getmtime(E2E_LIB) >= os.path.getmtime(E2E_SRC)
+            and os.path.getmtime(E2E_LIB) >= os.path.getmtime(LIB)):
+        return
+    tmp = E2E_LIB + f".tmp{os.getpid()}"
+    cmd = [nvcc, *ARCH, *FLAGS, "-shared", E2E_SRC, "-o", tmp, "-L", PKG, "-lfdec", "-Xlinker", "-rpath,$ORIGIN"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"building the e2e helper failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, E2E_LIB)
 
 
 if __name__ == "__main__":

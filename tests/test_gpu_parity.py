@@ -77,13 +77,21 @@ def test_multi_token_spec_decode(q_len):
 
 
 def test_multi_token_prefill_chunk_sampled_rows():
+    # every 16th query position plus the last, on one query head of every KV head (the 8
+    # heads step through the groups), and every query head at the tile and CTA boundaries
+    # (query rows of one 128-row tile are 32 positions x 4 heads; a CTA holds two tiles)
     w = W.multi_token(2048, device="cuda")
-    rows = []
+    strided = sorted(set(range(0, w.q_len, 16)) | {w.q_len - 1})
+    boundary = [0, 1, 31, 32, 63, 64, 127, 128, 1000, 2046, 2047]
+    spread_heads = [5 * k % w.num_qo_heads if k < 4 else 16 + 5 * (k - 4) for k in range(8)]
+    assert sorted({h // w.group for h in spread_heads}) == list(range(w.num_kv_heads))
+    rows = set()
     for b in range(w.batch):
-        for i in [0, 1, 31, 32, 63, 64, 1000, 2046, 2047]:
-            for h in (0, 3, 4, 5, 31):
-                rows.append((b * w.q_len + i) * w.num_qo_heads + h)
-    (e_out, e_lse), pd = _check(w, rows=rows)
+        for i in strided:
+            rows.update((b * w.q_len + i) * w.num_qo_heads + h for h in spread_heads)
+        for i in boundary:
+            rows.update((b * w.q_len + i) * w.num_qo_heads + h for h in range(w.num_qo_heads))
+    (e_out, e_lse), pd = _check(w, rows=sorted(rows))
     assert pd.info["path"] == fd.FDEC_PATH_TC
 
 

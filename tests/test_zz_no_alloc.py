@@ -77,3 +77,43 @@ def test_plans_larger_than_the_built_in_array_are_refused():
                                        ctypes.c_float(1.0), None, None, None)
     assert fd.STATUS_NAMES[st] == "FDEC_ERR_WORKSPACE"
     assert "16777216" in fd.fdec_last_error()
+
+
+_FRESH_PROCESS = r'''
+import sys
+sys.path.insert(0, sys.argv[1])
+import numpy as np
+import torch
+import paged_split_kv_gather_gb300 as fd
+from paged_split_kv_gather_gb300 import workloads as W
+from tests.helpers import LSE_TOL, OUT_TOL, lse_abs_err, oracle_run, row_rel_err
+w = W.make(2, 1, 32, 4, 128, 64, [5000, 70], dtype="bf16", device="cuda", seed=9)
+plan = fd.fdec_plan(w.seq_lens, 1, w.page_size, 32, 4, 128, "bf16")  # never uploaded
+table = torch.as_tensor(w.page_table, device="cuda")
+lens = torch.as_tensor(w.seq_lens, device="cuda")
+ref_o, ref_l = oracle_run(w.to("cpu"))
+for call in range(2):
+    o = torch.full((2, 1, 32, 128), float("nan"), device="cuda")
+    l = torch.full((2, 1, 32), float("nan"), device="cuda")
+    fd.fdec_run_static_workspace(plan, w.q, w.k, w.v, table, lens, o, l, scale=w.scale)
+    torch.cuda.synchronize()
+    e_o = row_rel_err(o.cpu().double().numpy(), ref_o)
+    e_l = lse_abs_err(l.cpu().double().numpy(), ref_l)
+    assert e_o <= OUT_TOL and e_l <= LSE_TOL, (call, e_o, e_l)
+print("fresh-process no-alloc run ok")
+'''
+
+
+@pytest.mark.gpu
+def test_first_call_in_a_fresh_process_on_a_plan_that_was_never_uploaded():
+    # The intended use: a caller that cannot allocate makes a plan and calls the
+    # no-alloc entry point first, before anything else in the process touched the
+    # kernels (attributes, tensor maps) or the built-in array.
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FRESH_PROCESS, root], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "fresh-process no-alloc run ok" in r.stdout
