@@ -120,6 +120,8 @@ struct fdec_plan_s {
     bool kv8 = false;  // K/V stored as E4M3 codes
     int causal = 0;
     int path = FDEC_PATH_SIMT;
+    bool persistent = false;  // MMA path over 16-bit caches: resident CTAs take work units
+    int n_units = 0, persist_grid = 0;
     int rc = 1, row_groups = 1;
     int blocks_per_split = 1, fanin = 64, num_sms = 0, ctas_per_sm = 1;
     int max_pages_needed = 0;  // max_b ceil(capacity_b / page_size)
@@ -128,7 +130,7 @@ struct fdec_plan_s {
     std::vector<WorkItem> items;
     std::vector<std::vector<ReduceTask>> passes;
     // workspace layout
-    size_t off_err = 0, off_cap = 0, off_items = 0;
+    size_t off_err = 0, off_ticket = 0, off_cap = 0, off_items = 0;
     std::vector<size_t> off_tasks;
     size_t off_a_o = 0, off_a_ml = 0, off_b_o = 0, off_b_ml = 0;
     size_t slots_a = 0, slots_b = 0;
@@ -216,10 +218,14 @@ int choose_blocks_per_split(const std::vector<int>& nblocks, int copies, int slo
     return best;
 }
 
-cudaError_t dispatch_split(const fdec_plan_s* p, const SplitParams& sp, dim3 grid, cudaStream_t stream, bool launch) {
+cudaError_t dispatch_split(const fdec_plan_s* p, const SplitParams& sp, dim3 grid, cudaStream_t stream, bool launch,
+                           bool persist = false) {
     const bool bf16 = p->dtype == FDEC_BF16;
     const CUtensorMap& tk = p->tmap_k;
     const CUtensorMap& tv = p->tmap_v;
+    if (persist)
+        return launch_split_mma_persist(sp, tk, tv, p->head_dim, bf16, dim3(static_cast<unsigned>(p->persist_grid), 1, 1),
+                                        stream, launch);
     if (p->path == FDEC_PATH_TC) return launch_split_tc(sp, tk, tv, p->rc / kTcRows, bf16, grid, stream, launch);
     if (p->path == FDEC_PATH_MMA)
         return launch_split_mma(sp, tk, tv, p->head_dim, bf16, p->kv8, grid, stream, launch);
@@ -386,8 +392,9 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
         p->path = (tc_ok && p->rows > kMmaRows) ? FDEC_PATH_TC : (mma_ok ? FDEC_PATH_MMA : FDEC_PATH_SIMT);
     else
         p->path = o.path;
+    p->persistent = p->path == FDEC_PATH_MMA && !kv8 && split_mma_persist_supported(head_dim);
     p->num_sms = num_sms;
-    p->fanin = o.reducer_fanin > 0 ? o.reducer_fanin : 256;
+    p->fanin = o.reducer_fanin > 0 ? o.reducer_fanin : 1024;
     size_t smem = 0;
     int threads = 0;
     if (p->path == FDEC_PATH_TC) {
@@ -410,7 +417,8 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
         delete p;
         return fail(FDEC_ERR_UNSUPPORTED, "q_len x group / rows per CTA or num_kv_heads above 65535");
     }
-    p->ctas_per_sm = std::max(1, std::min(static_cast<int>(233472 / (smem + 1024)), 2048 / threads));
+    p->ctas_per_sm = p->persistent ? kPersistCtasPerSm
+                                   : std::max(1, std::min(static_cast<int>(233472 / (smem + 1024)), 2048 / threads));
 
     p->capacity.assign(seq_lens_host, seq_lens_host + batch);
     std::vector<int> nblocks(batch);
@@ -429,23 +437,40 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
                                                  : choose_blocks_per_split(nblocks, copies, slots, partial_cost);
     const int C = p->blocks_per_split;
 
-    // Work items and level-0 partial slots.
+    // Work items and level-0 partial slots.  Uniform runs of C blocks; or, for the
+    // persistent kernel with an automatic plan, a first wave and a dynamic tail: a
+    // sequence the uniform plan cuts into ns items gets ns big items of 80 % of the
+    // even share (taken first, one per resident CTA slot) and the rest in small items
+    // of about C / 8 blocks, taken by whichever CTA frees up first (per-CTA stream
+    // rates differ by about +-12 % under saturation, so the tail balances them).
     p->splits.resize(batch);
     std::vector<int> slot_base(batch, -1);
     size_t next_slot = 0;
+    const bool wave_and_tail = p->persistent && o.blocks_per_split == 0 && C >= 4;
     for (int b = 0; b < batch; ++b) {
-        const int ns = (nblocks[b] + C - 1) / C;
-        p->splits[b] = ns;
-        if (ns > 1) {
-            slot_base[b] = static_cast<int>(next_slot);
-            next_slot += ns;
+        const int nb = nblocks[b];
+        const int ns = (nb + C - 1) / C;
+        std::vector<std::pair<int, int>> runs;  // [begin, end) in blocks
+        if (wave_and_tail && ns > 1) {
+            const int big = std::max(1, static_cast<int>(0.8 * nb / ns));
+            const int small = std::max(1, (C + 7) / 8);
+            for (int k = 0; k < ns; ++k) runs.emplace_back(k * big, (k + 1) * big);
+            for (int x = ns * big; x < nb; x += small) runs.emplace_back(x, std::min(x + small, nb));
+        } else {
+            for (int k = 0; k < ns; ++k) runs.emplace_back(k * C, std::min((k + 1) * C, nb));
         }
-        for (int k = 0; k < ns; ++k) {
+        const int n = static_cast<int>(runs.size());
+        p->splits[b] = n;
+        if (n > 1) {
+            slot_base[b] = static_cast<int>(next_slot);
+            next_slot += n;
+        }
+        for (int k = 0; k < n; ++k) {
             WorkItem it;
             it.seq = b;
-            it.block_begin = k * C;
-            it.block_end = std::min((k + 1) * C, nblocks[b]);
-            it.slot = ns > 1 ? slot_base[b] + k : -1;
+            it.block_begin = runs[k].first;
+            it.block_end = runs[k].second;
+            it.slot = n > 1 ? slot_base[b] + k : -1;
             p->items.push_back(it);
         }
     }
@@ -454,6 +479,8 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
         return (a.block_end - a.block_begin) > (b.block_end - b.block_begin);
     });
     p->slots_a = next_slot;
+    p->n_units = static_cast<int>(p->items.size()) * p->hk * p->row_groups;
+    p->persist_grid = std::min(p->n_units, num_sms * kPersistCtasPerSm);
 
     // Reduction passes: level l merges groups of `fanin` slots; levels alternate
     // between region A (even) and region B (odd).
@@ -495,7 +522,8 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
     // Workspace layout: metadata first (uploaded), partial regions after.
     size_t off = 0;
     p->off_err = off;
-    off = align_up(off + sizeof(uint32_t));
+    p->off_ticket = off + 8;  // the persistent kernel's unit counter (uint64)
+    off = align_up(off + 16);
     p->off_cap = off;
     off = align_up(off + sizeof(int32_t) * batch);
     p->off_items = off;
@@ -540,7 +568,7 @@ fdec_status fdec_plan_get_info(fdec_plan_t p, fdec_plan_info* info) {
     info->path = p->path;
     info->blocks_per_split = p->blocks_per_split;
     info->num_items = static_cast<int>(p->items.size());
-    info->num_split_ctas = static_cast<int>(p->items.size()) * p->hk * p->row_groups;
+    info->num_split_ctas = p->persistent ? p->persist_grid : static_cast<int>(p->items.size()) * p->hk * p->row_groups;
     info->row_groups = p->row_groups;
     info->rows_per_group = p->rc;
     for (int s : p->splits) info->max_splits = std::max(info->max_splits, s);
@@ -576,6 +604,7 @@ fdec_status fdec_plan_upload(fdec_plan_t p, void* workspace, cudaStream_t stream
     // Set the split kernel's shared-memory attribute here, outside any capture.
     SplitParams none{};
     e = dispatch_split(p, none, dim3(1, 1, 1), stream, false);
+    if (e == cudaSuccess && p->persistent) e = dispatch_split(p, none, dim3(1, 1, 1), stream, false, true);
     if (e != cudaSuccess) return fail_cuda(e, "preparing the split kernel");
     e = cudaMemcpyAsync(workspace, p->meta.data(), p->meta_bytes, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return fail_cuda(e, "uploading the plan");
@@ -692,10 +721,15 @@ fdec_status fdec_run_scaled(fdec_plan_t p, const void* q, int64_t q_stride_tok, 
     sp.v_pos_slot = p->v_pos[0];
     sp.v_pos_head = p->v_pos[1];
     sp.v_pos_page = p->v_pos[2];
+    sp.n_units = p->n_units;
+    sp.ticket = reinterpret_cast<unsigned long long*>(ws + p->off_ticket);
 
+    // The persistent kernel copies each unit's query rows with 16-byte bulk copies.
+    const bool q_rows_aligned = reinterpret_cast<uintptr_t>(q) % 16 == 0 && (q_stride_tok * 2) % 16 == 0 &&
+                                (q_stride_head * 2) % 16 == 0;
     const dim3 grid(static_cast<unsigned>(p->items.size()), static_cast<unsigned>(p->hk),
                     static_cast<unsigned>(p->row_groups));
-    cudaError_t e = dispatch_split(p, sp, grid, stream, true);
+    cudaError_t e = dispatch_split(p, sp, grid, stream, true, p->persistent && q_rows_aligned);
     if (e != cudaSuccess) return fail_cuda(e, "launching the split kernel");
     if (p->split_event != nullptr) {
         e = cudaEventRecord(p->split_event, stream);

@@ -59,6 +59,11 @@ struct SplitParams {
     // Coordinate position (1..3) of the slot, head and page dims in each tensor map.
     int k_pos_slot, k_pos_head, k_pos_page;
     int v_pos_slot, v_pos_head, v_pos_page;
+    // Persistent split kernel: work units = items x KV heads x row groups, in item
+    // order; CTA c starts with unit c and takes the units past the grid from the
+    // ticket counter (advanced by exactly n_units per launch).
+    int n_units;
+    unsigned long long* ticket;
 };
 
 struct ReduceParams {
@@ -95,6 +100,13 @@ cudaError_t launch_split_d512(const SplitParams& p, const CUtensorMap& tk, const
 cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int head_dim,
                              bool bf16, bool kv8, dim3 grid, cudaStream_t s, bool launch);
 size_t split_mma_smem_bytes(int head_dim, bool kv8);
+// The persistent form of the tensor-core split kernel (16-bit caches, head_dim 64, 128
+// and 192; q rows 16-byte aligned): CTAs stay resident and take work units until none
+// is left, so a unit's pipeline fill and the stragglers' tail are paid once per CTA.
+cudaError_t launch_split_mma_persist(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int head_dim,
+                                     bool bf16, dim3 grid, cudaStream_t s, bool launch);
+inline bool split_mma_persist_supported(int head_dim) { return head_dim == 64 || head_dim == 128 || head_dim == 192; }
+constexpr int kPersistCtasPerSm = 2;
 int split_mma_threads(int head_dim, bool kv8);
 inline bool split_mma_kv8_supported(int head_dim) { return head_dim == 128 || head_dim == 256; }
 constexpr int kMmaRows = 16;

@@ -168,189 +168,102 @@ __device__ __forceinline__ float q_row_factor(uint32_t mbits, bool forward) {
     return __int_as_float((127 + (forward ? sh : -sh)) << 23);
 }
 
+// One consumer warp of the tensor-core split kernels: its lane addressing into
+// the swizzled stages, its query fragments, its running state (O accumulators
+// of this warp's DH columns; row max m and sum l of rows g and g + 8, in log2
+// units) and the work of one 32-token stage.
 template <int D, bool BF16, bool KV8>
-__global__ void __launch_bounds__(MmaLayout<D, KV8>::THREADS, MmaLayout<D, KV8>::CTAS_PER_SM)
-split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
-                 const __grid_constant__ CUtensorMap tmv) {
+struct MmaWarp {
     using Lay = MmaLayout<D, KV8>;
     using G = StageGeom<D>;
     using GS = typename Lay::GS;
-    constexpr int NW = Lay::NW;
-    constexpr int S = Lay::S;
-    constexpr int RC = Lay::RC;
-    constexpr int NP = Lay::NP;          // consumer groups, one stage each
-    constexpr int DSPLIT = Lay::DSPLIT;  // warps per group (each owns DH columns of O)
-    constexpr int DH = Lay::DH;
-    constexpr int KSTEPS = D / 16;       // k-steps of S = Q K^T
-    constexpr int NT = DH / 8;           // n-tiles of this warp's O
-    constexpr bool MB = KV8 ? false : BF16;  // operand type of the MMAs (f16 over E4M3 caches)
-    constexpr bool QSCALE = KV8 && BF16;     // bf16 query rows rescaled into f16
-    constexpr bool P1 = KV8;                 // one f16 P (11 bits) instead of a 16-bit hi + lo pair
-    constexpr float kP1Scale = 128.f;        // 2^7
-    const float o_out = P1 ? 1.f / kP1Scale : 1.f;
+    static constexpr int RC = Lay::RC;
+    static constexpr int DH = Lay::DH;
+    static constexpr int KSTEPS = D / 16;    // k-steps of S = Q K^T
+    static constexpr int NT = DH / 8;        // n-tiles of this warp's O
+    static constexpr bool MB = KV8 ? false : BF16;  // operand type of the MMAs (f16 over E4M3 caches)
+    static constexpr bool P1 = KV8;                 // one f16 P (11 bits) instead of a 16-bit hi + lo pair
+    static constexpr float kP1Scale = 128.f;        // 2^7
+    static constexpr int QREGS = Lay::Q_IN_REGS ? KSTEPS : 1;
 
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + 2 * S;
-    uint16_t* q_s = reinterpret_cast<uint16_t*>(smem + Lay::BAR_BYTES);
-    uint8_t* stages;
-    {
-        const uint32_t raw = smem_addr(smem) + Lay::BAR_BYTES + Lay::Q_BYTES;
-        const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-        stages = smem + Lay::BAR_BYTES + Lay::Q_BYTES + pad;
-    }
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const WorkItem it = p.items[blockIdx.x];
-    const int b = it.seq;
-    const int kvh = blockIdx.y;
-    const int row0 = blockIdx.z * RC;
-    const bool tma_mode = p.page_shift >= 3;
-    if (threadIdx.x == 0) init_stage_barriers<S>(full, empty, tma_mode, DSPLIT);
-    __syncthreads();  // barriers initialised (nothing before this waits on memory)
-    const ItemRange ir = item_range(p, it);
-
-    if (warp == NW) {
-        // The producer starts at once: its page-table reads overlap the length and q loads.
-        if (lane == 0 && tma_mode) {
-            prefetch_tmap(&tmk);
-            prefetch_tmap(&tmv);
-        }
-        produce_stages<D, S, kStageTokens, KV8 ? 1 : 2>(p, &tmk, &tmv, full, empty, stages, b, kvh, ir, tma_mode);
-        return;
-    }
-    if (threadIdx.x == 0) report_item_range(p, ir);
-    // The group's query rows, as stored (16-bit, [RC][D]); rows past the group are zero.
-    // QSCALE: bf16 rows -> f16 rows times 2^sh(row), sh from the row's largest magnitude.
-    uint32_t* q_rmax = reinterpret_cast<uint32_t*>(smem + Lay::QMAX_OFFSET);  // [RC] largest |q| (bf16 bits)
-    {
-        QChunks<RC, D, NW * 32> qc;
-        qc.load(p, b, kvh, row0, threadIdx.x);
-        if constexpr (QSCALE) {
-            if (threadIdx.x < RC) q_rmax[threadIdx.x] = 0u;
-            named_barrier(1, NW * 32);
-#pragma unroll
-            for (int i = 0; i < qc.PER; ++i) {
-                const int idx = qc.chunk(threadIdx.x, i);
-                if (idx < qc.CH) {
-                    const uint32_t w[4] = {qc.v[i].x, qc.v[i].y, qc.v[i].z, qc.v[i].w};
-                    uint32_t mx = 0;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) mx = max(mx, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
-                    atomicMax(&q_rmax[idx / (D / 8)], mx);  // bf16 magnitudes order as integers
-                }
-            }
-            named_barrier(1, NW * 32);
-#pragma unroll
-            for (int i = 0; i < qc.PER; ++i) {
-                const int idx = qc.chunk(threadIdx.x, i);
-                if (idx < qc.CH) {
-                    const float f = q_row_factor(q_rmax[idx / (D / 8)], true);
-                    const uint32_t w[4] = {qc.v[i].x, qc.v[i].y, qc.v[i].z, qc.v[i].w};
-                    uint32_t h[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 v = unpack2<true>(w[e]);
-                        const __half2 hv = __floats2half2_rn(v.x * f, v.y * f);
-                        h[e] = *reinterpret_cast<const uint32_t*>(&hv);
-                    }
-                    *reinterpret_cast<uint4*>(q_s + idx * 8) = make_uint4(h[0], h[1], h[2], h[3]);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < qc.PER; ++i) {
-                const int idx = qc.chunk(threadIdx.x, i);
-                if (idx < qc.CH) *reinterpret_cast<uint4*>(q_s + idx * 8) = qc.v[i];
-            }
-        }
-    }
-    named_barrier(1, NW * 32);
-
-    // ---------------------------------------------------------------------- consumers
-    const int g = lane >> 2;   // fragment row (and row + 8)
-    const int tq = lane & 3;   // fragment column pair
-    const int mi = lane >> 3;  // ldmatrix: which 8x8 matrix this lane addresses
-
-    constexpr int QREGS = Lay::Q_IN_REGS ? KSTEPS : 1;
+    int lane, g, tq, mi;  // g: fragment row (and row + 8); tq: column pair; mi: ldmatrix matrix
+    // 16-bit stages: ldmatrix row addresses within a stage (chunk c of row r at c ^ (r & 7)).
+    uint32_t kb_row[2], kb_x[4], vb_row[2], vb_x[4];
+    // KV8 ldmatrix addresses in a code stage (32 token rows of D/128 regions of 128 bytes).
+    // K: lane l addresses token l (matrix = n-tile l / 8).  V: lane l addresses token
+    // 16 k2 + 8 ((l >> 3) & 1) + (l & 7) of chunk c + (l >> 4).
+    uint32_t k8_row, k8_x, v8_row[2], v8_x;
     uint32_t qa[QREGS][4];
-    const uint32_t q_lane = smem_addr(q_s) + ((mi & 1) * 8 + (lane & 7)) * (D * 2) + (mi >> 1) * 16;
+    float o[NT][4];
+    float mrow[2], lrow[2];
+
+    __device__ __forceinline__ explicit MmaWarp(int lane_) : lane(lane_), g(lane_ >> 2), tq(lane_ & 3), mi(lane_ >> 3) {
+        k8_row = static_cast<uint32_t>(lane * 128);
+        k8_x = static_cast<uint32_t>((lane & 7) << 4);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            v8_row[j] = static_cast<uint32_t>((16 * j + 8 * ((lane >> 3) & 1) + (lane & 7)) * 128);
+        v8_x = static_cast<uint32_t>((((lane >> 4) & 1) ^ (lane & 7)) << 4);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            kb_row[j] = static_cast<uint32_t>((8 * (2 * j + (mi >> 1)) + (lane & 7)) * 128);
+            vb_row[j] = static_cast<uint32_t>((16 * j + 8 * (mi & 1) + (lane & 7)) * 128);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            kb_x[j] = static_cast<uint32_t>(((2 * j + (mi & 1)) ^ (lane & 7)) << 4);
+            vb_x[j] = static_cast<uint32_t>(((2 * j + (mi >> 1)) ^ (lane & 7)) << 4);
+        }
+        reset();
+    }
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        mrow[0] = mrow[1] = -INFINITY;
+        lrow[0] = lrow[1] = 0.f;
+    }
+
+    // ldmatrix address of this lane in the query rows q_s ([RC][D] 16-bit, row-major).
+    __device__ __forceinline__ uint32_t q_lane(const uint16_t* q_s) const {
+        return smem_addr(q_s) + ((mi & 1) * 8 + (lane & 7)) * (D * 2) + (mi >> 1) * 16;
+    }
+
     // KV8: A fragments in the permuted k order of the code fragments (dims 16 kk + 4 tq .. + 3
     // of rows g and g + 8: k slots 2tq, 2tq+1 and 2tq+8, 2tq+9).
-    auto load_q8 = [&](int kk, uint32_t(&a)[4]) {
+    __device__ __forceinline__ void load_q8(const uint16_t* q_s, int kk, uint32_t (&a)[4]) const {
         const uint2 r0 = *reinterpret_cast<const uint2*>(q_s + g * D + 16 * kk + 4 * tq);
         const uint2 r1 = *reinterpret_cast<const uint2*>(q_s + (g + 8) * D + 16 * kk + 4 * tq);
         a[0] = r0.x;
         a[1] = r1.x;
         a[2] = r0.y;
         a[3] = r1.y;
-    };
-    if constexpr (Lay::Q_IN_REGS) {
-        static_for<0, KSTEPS>([&](auto kk_) {
-            constexpr int kk = decltype(kk_)::value;
-            if constexpr (KV8)
-                load_q8(kk, qa[kk]);
-            else
-                ldmatrix_x4(q_lane + 2 * kk * 16, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-        });
-    }
-    // KV8 ldmatrix addresses in a code stage (32 token rows of D/128 regions of 128 bytes;
-    // chunk c of row r at c ^ (r & 7)).  K: lane l addresses token l (matrix = n-tile l / 8).
-    // V: lane l addresses token 16 k2 + 8 ((l >> 3) & 1) + (l & 7) of chunk c + (l >> 4).
-    const uint32_t k8_row = static_cast<uint32_t>(lane * 128);
-    const uint32_t k8_x = static_cast<uint32_t>((lane & 7) << 4);
-    uint32_t v8_row[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) v8_row[j] = static_cast<uint32_t>((16 * j + 8 * ((lane >> 3) & 1) + (lane & 7)) * 128);
-    const uint32_t v8_x = static_cast<uint32_t>((((lane >> 4) & 1) ^ (lane & 7)) << 4);
-    // ldmatrix row addresses within a stage (swizzled: chunk c of row r at c ^ (r & 7)).
-    uint32_t kb_row[2], kb_x[4], vb_row[2], vb_x[4];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        kb_row[j] = static_cast<uint32_t>((8 * (2 * j + (mi >> 1)) + (lane & 7)) * 128);
-        vb_row[j] = static_cast<uint32_t>((16 * j + 8 * (mi & 1) + (lane & 7)) * 128);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        kb_x[j] = static_cast<uint32_t>(((2 * j + (mi & 1)) ^ (lane & 7)) << 4);
-        vb_x[j] = static_cast<uint32_t>(((2 * j + (mi >> 1)) ^ (lane & 7)) << 4);
     }
 
-    float o[NT][4];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float mrow[2] = {-INFINITY, -INFINITY};
-    float lrow[2] = {0.f, 0.f};
-    int lim[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int qi = (row0 + g + 8 * h) / p.group;
-        lim[h] = p.causal ? (ir.L - p.q_len + qi) : (ir.L - 1);
-    }
-    // Logit scale of rows g and g + 8 (QSCALE: the row factor taken back out).
-    float sl[2] = {p.scale_log2, p.scale_log2};
-    if constexpr (QSCALE) {
-        sl[0] = p.scale_log2 * q_row_factor(q_rmax[g], false);
-        sl[1] = p.scale_log2 * q_row_factor(q_rmax[g + 8], false);
-    }
-    bool ok = true;
-
-    const int grp = warp / DSPLIT;             // consumer group: stages grp, grp + NP, ...
-    const int half = warp - grp * DSPLIT;      // which DH columns of O this warp accumulates
-    const uint32_t v_half = static_cast<uint32_t>(half * (DH / 64) * G::REGION_BYTES);
-    for (int i = grp; i < ir.n_stage; i += NP) {
-        const int s = i % S;
-        if (!wait_stage<S>(full, i)) {
-            ok = false;
-            break;
+    // Q's A fragments into registers (when they stay there for the whole run).
+    __device__ __forceinline__ void load_q(const uint16_t* q_s) {
+        if constexpr (Lay::Q_IN_REGS) {
+            const uint32_t ql = q_lane(q_s);
+            static_for<0, KSTEPS>([&](auto kk_) {
+                constexpr int kk = decltype(kk_)::value;
+                if constexpr (KV8)
+                    load_q8(q_s, kk, qa[kk]);
+                else
+                    ldmatrix_x4(ql + 2 * kk * 16, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+            });
         }
-        const int t0 = ir.tok_begin + i * kStageTokens;
-        const int nv = min(kStageTokens, ir.tok_end - t0);
-        uint8_t* stage = stages + s * GS::STAGE_BYTES;
-        const uint32_t kbase = smem_addr(stage);
+    }
+
+    // One 32-token stage: S = Q K^T, masked online softmax in log2 units, O += P V.
+    // nv: tokens of the stage that exist (the V rows past them are zeroed here);
+    // vis0 / vis1: tokens rows g / g + 8 may see; sl: their logit scales; v_half:
+    // byte offset of this warp's DH columns of V.
+    __device__ __forceinline__ void stage(const uint16_t* q_s, uint8_t* stage_ptr, int nv, int vis0, int vis1,
+                                          const float (&sl)[2], uint32_t v_half) {
+        const uint32_t kbase = smem_addr(stage_ptr);
         const uint32_t vbase = kbase + GS::HALF_BYTES;
-        if (nv < kStageTokens) zero_v_tail<D, kStageTokens, KV8 ? 1 : 2>(stage, nv);
+        if (nv < kStageTokens) zero_v_tail<D, kStageTokens, KV8 ? 1 : 2>(stage_ptr, nv);
+        const uint32_t ql = Lay::Q_IN_REGS ? 0u : q_lane(q_s);
 
         // S = Q K^T for the stage's 32 tokens (4 n-tiles of 8)
         float sc[4][4];
@@ -360,7 +273,7 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
             constexpr int kk = decltype(kk_)::value;
             constexpr int qk = Lay::Q_IN_REGS ? kk : 0;
             if constexpr (KV8) {
-                if constexpr (!Lay::Q_IN_REGS) load_q8(kk, qa[0]);
+                if constexpr (!Lay::Q_IN_REGS) load_q8(q_s, kk, qa[0]);
                 uint32_t r[4];
                 ldmatrix_x4(kbase + (kk >> 3) * GS::REGION_BYTES + k8_row + ((static_cast<uint32_t>(kk & 7) << 4) ^ k8_x),
                             r[0], r[1], r[2], r[3]);
@@ -372,7 +285,7 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
                 }
             } else {
                 if constexpr (!Lay::Q_IN_REGS)
-                    ldmatrix_x4(q_lane + 2 * kk * 16, qa[0][0], qa[0][1], qa[0][2], qa[0][3]);
+                    ldmatrix_x4(ql + 2 * kk * 16, qa[0][0], qa[0][1], qa[0][2], qa[0][3]);
 #pragma unroll
                 for (int pr = 0; pr < 2; ++pr) {
                     uint32_t b0, b1, b2, b3;
@@ -385,8 +298,6 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
 
         // softmax in log2 units on the fragments: element e of n-tile n is
         // row g + 8 * (e >> 1), token 8 n + 2 tq + (e & 1)
-        const int vis0 = min(nv, lim[0] - t0 + 1);
-        const int vis1 = min(nv, lim[1] - t0 + 1);
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
@@ -483,15 +394,151 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
                 });
             }
         }
+    }
+
+    // Row sums of the lane quad (after the last stage).
+    __device__ __forceinline__ void finish_l() {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 1);
+            lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 2);
+        }
+    }
+};
+
+template <int D, bool BF16, bool KV8>
+__global__ void __launch_bounds__(MmaLayout<D, KV8>::THREADS, MmaLayout<D, KV8>::CTAS_PER_SM)
+split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
+                 const __grid_constant__ CUtensorMap tmv) {
+    using Lay = MmaLayout<D, KV8>;
+    using W = MmaWarp<D, BF16, KV8>;
+    using G = StageGeom<D>;
+    using GS = typename Lay::GS;
+    constexpr int NW = Lay::NW;
+    constexpr int S = Lay::S;
+    constexpr int RC = Lay::RC;
+    constexpr int NP = Lay::NP;          // consumer groups, one stage each
+    constexpr int DSPLIT = Lay::DSPLIT;  // warps per group (each owns DH columns of O)
+    constexpr int DH = Lay::DH;
+    constexpr int NT = W::NT;
+    constexpr bool QSCALE = KV8 && BF16;     // bf16 query rows rescaled into f16
+    const float o_out = W::P1 ? 1.f / W::kP1Scale : 1.f;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + 2 * S;
+    uint16_t* q_s = reinterpret_cast<uint16_t*>(smem + Lay::BAR_BYTES);
+    uint8_t* stages;
+    {
+        const uint32_t raw = smem_addr(smem) + Lay::BAR_BYTES + Lay::Q_BYTES;
+        const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+        stages = smem + Lay::BAR_BYTES + Lay::Q_BYTES + pad;
+    }
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const WorkItem it = p.items[blockIdx.x];
+    const int b = it.seq;
+    const int kvh = blockIdx.y;
+    const int row0 = blockIdx.z * RC;
+    const bool tma_mode = p.page_shift >= 3;
+    if (threadIdx.x == 0) init_stage_barriers<S>(full, empty, tma_mode, DSPLIT);
+    __syncthreads();  // barriers initialised (nothing before this waits on memory)
+    const ItemRange ir = item_range(p, it);
+
+    if (warp == NW) {
+        // The producer starts at once: its page-table reads overlap the length and q loads.
+        if (lane == 0 && tma_mode) {
+            prefetch_tmap(&tmk);
+            prefetch_tmap(&tmv);
+        }
+        produce_stages<D, S, kStageTokens, KV8 ? 1 : 2>(p, &tmk, &tmv, full, empty, stages, b, kvh, ir, tma_mode);
+        return;
+    }
+    if (threadIdx.x == 0) report_item_range(p, ir);
+    // The group's query rows, as stored (16-bit, [RC][D]); rows past the group are zero.
+    // QSCALE: bf16 rows -> f16 rows times 2^sh(row), sh from the row's largest magnitude.
+    uint32_t* q_rmax = reinterpret_cast<uint32_t*>(smem + Lay::QMAX_OFFSET);  // [RC] largest |q| (bf16 bits)
+    {
+        QChunks<RC, D, NW * 32> qc;
+        qc.load(p, b, kvh, row0, threadIdx.x);
+        if constexpr (QSCALE) {
+            if (threadIdx.x < RC) q_rmax[threadIdx.x] = 0u;
+            named_barrier(1, NW * 32);
+#pragma unroll
+            for (int i = 0; i < qc.PER; ++i) {
+                const int idx = qc.chunk(threadIdx.x, i);
+                if (idx < qc.CH) {
+                    const uint32_t w[4] = {qc.v[i].x, qc.v[i].y, qc.v[i].z, qc.v[i].w};
+                    uint32_t mx = 0;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) mx = max(mx, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
+                    atomicMax(&q_rmax[idx / (D / 8)], mx);  // bf16 magnitudes order as integers
+                }
+            }
+            named_barrier(1, NW * 32);
+#pragma unroll
+            for (int i = 0; i < qc.PER; ++i) {
+                const int idx = qc.chunk(threadIdx.x, i);
+                if (idx < qc.CH) {
+                    const float f = q_row_factor(q_rmax[idx / (D / 8)], true);
+                    const uint32_t w[4] = {qc.v[i].x, qc.v[i].y, qc.v[i].z, qc.v[i].w};
+                    uint32_t h[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 v = unpack2<true>(w[e]);
+                        const __half2 hv = __floats2half2_rn(v.x * f, v.y * f);
+                        h[e] = *reinterpret_cast<const uint32_t*>(&hv);
+                    }
+                    *reinterpret_cast<uint4*>(q_s + idx * 8) = make_uint4(h[0], h[1], h[2], h[3]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < qc.PER; ++i) {
+                const int idx = qc.chunk(threadIdx.x, i);
+                if (idx < qc.CH) *reinterpret_cast<uint4*>(q_s + idx * 8) = qc.v[i];
+            }
+        }
+    }
+    named_barrier(1, NW * 32);
+
+    // ---------------------------------------------------------------------- consumers
+    W cw(lane);
+    const int g = cw.g, tq = cw.tq;
+    cw.load_q(q_s);
+    int lim[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int qi = (row0 + g + 8 * h) / p.group;
+        lim[h] = p.causal ? (ir.L - p.q_len + qi) : (ir.L - 1);
+    }
+    // Logit scale of rows g and g + 8 (QSCALE: the row factor taken back out).
+    float sl[2] = {p.scale_log2, p.scale_log2};
+    if constexpr (QSCALE) {
+        sl[0] = p.scale_log2 * q_row_factor(q_rmax[g], false);
+        sl[1] = p.scale_log2 * q_row_factor(q_rmax[g + 8], false);
+    }
+    bool ok = true;
+
+    const int grp = warp / DSPLIT;             // consumer group: stages grp, grp + NP, ...
+    const int half = warp - grp * DSPLIT;      // which DH columns of O this warp accumulates
+    const uint32_t v_half = static_cast<uint32_t>(half * (DH / 64) * G::REGION_BYTES);
+    for (int i = grp; i < ir.n_stage; i += NP) {
+        const int s = i % S;
+        if (!wait_stage<S>(full, i)) {
+            ok = false;
+            break;
+        }
+        const int t0 = ir.tok_begin + i * kStageTokens;
+        const int nv = min(kStageTokens, ir.tok_end - t0);
+        cw.stage(q_s, stages + s * GS::STAGE_BYTES, nv, min(nv, lim[0] - t0 + 1), min(nv, lim[1] - t0 + 1), sl,
+                 v_half);
         if (nv < kStageTokens) fence_proxy_async_shared();  // generic zeroing before the slot's next TMA write
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
     }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 1);
-        lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 2);
-    }
+    cw.finish_l();
     if (!ok && lane == 0) atomicOr(p.err, FDEC_DEVERR_TIMEOUT);
 
     // ---------------------------------------------------------------------- epilogue
@@ -502,10 +549,10 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
     float* sm_l = sm_m + NP * RC;                     // [NP][RC]
     float* sm_o = sm_l + NP * RC;                     // [NP][RC][D]
     if (tq == 0 && half == 0) {  // the warps of a group hold the same m and l
-        sm_m[grp * RC + g] = mrow[0];
-        sm_m[grp * RC + g + 8] = mrow[1];
-        sm_l[grp * RC + g] = lrow[0];
-        sm_l[grp * RC + g + 8] = lrow[1];
+        sm_m[grp * RC + g] = cw.mrow[0];
+        sm_m[grp * RC + g + 8] = cw.mrow[1];
+        sm_l[grp * RC + g] = cw.lrow[0];
+        sm_l[grp * RC + g + 8] = cw.lrow[1];
     }
     if constexpr (KV8) {
         // o[2c] / o[2c+1]: dims 16c + 2n / 16c + 2n + 1 of column n: this lane's columns 2tq, 2tq+1
@@ -513,17 +560,19 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
 #pragma unroll
         for (int c = 0; c < D / 16; ++c) {
             *reinterpret_cast<float4*>(sm_o + (grp * RC + g) * D + 16 * c + 4 * tq) =
-                make_float4(o[2 * c][0] * o_out, o[2 * c + 1][0] * o_out, o[2 * c][1] * o_out, o[2 * c + 1][1] * o_out);
+                make_float4(cw.o[2 * c][0] * o_out, cw.o[2 * c + 1][0] * o_out, cw.o[2 * c][1] * o_out,
+                            cw.o[2 * c + 1][1] * o_out);
             *reinterpret_cast<float4*>(sm_o + (grp * RC + g + 8) * D + 16 * c + 4 * tq) =
-                make_float4(o[2 * c][2] * o_out, o[2 * c + 1][2] * o_out, o[2 * c][3] * o_out, o[2 * c + 1][3] * o_out);
+                make_float4(cw.o[2 * c][2] * o_out, cw.o[2 * c + 1][2] * o_out, cw.o[2 * c][3] * o_out,
+                            cw.o[2 * c + 1][3] * o_out);
         }
     }
 #pragma unroll
     for (int n = 0; n < (KV8 ? 0 : NT); ++n) {
         *reinterpret_cast<float2*>(sm_o + (grp * RC + g) * D + half * DH + 8 * n + 2 * tq) =
-            make_float2(o[n][0] * o_out, o[n][1] * o_out);
+            make_float2(cw.o[n][0] * o_out, cw.o[n][1] * o_out);
         *reinterpret_cast<float2*>(sm_o + (grp * RC + g + 8) * D + half * DH + 8 * n + 2 * tq) =
-            make_float2(o[n][2] * o_out, o[n][3] * o_out);
+            make_float2(cw.o[n][2] * o_out, cw.o[n][3] * o_out);
     }
     named_barrier(1, NW * 32);
     merge_and_store<NP, RC, D, NW * 32>(p, it, kvh, row0, sm_m, sm_l, sm_o);

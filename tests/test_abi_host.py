@@ -315,14 +315,25 @@ def test_plan_invariants_hold_for_random_batches():
         if bps:
             assert C == bps
         nb = np.maximum(1, -(-np.asarray(lens, dtype=np.int64) // 64))
-        assert np.array_equal(splits, -(-nb // C))
-        assert info["num_items"] == int(splits.sum()) and info["max_splits"] == int(splits.max())
         rows = q_len * group
         want_path = fd.FDEC_PATH_TC if (not kv8 and d == 128 and rows > 16) else fd.FDEC_PATH_MMA
         assert info["path"] == want_path
+        # the persistent kernel (16-bit caches, head_dim 64/128/192 on the 16-row path)
+        persistent = want_path == fd.FDEC_PATH_MMA and not kv8 and d in (64, 128, 192)
+        ns = -(-nb // C)
+        if persistent and not bps and C >= 4:
+            # ns big items of 80 % of the even share, then small items of ceil(C / 8) blocks
+            big = np.maximum(1, (0.8 * nb / ns).astype(np.int64))
+            small = max(1, (C + 7) // 8)
+            want = np.where(ns > 1, ns + -(-(nb - ns * big) // small), ns)
+        else:
+            want = ns
+        assert np.array_equal(splits, want)
+        assert info["num_items"] == int(splits.sum()) and info["max_splits"] == int(splits.max())
         assert info["row_groups"] == -(-rows // info["rows_per_group"])
-        assert info["num_split_ctas"] == info["num_items"] * hk * info["row_groups"]
-        F = fanin or 256
+        units = info["num_items"] * hk * info["row_groups"]
+        assert info["num_split_ctas"] == (min(units, 152 * 2) if persistent else units)
+        F = fanin or 1024
         n, passes = int(splits.max()), 0
         while n > 1:
             n, passes = -(-n // F), passes + 1

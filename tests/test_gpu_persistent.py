@@ -1,0 +1,113 @@
+"""The persistent split kernel (resident CTAs taking work units from a counter)
+against the one-CTA-per-item kernel and the oracle.
+
+Both kernels run the same plan: the persistent one when q's rows are 16-byte
+aligned, the other when they are not (q offset by one element).  A unit is
+computed by the same code in the same order whichever CTA takes it, so the two
+must agree bit for bit, call after call (the ticket counter carries over from
+call to call and must hand out every unit exactly once each time)."""
+import numpy as np
+import pytest
+import torch
+
+import paged_split_kv_gather_gb300 as fd
+from paged_split_kv_gather_gb300 import workloads as W
+from tests.helpers import assert_parity, oracle_run
+
+pytestmark = pytest.mark.gpu
+
+
+def _misaligned_copy(q):
+    """The same values as q, with rows that start 2 bytes past a 16-byte boundary."""
+    flat = torch.empty(q.numel() + 1, dtype=q.dtype, device=q.device)
+    qm = flat[1:].view(q.shape)
+    qm.copy_(q)
+    assert qm.data_ptr() % 16 != 0
+    return qm
+
+
+def _run(pd, w, q, table, lens):
+    out = torch.full((w.batch, w.q_len, w.num_qo_heads, w.head_dim), float("nan"), device="cuda")
+    lse = torch.full((w.batch, w.q_len, w.num_qo_heads), float("nan"), device="cuda")
+    pd.run(q, w.k, w.v, table, lens, out, lse, scale=w.scale)
+    return out, lse
+
+
+CASES = {
+    "long_32768": lambda: W.long_context(32768, device="cuda"),
+    "long_131072": lambda: W.long_context(131072, device="cuda"),
+    "gqa": lambda: W.batched_gqa(device="cuda"),
+    "tiny_d64": lambda: W.tiny(device="cuda"),
+    "ragged_d192": lambda: W.ragged(192, device="cuda"),
+    "spec4_causal": lambda: W.multi_token(4, device="cuda"),
+    "page1_f16": lambda: W.make(3, 1, 8, 2, 128, 1, [700, 64, 2050], dtype="f16", device="cuda", seed=5),
+    "page4_rows32": lambda: W.make(2, 2, 32, 2, 64, 4, [3000, 4500], dtype="bf16", causal=True, device="cuda",
+                                   seed=6),
+    "page256_nhd": lambda: W.make(2, 1, 16, 4, 128, 256, [20000, 9000], dtype="bf16", layout="nhd", device="cuda",
+                                  seed=7),
+    "many_sequences": lambda: W.make(40, 1, 8, 1, 128, 16, list(range(100, 40 * 997, 997)), dtype="bf16",
+                                     device="cuda", seed=8),
+}
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_persistent_and_grid_kernels_agree_bitwise(case):
+    w = CASES[case]()
+    pd = fd.PagedDecode(w.seq_lens, w.q_len, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
+                        w.causal, device="cuda")
+    table = torch.as_tensor(w.page_table, device="cuda")
+    lens = torch.as_tensor(w.seq_lens, device="cuda")
+    assert w.q.data_ptr() % 16 == 0
+    first = _run(pd, w, w.q, table, lens)
+    qm = _misaligned_copy(w.q)
+    grid = _run(pd, w, qm, table, lens)
+    torch.cuda.synchronize()
+    assert pd.device_errors() == 0
+    assert torch.equal(first[0], grid[0]) and torch.equal(first[1], grid[1]), "persistent != one CTA per item"
+    # the persistent kernel again, several times: the counter must stay in step
+    for _ in range(5):
+        again = _run(pd, w, w.q, table, lens)
+        assert torch.equal(first[0], again[0]) and torch.equal(first[1], again[1])
+    torch.cuda.synchronize()
+    assert pd.device_errors() == 0
+
+
+@pytest.mark.parametrize("case", ["long_131072", "ragged_d192", "page1_f16", "many_sequences"])
+def test_persistent_kernel_matches_the_oracle(case):
+    w = CASES[case]()
+    pd = fd.PagedDecode(w.seq_lens, w.q_len, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
+                        w.causal, device="cuda")
+    info = pd.info
+    assert info["path"] == fd.FDEC_PATH_MMA
+    table = torch.as_tensor(w.page_table, device="cuda")
+    lens = torch.as_tensor(w.seq_lens, device="cuda")
+    out, lse = _run(pd, w, w.q, table, lens)
+    torch.cuda.synchronize()
+    assert pd.device_errors() == 0
+    wc = w.to("cpu")
+    rows = None
+    if case == "ragged_d192":  # a sample of output rows: two query heads of every sequence
+        rows = [b * w.num_qo_heads + h for b in range(w.batch) for h in (0, w.num_qo_heads - 1)]
+    ref_o, ref_l = oracle_run(wc, rows=rows)
+    if rows is None:
+        assert_parity(out.cpu(), lse.cpu(), ref_o, ref_l, case)
+    else:
+        idx = torch.as_tensor(np.asarray(rows, dtype=np.int64))
+        assert_parity(out.reshape(-1, w.head_dim).cpu()[idx], lse.reshape(-1).cpu()[idx], ref_o, ref_l, case)
+
+
+def test_run_time_lengths_below_capacity_and_empty_sequences():
+    # capacities fix the units; shorter run-time lengths leave some units empty
+    w = W.make(4, 1, 16, 2, 128, 16, [9000, 7000, 300, 5000], dtype="bf16", device="cuda", seed=12)
+    pd = fd.PagedDecode(w.seq_lens, 1, 16, 16, 2, 128, "bf16", device="cuda")
+    table = torch.as_tensor(w.page_table, device="cuda")
+    wc = w.to("cpu")
+    for run_lens in ([9000, 7000, 300, 5000], [4100, 0, 299, 64], [1, 6999, 0, 0]):
+        lens = torch.as_tensor(np.asarray(run_lens, dtype=np.int32), device="cuda")
+        out, lse = _run(pd, w, w.q, table, lens)
+        grid = _run(pd, w, _misaligned_copy(w.q), table, lens)
+        torch.cuda.synchronize()
+        assert pd.device_errors() == 0
+        assert torch.equal(out, grid[0]) and torch.equal(lse, grid[1])
+        ref_o, ref_l = oracle_run(wc, seq_lens=np.asarray(run_lens, dtype=np.int32))
+        assert_parity(out.cpu(), lse.cpu(), ref_o, ref_l, str(run_lens))
