@@ -82,6 +82,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     }
 }
 
+// Wait for the phase with the given parity to complete by polling (try_wait
+// without a suspend-time hint); false after kWaitLimitNs.  For waits that must
+// end as soon as the phase completes: measured on the persistent split kernel's
+// consumers, a suspended wait resumed late enough to cost 2-10 us per call on
+// multi-block decodes.
+__device__ __forceinline__ bool mbar_wait_polling(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        for (int k = 0; k < 64; ++k)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
 // 1-D bulk copy global -> shared (TMA), completion counted in bytes on `bar`.
 // dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -100,6 +114,23 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int 
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+// The K or V rows of one page run: a 5-D tiled TMA load over a pool map of dims
+// (128 bytes of a row, slot, 128-byte region, KV head, page) (see encode_kv_map).
+// When the box spans a whole stage's token rows, its region extent is every region
+// of the row and one instruction lands [region][row][128 B] (region-major,
+// 128B-swizzled), the stage layout; shorter boxes (pages smaller than a stage)
+// take one region each (`region`), placed by the caller.  A TMA instruction costs
+// ~50-60 ns of issue time whatever its size (measured on sm_103a), hence the
+// widest box the page size allows.  Completion is counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_kv_box(uint32_t dst, const void* tmap, int slot, int region, int kvh, int page,
+                                                uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(slot), "r"(region), "r"(kvh), "r"(page), "r"(bar)
         : "memory");
 }
 

@@ -143,7 +143,6 @@ struct fdec_plan_s {
     fdec_kv_desc map_k{}, map_v{};
     CUtensorMap tmap_k{};
     CUtensorMap tmap_v{};
-    int k_pos[3] = {1, 2, 3}, v_pos[3] = {1, 2, 3};
 };
 
 namespace {
@@ -186,8 +185,10 @@ int choose_blocks_per_split(const std::vector<int>& nblocks, int copies, int slo
     long long total = 0;
     for (int nb : nblocks) total += std::max(nb, 1);
     // Cost model in units of one 64-token block streamed by one CTA slot: the
-    // LPT makespan of the items, a fixed start-up cost per item, the extra
-    // reduction launch when any sequence is split, and the partials' traffic.
+    // LPT makespan of the items, a fixed cost per item (a CTA's start-up and
+    // epilogue, or a persistent CTA's unit switch: both measured at a few blocks'
+    // worth), the extra reduction launch when any sequence is split, and the
+    // partials' traffic.
     const double per_item = 2.0;
     const double reduce_cost = 4.0;
     std::vector<int> cands;
@@ -255,34 +256,35 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// A 4-D tensor map over one K or V pool: dims (head_dim, and the slot, head and
-// page dims ordered by increasing stride), box = 128 bytes of a row (64 16-bit
-// elements or 128 E4M3 codes; eb = element bytes) x box_rows slots, 128-byte
-// swizzle.  pos[role] receives the coordinate position of slot (0), head (1), page (2).
+// A 5-D tensor map over one K or V pool, dims (128 bytes of a row: 64 16-bit
+// elements or 128 E4M3 codes; eb = element bytes), slot, 128-byte region of the
+// row, KV head, page), 128-byte swizzle; box (128 bytes, box_rows slots, R, 1, 1)
+// with R = every region when a box spans a whole stage (box_rows == the stage's
+// token rows), else 1.  With the region dim after the slot dim a whole-stage box
+// lands region-major in shared memory, [region][slot][128 B], the stage layout
+// every split kernel reads.  The strides need not increase with the dim index (the
+// region stride is 128 bytes, the slot stride a whole row); dims of one index take
+// any stride.
 fdec_status encode_kv_map(CUtensorMap* map, const fdec_kv_desc& d, int head_dim, int page_size, int hk,
-                          int box_rows, int pos[3], int eb) {
+                          int box_rows, int stage_rows, int eb) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr) return fail(FDEC_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    struct Dim {
-        uint64_t size, stride;
-        int role;
-    } dims[3] = {{static_cast<uint64_t>(page_size), static_cast<uint64_t>(d.stride_token) * eb, 0},
-                 {static_cast<uint64_t>(hk), static_cast<uint64_t>(d.stride_head) * eb, 1},
-                 {static_cast<uint64_t>(d.num_pages), static_cast<uint64_t>(d.stride_page) * eb, 2}};
-    for (Dim& x : dims)
-        if (x.size == 1 && x.stride == 0) x.stride = 16;  // any stride works for a single index
-    std::stable_sort(dims, dims + 3, [](const Dim& a, const Dim& b) { return a.stride < b.stride; });
-    cuuint64_t gdim[4] = {static_cast<cuuint64_t>(head_dim), dims[0].size, dims[1].size, dims[2].size};
-    cuuint64_t gstride[3] = {dims[0].stride, dims[1].stride, dims[2].stride};
-    cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), 1, 1, 1};
-    cuuint32_t estride[4] = {1, 1, 1, 1};
-    for (int i = 0; i < 3; ++i) {
-        pos[dims[i].role] = i + 1;
-        if (dims[i].role == 0) box[i + 1] = static_cast<cuuint32_t>(box_rows);
-    }
-    CUresult r = enc(map, eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(d.base), gdim, gstride, box, estride,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const int regions = head_dim * eb / 128;
+    auto stride_of = [](uint64_t size, int64_t stride_bytes) -> cuuint64_t {
+        return (size == 1 && stride_bytes == 0) ? 16 : static_cast<cuuint64_t>(stride_bytes);
+    };
+    cuuint64_t gdim[5] = {static_cast<cuuint64_t>(128 / eb), static_cast<cuuint64_t>(page_size),
+                          static_cast<cuuint64_t>(regions), static_cast<cuuint64_t>(hk),
+                          static_cast<cuuint64_t>(d.num_pages)};
+    cuuint64_t gstride[4] = {stride_of(page_size, d.stride_token * eb), 128,
+                             stride_of(hk, d.stride_head * eb), stride_of(d.num_pages, d.stride_page * eb)};
+    if (regions == 1) gstride[1] = 16;  // a single region: any stride
+    cuuint32_t box[5] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(box_rows),
+                         static_cast<cuuint32_t>(box_rows == stage_rows ? regions : 1), 1, 1};
+    cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(map, eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 5,
+                     const_cast<void*>(d.base), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(FDEC_ERR_LAYOUT, "cuTensorMapEncodeTiled rejected the K/V layout (error " + std::to_string(r) + ")");
     return FDEC_OK;
@@ -437,40 +439,23 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
                                                  : choose_blocks_per_split(nblocks, copies, slots, partial_cost);
     const int C = p->blocks_per_split;
 
-    // Work items and level-0 partial slots.  Uniform runs of C blocks; or, for the
-    // persistent kernel with an automatic plan, a first wave and a dynamic tail: a
-    // sequence the uniform plan cuts into ns items gets ns big items of 80 % of the
-    // even share (taken first, one per resident CTA slot) and the rest in small items
-    // of about C / 8 blocks, taken by whichever CTA frees up first (per-CTA stream
-    // rates differ by about +-12 % under saturation, so the tail balances them).
+    // Work items and level-0 partial slots: runs of C blocks.
     p->splits.resize(batch);
     std::vector<int> slot_base(batch, -1);
     size_t next_slot = 0;
-    const bool wave_and_tail = p->persistent && o.blocks_per_split == 0 && C >= 4;
     for (int b = 0; b < batch; ++b) {
-        const int nb = nblocks[b];
-        const int ns = (nb + C - 1) / C;
-        std::vector<std::pair<int, int>> runs;  // [begin, end) in blocks
-        if (wave_and_tail && ns > 1) {
-            const int big = std::max(1, static_cast<int>(0.8 * nb / ns));
-            const int small = std::max(1, (C + 7) / 8);
-            for (int k = 0; k < ns; ++k) runs.emplace_back(k * big, (k + 1) * big);
-            for (int x = ns * big; x < nb; x += small) runs.emplace_back(x, std::min(x + small, nb));
-        } else {
-            for (int k = 0; k < ns; ++k) runs.emplace_back(k * C, std::min((k + 1) * C, nb));
-        }
-        const int n = static_cast<int>(runs.size());
-        p->splits[b] = n;
-        if (n > 1) {
+        const int ns = (nblocks[b] + C - 1) / C;
+        p->splits[b] = ns;
+        if (ns > 1) {
             slot_base[b] = static_cast<int>(next_slot);
-            next_slot += n;
+            next_slot += ns;
         }
-        for (int k = 0; k < n; ++k) {
+        for (int k = 0; k < ns; ++k) {
             WorkItem it;
             it.seq = b;
-            it.block_begin = runs[k].first;
-            it.block_end = runs[k].second;
-            it.slot = n > 1 ? slot_base[b] + k : -1;
+            it.block_begin = k * C;
+            it.block_end = std::min((k + 1) * C, nblocks[b]);
+            it.slot = ns > 1 ? slot_base[b] + k : -1;
             p->items.push_back(it);
         }
     }
@@ -669,10 +654,11 @@ fdec_status fdec_run_scaled(fdec_plan_t p, const void* q, int64_t q_stride_tok, 
         return fail(FDEC_ERR_WORKSPACE, "workspace is not the buffer this plan was uploaded to");
 
     if (p->page_size >= 8 && !(p->maps_valid && same_desc(p->map_k, k) && same_desc(p->map_v, v))) {
-        const int box_rows = std::min(p->page_size, p->path == FDEC_PATH_TC ? kTcStageTokens : kStageTokens);
-        fdec_status st = encode_kv_map(&p->tmap_k, k, p->head_dim, p->page_size, p->hk, box_rows, p->k_pos, eb);
+        const int stage_rows = p->path == FDEC_PATH_TC ? kTcStageTokens : kStageTokens;
+        const int box_rows = std::min(p->page_size, stage_rows);
+        fdec_status st = encode_kv_map(&p->tmap_k, k, p->head_dim, p->page_size, p->hk, box_rows, stage_rows, eb);
         if (st == FDEC_OK)
-            st = encode_kv_map(&p->tmap_v, v, p->head_dim, p->page_size, p->hk, box_rows, p->v_pos, eb);
+            st = encode_kv_map(&p->tmap_v, v, p->head_dim, p->page_size, p->hk, box_rows, stage_rows, eb);
         if (st != FDEC_OK) {
             p->maps_valid = false;
             return st;
@@ -715,14 +701,11 @@ fdec_status fdec_run_scaled(fdec_plan_t p, const void* q, int64_t q_stride_tok, 
     sp.causal = p->causal;
     sp.scale_log2 = scale * k_scale * 1.4426950408889634074f;
     sp.v_scale = v_scale;
-    sp.k_pos_slot = p->k_pos[0];
-    sp.k_pos_head = p->k_pos[1];
-    sp.k_pos_page = p->k_pos[2];
-    sp.v_pos_slot = p->v_pos[0];
-    sp.v_pos_head = p->v_pos[1];
-    sp.v_pos_page = p->v_pos[2];
     sp.n_units = p->n_units;
     sp.ticket = reinterpret_cast<unsigned long long*>(ws + p->off_ticket);
+    sp.seq1_bps = p->batch == 1 ? p->blocks_per_split : 0;
+    sp.seq1_blocks = std::max(1, (p->capacity[0] + kBlockTokens - 1) / kBlockTokens);
+    sp.seq1_capacity = p->capacity[0];
 
     // The persistent kernel copies each unit's query rows with 16-byte bulk copies.
     const bool q_rows_aligned = reinterpret_cast<uintptr_t>(q) % 16 == 0 && (q_stride_tok * 2) % 16 == 0 &&

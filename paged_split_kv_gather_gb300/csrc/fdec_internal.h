@@ -56,14 +56,14 @@ struct SplitParams {
     int q_len, hq, hk, group, rows, page_shift, causal;
     float scale_log2;          // scale * k_scale * log2(e): logits are kept in log2 units
     float v_scale;             // value scale (quantised caches; 1 otherwise), applied to O
-    // Coordinate position (1..3) of the slot, head and page dims in each tensor map.
-    int k_pos_slot, k_pos_head, k_pos_page;
-    int v_pos_slot, v_pos_head, v_pos_page;
     // Persistent split kernel: work units = items x KV heads x row groups, in item
     // order; CTA c starts with unit c and takes the units past the grid from the
     // ticket counter (advanced by exactly n_units per launch).
     int n_units;
     unsigned long long* ticket;
+    // One sequence (batch 1): its work items are runs of seq1_bps blocks in order, so
+    // a unit's item follows from its index with no table read (0: read the table).
+    int seq1_bps, seq1_blocks, seq1_capacity;
 };
 
 struct ReduceParams {

@@ -183,23 +183,17 @@ __device__ __forceinline__ void produce_stages(const SplitParams& p, const CUten
             const unsigned vmask = __ballot_sync(0xffffffffu, valid);
             const uint32_t fbar = smem_addr(&full[i % (2 * S)]);
             if (lane == 0) mbar_arrive_expect_tx(fbar, static_cast<uint32_t>(__popc(vmask)) * box_bytes);
-            for (int j = 0; j < NB; ++j) {
-                const int page = __shfl_sync(0xffffffffu, my_page, j);
-                if (lane == 0 && ((vmask >> j) & 1u)) {
-                    const int slot0 = (tok_begin + (box0 + j) * BR) & page_mask;
-                    uint8_t* kdst = stages + s * G::STAGE_BYTES + j * BR * 128;
-                    // coordinate n (1..3) of each map: whichever of slot, head, page sits there
-                    auto coord = [&](int n, int ps, int ph) { return n == ps ? slot0 : (n == ph ? kvh : page); };
-                    const int k1 = coord(1, p.k_pos_slot, p.k_pos_head), k2 = coord(2, p.k_pos_slot, p.k_pos_head),
-                              k3 = coord(3, p.k_pos_slot, p.k_pos_head);
-                    const int v1 = coord(1, p.v_pos_slot, p.v_pos_head), v2 = coord(2, p.v_pos_slot, p.v_pos_head),
-                              v3 = coord(3, p.v_pos_slot, p.v_pos_head);
-#pragma unroll
+            __syncwarp();
+            if (valid) {  // lane j issues box j (every region in one instruction when the box spans the stage)
+                const int slot0 = (tok_begin + (box0 + lane) * BR) & page_mask;
+                const uint32_t kdst = smem_addr(stages + s * G::STAGE_BYTES + lane * BR * 128);
+                if (NB == 1) {
+                    tma_load_kv_box(kdst, tmk, slot0, 0, kvh, my_page, fbar);
+                    tma_load_kv_box(kdst + G::HALF_BYTES, tmv, slot0, 0, kvh, my_page, fbar);
+                } else {
                     for (int r = 0; r < G::REGIONS; ++r) {
-                        // x = the region's first element: 128 bytes per region, a multiple of 16 bytes
-                        tma_load_4d(smem_addr(kdst + r * G::REGION_BYTES), tmk, r * (128 / EB), k1, k2, k3, fbar);
-                        tma_load_4d(smem_addr(kdst + G::HALF_BYTES + r * G::REGION_BYTES), tmv, r * (128 / EB), v1,
-                                    v2, v3, fbar);
+                        tma_load_kv_box(kdst + r * G::REGION_BYTES, tmk, slot0, r, kvh, my_page, fbar);
+                        tma_load_kv_box(kdst + G::HALF_BYTES + r * G::REGION_BYTES, tmv, slot0, r, kvh, my_page, fbar);
                     }
                 }
             }

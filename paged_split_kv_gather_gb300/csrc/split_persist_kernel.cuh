@@ -30,8 +30,8 @@
 //     goes to consumer warp j mod 3; the unit's query rows (16-byte aligned
 //     rows, one bulk copy each) land with its first stage in one of two query
 //     buffers; a tag per ring slot names the unit buffer and j (2 j + buffer).  The next unit's
-//     ticket, work item, length and first page ids are fetched while the current
-//     unit's stages are issued.
+//     ticket, work item, length and first page ids are fetched while the last
+//     three stages of the current unit are issued.
 //   - a consumer warp resets its state at its first stage of a unit and, at its
 //     last, writes its (m, l, O) into that stage's slot (kept, not released) and
 //     counts itself in; the third warp to arrive merges the three states, writes
@@ -43,6 +43,23 @@
 #include "split_mma_kernel.cuh"
 
 namespace fdec {
+
+// Consumer side of stage i (the parity argument of wait_stage).  poll: wait by
+// polling rather than suspended.  Measured on sm_103a: with pages of fewer than 32
+// tokens (a stage lands as several TMA boxes) suspended consumers resumed late,
+// 10 us of 47 on a speculative-decode batch, and polling wins; with whole-stage
+// boxes suspending is better (polling warps take issue slots from the producers:
+// +1.5 us at 131072 tokens).
+template <int S>
+__device__ __forceinline__ bool wait_stage_mode(uint64_t* full, int i, bool poll) {
+    bool got = true;
+    if ((threadIdx.x & 31) == 0) {
+        const uint32_t bar = smem_addr(&full[i % (2 * S)]);
+        const uint32_t parity = (i / (2 * S)) & 1;
+        got = poll ? mbar_wait_polling(bar, parity) : mbar_wait_bounded(bar, parity);
+    }
+    return __shfl_sync(0xffffffffu, got, 0) != 0;
+}
 
 // What the producer tells the consumers about a unit (with its first stage).
 struct UnitMeta {
@@ -81,11 +98,52 @@ struct PersistLayout {
     static_assert(S >= NP + 1, "stage ring too small");
 };
 
-// The producer warp of the persistent kernel.
+// A work unit as the producer sees it: the unit index, its work item, the run-time
+// length and capacity of its sequence, and this lane's page ids of box groups 0
+// and 1 (TMA mode).
+struct PUnit {
+    int unit;  // -1: none
+    int4 it;   // seq, block_begin, block_end, slot
+    int L0, cap;
+    int pid0, pid1;
+};
+
+__device__ __forceinline__ void punit_load_item(const SplitParams& p, PUnit& u, int upi) {
+    const int idx = u.unit / upi;
+    if (p.seq1_bps > 0) {
+        const int ns = (p.seq1_blocks + p.seq1_bps - 1) / p.seq1_bps;
+        u.it = make_int4(0, idx * p.seq1_bps, min((idx + 1) * p.seq1_bps, p.seq1_blocks), ns > 1 ? idx : -1);
+    } else {
+        u.it = __ldg(reinterpret_cast<const int4*>(p.items) + idx);
+    }
+}
+
+// Page id of TMA box n (BR token rows) of the unit, or -1 past its planned blocks.
+__device__ __forceinline__ int punit_box_page(const SplitParams& p, const PUnit& u, int n, int BR) {
+    const int t = u.it.y * kBlockTokens + n * BR;
+    const int32_t* pt = p.page_table + static_cast<int64_t>(u.it.x) * p.pt_stride;
+    return (t < u.it.z * kBlockTokens && (t >> p.page_shift) < p.pt_stride) ? __ldg(pt + (t >> p.page_shift)) : -1;
+}
+
+// Length and first page ids (before the length is known: bounded by the item's
+// planned blocks and the table row, so every read is in bounds).
+__device__ __forceinline__ void punit_load_lens_pages(const SplitParams& p, PUnit& u, int lane, int BR,
+                                                      bool tma_mode) {
+    u.L0 = __ldg(p.seq_lens + u.it.x);
+    u.cap = p.seq1_bps > 0 ? p.seq1_capacity : __ldg(p.capacity + u.it.x);
+    if (tma_mode) {
+        u.pid0 = punit_box_page(p, u, lane, BR);
+        u.pid1 = punit_box_page(p, u, 32 + lane, BR);
+    }
+}
+
+// The producer warp of the persistent kernel.  `first`: the CTA's first unit, its
+// loads issued before the CTA's set-up so that they overlap it.
 template <int D, int S, int NP>
 __device__ __forceinline__ void produce_units(const SplitParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                               uint64_t* full, uint64_t* empty, uint64_t* qfree, int* tag,
-                                              UnitMeta* um, uint16_t* qbuf, uint8_t* stages, bool tma_mode) {
+                                              UnitMeta* um, uint16_t* qbuf, uint8_t* stages, bool tma_mode,
+                                              PUnit cur) {
     using G = StageGeom<D>;
     constexpr int RC = 16;
     constexpr int TOK = kStageTokens;
@@ -100,31 +158,9 @@ __device__ __forceinline__ void produce_units(const SplitParams& p, const CUtens
     const uint32_t box_bytes = static_cast<uint32_t>(BR) * 2u * G::ROW_BYTES;  // K and V
     const uint32_t q_row_bytes = D * 2;
 
-    struct Unit {
-        int unit;      // -1: none
-        int4 it;       // seq, block_begin, block_end, slot
-        int L0, cap;
-        int pid0, pid1;  // this lane's page ids of box groups 0 and 1 (TMA mode)
-    };
-    auto load_item = [&](Unit& u) {
-        u.it = __ldg(reinterpret_cast<const int4*>(p.items) + u.unit / upi);
-    };
-    auto box_page = [&](const Unit& u, int n) -> int {
-        const int t = u.it.y * kBlockTokens + n * BR;
-        const int32_t* pt = p.page_table + static_cast<int64_t>(u.it.x) * p.pt_stride;
-        return (t < u.it.z * kBlockTokens && (t >> p.page_shift) < p.pt_stride) ? __ldg(pt + (t >> p.page_shift))
-                                                                                 : -1;
-    };
-    // Length and first page ids (before the length is known: bounded by the item's
-    // planned blocks and the table row, so every read is in bounds).
-    auto load_lens_pages = [&](Unit& u) {
-        u.L0 = __ldg(p.seq_lens + u.it.x);
-        u.cap = __ldg(p.capacity + u.it.x);
-        if (tma_mode) {
-            u.pid0 = box_page(u, lane);
-            u.pid1 = box_page(u, 32 + lane);
-        }
-    };
+    auto load_item = [&](PUnit& u) { punit_load_item(p, u, upi); };
+    auto box_page = [&](const PUnit& u, int n) -> int { return punit_box_page(p, u, n, BR); };
+    auto load_lens_pages = [&](PUnit& u) { punit_load_lens_pages(p, u, lane, BR, tma_mode); };
     // Tickets: lane 0 takes one; resolved to a unit (or -1: no unit left).
     unsigned long long ticket = 0;
     auto take = [&]() {
@@ -140,11 +176,7 @@ __device__ __forceinline__ void produce_units(const SplitParams& p, const CUtens
     int i = 0;  // ring stages issued
     int k = 0;  // units issued by this CTA
     bool pending = false;  // a ticket taken and not resolved
-    Unit cur;
-    cur.unit = blockIdx.x;
-    load_item(cur);
-    load_lens_pages(cur);
-    Unit nxt;
+    PUnit nxt;
     nxt.unit = -1;
     // Look-ahead of the next unit, one step per issued stage over the last three stages
     // of the current one: 0 nothing yet, 1 ticket taken, 2 unit known and its work item
@@ -223,7 +255,9 @@ __device__ __forceinline__ void produce_units(const SplitParams& p, const CUtens
         uint16_t* q_dst = qbuf + cb * RC * D;
         for (int j = 0; j < n_pad; ++j, ++i) {
             // The next unit is taken only near the end of this one (the producer runs about
-            // S stages ahead of the consumers), so that a CTA that streams slowly takes fewer.
+            // S stages ahead of the consumers), so that a CTA that streams slowly takes
+            // fewer.  (Taking it as a unit starts was measured slower on a ragged batch,
+            // 382 against 283 us: the assignment then runs one unit ahead of the work.)
             if (j >= n_pad - 3 && ahead < 3) advance();
             const int s = i % S;
             if (!wait_slot(i)) {
@@ -269,21 +303,16 @@ __device__ __forceinline__ void produce_units(const SplitParams& p, const CUtens
                                           static_cast<int64_t>(h) * p.q_stride_head;
                     bulk_g2s(smem_addr(q_dst + lane * D), src, q_row_bytes, fbar);
                 }
-                for (int jb = 0; jb < NB; ++jb) {
-                    const int page = __shfl_sync(0xffffffffu, my_page, jb);
-                    if (lane == 0 && ((vmask >> jb) & 1u)) {
-                        const int slot0 = (tok_begin + (box0 + jb) * BR) & page_mask;
-                        uint8_t* kdst = sbase + jb * BR * 128;
-                        auto coord = [&](int n, int ps, int ph) { return n == ps ? slot0 : (n == ph ? kvh : page); };
-                        const int k1 = coord(1, p.k_pos_slot, p.k_pos_head), k2 = coord(2, p.k_pos_slot, p.k_pos_head),
-                                  k3 = coord(3, p.k_pos_slot, p.k_pos_head);
-                        const int v1 = coord(1, p.v_pos_slot, p.v_pos_head), v2 = coord(2, p.v_pos_slot, p.v_pos_head),
-                                  v3 = coord(3, p.v_pos_slot, p.v_pos_head);
-#pragma unroll
+                if (valid) {  // lane j issues box j (every region in one instruction when the box spans the stage)
+                    const int slot0 = (tok_begin + (box0 + lane) * BR) & page_mask;
+                    const uint32_t kdst = smem_addr(sbase + lane * BR * 128);
+                    if (NB == 1) {
+                        tma_load_kv_box(kdst, tmk, slot0, 0, kvh, my_page, fbar);
+                        tma_load_kv_box(kdst + G::HALF_BYTES, tmv, slot0, 0, kvh, my_page, fbar);
+                    } else {
                         for (int r = 0; r < G::REGIONS; ++r) {
-                            tma_load_4d(smem_addr(kdst + r * G::REGION_BYTES), tmk, r * 64, k1, k2, k3, fbar);
-                            tma_load_4d(smem_addr(kdst + G::HALF_BYTES + r * G::REGION_BYTES), tmv, r * 64, v1, v2,
-                                        v3, fbar);
+                            tma_load_kv_box(kdst + r * G::REGION_BYTES, tmk, slot0, r, kvh, my_page, fbar);
+                            tma_load_kv_box(kdst + G::HALF_BYTES + r * G::REGION_BYTES, tmv, slot0, r, kvh, my_page, fbar);
                         }
                     }
                 }
@@ -375,57 +404,74 @@ __device__ __forceinline__ void produce_units(const SplitParams& p, const CUtens
 
 // Merge the NP consumer states of a unit (m, l per row in ml[NP][RC]; O rows in the
 // kept slots, [RC][O_STRIDE] floats each) and write the unit's partial or out / lse.
-// One warp; the arithmetic and its order are those of merge_and_store.
+// One warp: lane r first takes the statistics of row r (max, weights, sum), then the
+// lanes stride over (row, 4 columns) pairs with the row's values broadcast from its
+// lane.  The arithmetic and its order are those of merge_and_store.
 template <int D, int NP, int RC, int O_STRIDE>
 __device__ __forceinline__ void merge_unit(const SplitParams& p, const UnitMeta& u, const float2* ml,
                                            const float* const (&o_w)[NP], int lane) {
     constexpr float kLn2 = 0.69314718055994530942f;
-    for (int r = 0; r < RC; ++r) {
-        const int row = u.row0 + r;
-        if (row >= p.rows) break;
-        float M = -INFINITY;
+    constexpr int C4 = D / 4;
+    const int nrows = min(RC, p.rows - u.row0);
+    float M = -INFINITY, Ls = 0.f, e[NP];
 #pragma unroll
-        for (int w = 0; w < NP; ++w) M = fmaxf(M, ml[w * RC + r].x);
-        float e[NP];
-        float Ls = 0.f;
+    for (int w = 0; w < NP; ++w) e[w] = 0.f;
+    if (lane < nrows) {
 #pragma unroll
-        for (int w = 0; w < NP; ++w) {
-            e[w] = M != -INFINITY ? exp2_approx(ml[w * RC + r].x - M) : 0.f;
-            Ls += ml[w * RC + r].y * e[w];
+        for (int w = 0; w < NP; ++w) M = fmaxf(M, ml[w * RC + lane].x);
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NP; ++w) {
+                e[w] = exp2_approx(ml[w * RC + lane].x - M);
+                Ls += ml[w * RC + lane].y * e[w];
+            }
         }
-        if (M == -INFINITY) Ls = 0.f;
+        const int row = u.row0 + lane;
         const int qi = row / p.group;
         const int h = u.kvh * p.group + (row - qi * p.group);
-        const int64_t orow = static_cast<int64_t>(u.seq * p.q_len + qi) * p.hq + h;
-        const int64_t prow = (static_cast<int64_t>(u.slot) * p.hk + u.kvh) * p.rows + row;
-        for (int c4 = lane; c4 < D / 4; c4 += 32) {
-            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (M != -INFINITY) {
+        if (u.slot < 0) {
+            if (p.lse != nullptr)
+                p.lse[static_cast<int64_t>(u.seq * p.q_len + qi) * p.hq + h] =
+                    Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+        } else {
+            p.part_ml[(static_cast<int64_t>(u.slot) * p.hk + u.kvh) * p.rows + row] = make_float2(M, Ls);
+        }
+    }
+    const int total = nrows * C4;
+    for (int x0 = 0; x0 < total; x0 += 32) {
+        const int x = x0 + lane;
+        const int r = min(x, total - 1) / C4;
+        const float Mr = __shfl_sync(0xffffffffu, M, r);
+        const float Lr = __shfl_sync(0xffffffffu, Ls, r);
+        float er[NP];
 #pragma unroll
-                for (int w = 0; w < NP; ++w) {
-                    const float4 v = *reinterpret_cast<const float4*>(o_w[w] + r * O_STRIDE + 4 * c4);
-                    O.x += v.x * e[w];
-                    O.y += v.y * e[w];
-                    O.z += v.z * e[w];
-                    O.w += v.w * e[w];
-                }
-            }
-            if (u.slot < 0) {
-                const float4 res = Ls > 0.f ? make_float4(O.x / Ls * p.v_scale, O.y / Ls * p.v_scale,
-                                                          O.z / Ls * p.v_scale, O.w / Ls * p.v_scale)
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4*>(p.out + orow * D + 4 * c4) = res;
-            } else {
-                *reinterpret_cast<float4*>(p.part_o + prow * D + 4 * c4) =
-                    make_float4(O.x * p.v_scale, O.y * p.v_scale, O.z * p.v_scale, O.w * p.v_scale);
+        for (int w = 0; w < NP; ++w) er[w] = __shfl_sync(0xffffffffu, e[w], r);
+        if (x >= total) continue;
+        const int c4 = x - r * C4;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (Mr != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NP; ++w) {
+                const float4 v = *reinterpret_cast<const float4*>(o_w[w] + r * O_STRIDE + 4 * c4);
+                O.x += v.x * er[w];
+                O.y += v.y * er[w];
+                O.z += v.z * er[w];
+                O.w += v.w * er[w];
             }
         }
-        if (lane == 0) {
-            if (u.slot < 0) {
-                if (p.lse != nullptr) p.lse[orow] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
-            } else {
-                p.part_ml[prow] = make_float2(M, Ls);
-            }
+        const int row = u.row0 + r;
+        const int qi = row / p.group;
+        const int h = u.kvh * p.group + (row - qi * p.group);
+        if (u.slot < 0) {
+            const int64_t orow = static_cast<int64_t>(u.seq * p.q_len + qi) * p.hq + h;
+            *reinterpret_cast<float4*>(p.out + orow * D + 4 * c4) =
+                Lr > 0.f ? make_float4(O.x / Lr * p.v_scale, O.y / Lr * p.v_scale, O.z / Lr * p.v_scale,
+                                       O.w / Lr * p.v_scale)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            const int64_t prow = (static_cast<int64_t>(u.slot) * p.hk + u.kvh) * p.rows + row;
+            *reinterpret_cast<float4*>(p.part_o + prow * D + 4 * c4) =
+                make_float4(O.x * p.v_scale, O.y * p.v_scale, O.z * p.v_scale, O.w * p.v_scale);
         }
     }
 }
@@ -462,6 +508,15 @@ split_mma_persist_kernel(const __grid_constant__ SplitParams p, const __grid_con
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const bool tma_mode = p.page_shift >= 3;
+    // The producer's first unit: its work item, length and page ids are requested now,
+    // before the set-up below, so that those round trips overlap it.
+    PUnit first;
+    first.unit = -1;
+    if (warp == NP) {
+        first.unit = blockIdx.x;
+        punit_load_item(p, first, p.hk * ((p.rows + RC - 1) / RC));
+        punit_load_lens_pages(p, first, lane, tma_mode ? min(1 << p.page_shift, kStageTokens) : 1, tma_mode);
+    }
     if (threadIdx.x == 0) {
         // Stage barriers: TMA stages complete on one expect-tx arrival; small-page stages
         // on the 32 cp.async arrivals of the producer lanes plus one plain arrival of lane
@@ -487,7 +542,7 @@ split_mma_persist_kernel(const __grid_constant__ SplitParams p, const __grid_con
             prefetch_tmap(&tmk);
             prefetch_tmap(&tmv);
         }
-        produce_units<D, S, NP>(p, &tmk, &tmv, full, empty, qfree, tag, um, qbuf, stages, tma_mode);
+        produce_units<D, S, NP>(p, &tmk, &tmv, full, empty, qfree, tag, um, qbuf, stages, tma_mode, first);
         return;
     }
 
@@ -495,11 +550,12 @@ split_mma_persist_kernel(const __grid_constant__ SplitParams p, const __grid_con
     W cw(lane);
     const int g = cw.g, tq = cw.tq;
     const float sl[2] = {p.scale_log2, p.scale_log2};
+    const bool poll = p.page_shift < 5;  // stages of several boxes (see wait_stage_mode)
     int lim[2] = {0, 0};
     bool ok = true;
     for (int i = warp;; i += NP) {
         const int s = i % S;
-        if (!wait_stage<S>(full, i)) {
+        if (!wait_stage_mode<S>(full, i, poll)) {
             ok = false;
             break;
         }
@@ -512,7 +568,7 @@ split_mma_persist_kernel(const __grid_constant__ SplitParams p, const __grid_con
             // the unit's query rows land with its stage 0 (stage i - j); that barrier is
             // still in this phase: its next use, stage i - j + 2S, cannot be issued before
             // this warp releases stage i
-            if (j > 0 && !wait_stage<S>(full, i - j)) {
+            if (j > 0 && !wait_stage_mode<S>(full, i - j, poll)) {
                 ok = false;
                 break;
             }

@@ -320,15 +320,7 @@ def test_plan_invariants_hold_for_random_batches():
         assert info["path"] == want_path
         # the persistent kernel (16-bit caches, head_dim 64/128/192 on the 16-row path)
         persistent = want_path == fd.FDEC_PATH_MMA and not kv8 and d in (64, 128, 192)
-        ns = -(-nb // C)
-        if persistent and not bps and C >= 4:
-            # ns big items of 80 % of the even share, then small items of ceil(C / 8) blocks
-            big = np.maximum(1, (0.8 * nb / ns).astype(np.int64))
-            small = max(1, (C + 7) // 8)
-            want = np.where(ns > 1, ns + -(-(nb - ns * big) // small), ns)
-        else:
-            want = ns
-        assert np.array_equal(splits, want)
+        assert np.array_equal(splits, -(-nb // C))
         assert info["num_items"] == int(splits.sum()) and info["max_splits"] == int(splits.max())
         assert info["row_groups"] == -(-rows // info["rows_per_group"])
         units = info["num_items"] * hk * info["row_groups"]
