@@ -366,12 +366,13 @@ def _config_points(dev, calls, hbm_peak):
 # The sources each profiled kernel is built from: a committed traffic figure
 # stands only while these files are unchanged.
 KERNEL_SOURCES = {
-    "split_mma_kernel": ["device_utils.cuh", "fdec_internal.h", "split_common.cuh", "split_mma_kernel.cuh",
-                         "split_mma.cu"],
+    "split_mma_persist_kernel": ["device_utils.cuh", "fdec_internal.h", "split_common.cuh", "split_mma_kernel.cuh",
+                                 "split_persist_kernel.cuh", "split_persist.cu"],
 }
+HEADLINE_KERNEL = "split_mma_persist_kernel"
 
 
-def _kernel_source_hash(kernel: str = "split_mma_kernel") -> str:
+def _kernel_source_hash(kernel: str = HEADLINE_KERNEL) -> str:
     csrc = os.path.join(ROOT, "paged_split_kv_gather_gb300", "csrc")
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
@@ -514,6 +515,32 @@ def _run_fdec(args):
             dist.destroy_process_group()
         return
 
+    if args.only_long:
+        # Flushed calls of one long-context length alone (profiling the decode kernel); not a bench line.
+        peak, _ = _peaks()
+        w = _make_inputs(args.only_long, dev)
+        pdl = fd.PagedDecode(w.seq_lens, 1, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
+                             device=dev)
+        tb = torch.as_tensor(w.page_table, device=dev)
+        ln = torch.as_tensor(w.seq_lens, device=dev)
+        o = torch.empty((1, 1, w.num_qo_heads, w.head_dim), device=dev)
+        l = torch.empty((1, 1, w.num_qo_heads), device=dev)
+
+        def run_long():
+            pdl.run(w.q, w.k, w.v, tb, ln, o, l, scale=w.scale)
+
+        for _ in range(3):
+            run_long()
+        med, mn = _time_calls(torch, run_long, args.sweep_calls, L2Flush(torch, dev))
+        if rank == 0:
+            gbs = w.kv_bytes / (med * 1e-6) / 1e9
+            print(json.dumps({f"long_context_L{args.only_long}": {
+                "us_per_call": round(med, 2), "us_min": round(mn, 2), "GB_per_s": round(gbs, 1),
+                "frac_of_peak": round(gbs / peak, 4), "plan": pdl.info}}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
     if args.only_dense:
         # The multi-token points alone (for profiling the tcgen05 kernel); not a bench line.
         peak, _ = _peaks()
@@ -535,6 +562,7 @@ def _run_fdec(args):
     pd = fd.PagedDecode(w.seq_lens, 1, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
                         device=dev)
     info = pd.info
+    assert info["path"] == fd.FDEC_PATH_MMA, info  # the persistent tensor-core split kernel (HEADLINE_KERNEL)
     kv_bytes = w.kv_bytes
 
     def step():
@@ -684,8 +712,7 @@ def _run_fdec(args):
             "config": _headline_config(world, kv_bytes),
             "plan": {k: info[k] for k in ("blocks_per_split", "num_split_ctas", "max_splits", "reduce_passes",
                                           "launches")},
-            "roofline": {"bound": "hbm", "kernel": ("split_mma_kernel<128,bf16>" if info["path"] == fd.FDEC_PATH_MMA
-                                                    else f"split_kernel<128,{info['rows_per_group']},bf16>"), "achieved": round(achieved, 1),
+            "roofline": {"bound": "hbm", "kernel": f"{HEADLINE_KERNEL}<128,bf16>", "achieved": round(achieved, 1),
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes,
                          "split_kernel_us": round(split_ms * 1e3, 2)},
@@ -883,6 +910,9 @@ def main():
     ap.add_argument("--only-dense", action="store_true",
                     help="run only the multi-token points and print them (profiling; no bench line)")
     ap.add_argument("--dense-q", type=int, nargs="+", default=[4, 8, 2048], help="q_len of the multi-token points")
+    ap.add_argument("--only-long", type=int, default=0, metavar="L",
+                    help="run only flushed calls of the long-context shape at L tokens and print them "
+                         "(profiling; no bench line)")
     ap.add_argument("--only-e4m3", action="store_true",
                     help="run only the E4M3 (fp8) long-context point and print it (profiling; no bench line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
