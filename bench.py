@@ -119,6 +119,48 @@ def _dense_query(dev, calls, hbm_peak, q_lens=(4, 8, 2048)):
             "flops": "4 x head_dim per visible (query head, query token, key token)", "points": res}
 
 
+def _crossover(dev, calls):
+    """16-row warp-level kernel against the tcgen05 kernel per head_dim and row count
+    (rows = q_len x group): batch 4, 32/8 heads, KV 8192 + q_len, causal, bf16, page 16.
+    The planner's AUTO rule takes tcgen05 above 16 rows for head_dim 64-256."""
+    import torch
+
+    import paged_split_kv_gather_gb300 as fd
+    from paged_split_kv_gather_gb300 import workloads as W
+
+    flush = L2Flush(torch, dev)
+    table_out = {}
+    for d in (64, 128, 192, 256, 512):
+        for q_len in (4, 8, 16):
+            rows = q_len * 4
+            w = W.make(4, q_len, 32, 8, d, 16, [8192 + q_len] * 4, dtype="bf16", causal=True, device=dev, seed=3)
+            tb = torch.as_tensor(w.page_table, device=dev)
+            ln = torch.as_tensor(w.seq_lens, device=dev)
+            out = torch.empty((4, q_len, 32, d), device=dev)
+            lse = torch.empty((4, q_len, 32), device=dev)
+            entry = {}
+            for name, path in (("mma", fd.FDEC_PATH_MMA), ("tcgen05", fd.FDEC_PATH_TC), ("auto", fd.FDEC_PATH_AUTO)):
+                if path == fd.FDEC_PATH_TC and d == 512:
+                    continue
+                pd = fd.PagedDecode(w.seq_lens, q_len, 16, 32, 8, d, "bf16", True, device=dev, path=path)
+
+                def run(pd=pd, w=w, tb=tb, ln=ln, out=out, lse=lse):
+                    pd.run(w.q, w.k, w.v, tb, ln, out, lse, scale=w.scale)
+
+                for _ in range(3):
+                    run()
+                med, _ = _time_calls(torch, run, calls, flush)
+                entry[name] = round(med, 2) if name != "auto" else ("tcgen05" if pd.info["path"] == fd.FDEC_PATH_TC
+                                                                   else "mma")
+                del pd
+            table_out[f"D{d}_rows{rows}"] = entry
+            del w, tb, ln, out, lse
+        torch.cuda.empty_cache()
+    del flush
+    return {"workload": "batch 4, 32/8 heads, KV 8192 + q_len, causal, bf16, page 16; us per flushed call",
+            "points": table_out}
+
+
 class L2Flush:
     """Evict the L2 between timed calls: write one buffer larger than the L2, then
     read another, so that the write-back of the dirty lines happens here, outside
@@ -686,6 +728,7 @@ def _run_fdec(args):
     dense = None
     if not args.no_dense:
         dense = _dense_query(dev, args.sweep_calls, peak, tuple(args.dense_q))
+        dense["crossover"] = _crossover(dev, max(5, args.sweep_calls // 5))
 
     clocks.__exit__(None, None, None)
 

@@ -227,7 +227,8 @@ cudaError_t dispatch_split(const fdec_plan_s* p, const SplitParams& sp, dim3 gri
     if (persist)
         return launch_split_mma_persist(sp, tk, tv, p->head_dim, bf16, dim3(static_cast<unsigned>(p->persist_grid), 1, 1),
                                         stream, launch);
-    if (p->path == FDEC_PATH_TC) return launch_split_tc(sp, tk, tv, p->rc / kTcRows, bf16, grid, stream, launch);
+    if (p->path == FDEC_PATH_TC)
+        return launch_split_tc(sp, tk, tv, p->rc / kTcRows, p->head_dim, bf16, grid, stream, launch);
     if (p->path == FDEC_PATH_MMA)
         return launch_split_mma(sp, tk, tv, p->head_dim, bf16, p->kv8, grid, stream, launch);
     switch (p->head_dim) {
@@ -348,11 +349,11 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
     if (kv8 && o.path != FDEC_PATH_AUTO && o.path != FDEC_PATH_MMA)
         return fail(FDEC_ERR_UNSUPPORTED, "E4M3 caches run on the MMA path only");
     const bool mma_ok = head_dim_supported(head_dim);  // every supported head_dim
-    const bool tc_ok = head_dim == 128;
+    const bool tc_ok = split_tc_supported(head_dim);
     if (o.path == FDEC_PATH_MMA && !mma_ok)
         return fail(FDEC_ERR_UNSUPPORTED, "the tensor-core path supports head_dim 64, 128, 192, 256 and 512");
     if (o.path == FDEC_PATH_TC && !tc_ok)
-        return fail(FDEC_ERR_UNSUPPORTED, "the tcgen05 path supports head_dim 128");
+        return fail(FDEC_ERR_UNSUPPORTED, "the tcgen05 path supports head_dim 64, 128, 192 and 256");
     const long long rows_ll = static_cast<long long>(q_len) * (num_qo_heads / num_kv_heads);
     if (rows_ll > (1 << 24)) return fail(FDEC_ERR_UNSUPPORTED, "q_len x group too large");
     for (int b = 0; b < batch; ++b)
@@ -400,10 +401,11 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
     size_t smem = 0;
     int threads = 0;
     if (p->path == FDEC_PATH_TC) {
-        // Two 128-row tiles per CTA share each staged K/V block once there are more than 128 rows.
-        const int tiles = p->rows > kTcRows ? 2 : 1;
+        // Two 128-row tiles per CTA share each staged K/V block once there are more than 128 rows
+        // (where tensor memory holds two tiles' S/P buffers and O: head_dim up to 128).
+        const int tiles = (p->rows > kTcRows && split_tc_max_tiles(head_dim) == 2) ? 2 : 1;
         p->rc = kTcRows * tiles;
-        smem = split_tc_smem_bytes(tiles);
+        smem = split_tc_smem_bytes(tiles, head_dim);
         threads = split_tc_threads(tiles);
     } else if (p->path == FDEC_PATH_MMA) {
         p->rc = kMmaRows;

@@ -111,13 +111,17 @@ int split_mma_threads(int head_dim, bool kv8);
 inline bool split_mma_kv8_supported(int head_dim) { return head_dim == 128 || head_dim == 256; }
 constexpr int kMmaRows = 16;
 
-// The tcgen05 dense-query split kernel (head_dim 128; `tiles` (1 or 2) 128-row
-// query tiles per CTA, 64-token stages: its tensor maps use boxes of
-// min(page_size, 64) token rows).
-cudaError_t launch_split_tc(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int tiles, bool bf16,
-                            dim3 grid, cudaStream_t s, bool launch);
-size_t split_tc_smem_bytes(int tiles);
+// The tcgen05 dense-query split kernel (head_dim 64, 128, 192, 256; `tiles` 128-row
+// query tiles per CTA: 1 or 2 for head_dim 64 and 128, 1 above; 64-token stages: its
+// tensor maps use boxes of min(page_size, 64) token rows).
+cudaError_t launch_split_tc(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int tiles, int head_dim,
+                            bool bf16, dim3 grid, cudaStream_t s, bool launch);
+size_t split_tc_smem_bytes(int tiles, int head_dim);
 int split_tc_threads(int tiles);
+inline bool split_tc_supported(int head_dim) {
+    return head_dim == 64 || head_dim == 128 || head_dim == 192 || head_dim == 256;
+}
+inline int split_tc_max_tiles(int head_dim) { return head_dim <= 128 ? 2 : 1; }
 constexpr int kTcRows = 128;
 constexpr int kTcStageTokens = 64;
 

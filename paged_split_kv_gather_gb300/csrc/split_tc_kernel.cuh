@@ -1,15 +1,17 @@
 // split_tc_kernel.cuh -- the dense-query split kernel on 5th-generation tensor
-// cores (tcgen05, accumulators in tensor memory), for q_len x group >= 64 rows
-// (speculative-decode and prefill chunks).
+// cores (tcgen05, accumulators in tensor memory), for more than 16 query rows
+// (q_len x group: speculative-decode and prefill chunks), head_dim D = 64, 128,
+// 192 or 256.
 //
 // One CTA: one work item (a run of 64-token blocks) x one KV head x NT tiles of
 // 128 query rows (rows = q positions x heads of the group, flattened).  The NT
-// tiles share every staged K/V block.  With a causal mask the item's token
-// range is clipped to the last token any row of the CTA can see.  Warps:
+// tiles share every staged K/V block (NT = 2 needs 2 x (128 + D) tensor-memory
+// columns: head_dim up to 128).  With a causal mask the item's token range is
+// clipped to the last token any row of the CTA can see.  Warps:
 //   warp 0      TMA producer: 64-token K/V stages (the shared producer).
 //   warp 1      MMA issuer (one lane), per tile t and block j:
-//                 S_t  = Q_t K^T            M 128 rows, N 64 tokens, K 128 dims  (8 MMAs)
-//                 O_t += P_t,hi V + P_t,lo V  M 128, N 128 dims, K 64 tokens      (2 x 4 MMAs)
+//                 S_t  = Q_t K^T            M 128 rows, N 64 tokens, K = D dims  (D / 16 MMAs)
+//                 O_t += P_t,hi V + P_t,lo V  M 128, N = D dims, K 64 tokens      (2 x 4 MMAs)
 //               Q and K are K-major and V MN-major, 128B-swizzled in shared
 //               memory; S_t, P_t and O_t live in tensor memory.  S_t has two
 //               buffers (block parity); P_t overwrites the S_t it came from (hi
@@ -39,27 +41,32 @@
 
 namespace fdec {
 
-template <int NT>
+template <int NT, int D_>
 struct TcLayout {
-    static constexpr int D = 128;
+    static constexpr int D = D_;
     static constexpr int TM = 128;                 // query rows per tile
     static constexpr int ROWS = NT * TM;           // query rows per CTA
     static constexpr int TOK = 64;                 // tokens per stage / S tile
     using G = StageGeom<D, TOK>;
-    static constexpr int S = NT == 1 ? 6 : 5;      // stages
-    static constexpr int Q_BYTES = TM * D * 2;     // per tile: 2 regions x 128 rows x 128 B
+    static constexpr int Q_BYTES = TM * D * 2;     // per tile: D/64 regions x 128 rows x 128 B
+    static constexpr int BAR_BYTES = 256;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_STAGES = OFF_Q + NT * Q_BYTES;
+    static constexpr int S_FIT = (232448 - 1024 - BAR_BYTES - NT * Q_BYTES) / G::STAGE_BYTES;
+    static constexpr int S = S_FIT > 6 ? 6 : S_FIT;  // stages
     static constexpr int OFF_BARS = OFF_STAGES + S * G::STAGE_BYTES;
     static constexpr int NBARS = 3 * S + 6 * NT + 1;
-    static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM = OFF_BARS + BAR_BYTES + 1024;  // + alignment slack
     static constexpr int THREADS = (2 + 4 * NT) * 32;
-    // tensor memory per tile t (base 256 t): S / P buffers at +0 and +64, O at +128
-    static constexpr uint32_t TMEM_COLS = NT == 1 ? 256u : 512u;
+    // tensor memory per tile t (base TILE_COLS t): S / P buffers at +0 and +64, O (D columns) at +128
+    static constexpr uint32_t TILE_COLS = 128 + D;
+    static constexpr uint32_t TMEM_COLS = NT * TILE_COLS <= 256 ? 256u : 512u;
+    static_assert(NT * TILE_COLS <= 512, "tensor memory: two S/P buffers and O per tile");
+    static_assert(S >= 2, "stages");
     static_assert(SMEM <= 232448, "shared memory");
     static_assert(NBARS * 8 + 8 <= BAR_BYTES, "barriers");
     static_assert(NT == 1 || NT == 2, "tiles per CTA");
+    static_assert(D % 64 == 0 && D <= 256, "P V is one MMA of N = head_dim (at most 256)");
 };
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row r in a 128B-swizzled region of 128-byte rows.
@@ -90,15 +97,15 @@ __device__ __forceinline__ uint32_t pack2(float x, float y) {
     }
 }
 
-template <int NT, bool BF16>
-__global__ void __launch_bounds__(TcLayout<NT>::THREADS, 1)
+template <int NT, int D, bool BF16>
+__global__ void __launch_bounds__(TcLayout<NT, D>::THREADS, 1)
 split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv) {
-    using Lay = TcLayout<NT>;
+    using Lay = TcLayout<NT, D>;
     using G = typename Lay::G;
     constexpr int S = Lay::S;
     constexpr int TOK = Lay::TOK;
-    constexpr int D = Lay::D;
+    constexpr uint32_t TC = Lay::TILE_COLS;
     constexpr float kLn2 = 0.69314718055994530942f;
     constexpr float kLazyRescale = 8.f;
     // bf16: P = hi + lo, both bf16 (hi = p truncated to bf16, lo = the residual
@@ -210,7 +217,7 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
             auto issue_qk = [&](int t, int slot, int buf) {
                 const uint64_t qd = qd0 + t * kQTile;
                 const uint64_t kd = kd0 + static_cast<uint32_t>(slot) * kStage;
-                const uint32_t d = tmem + 256 * t + 64 * buf;
+                const uint32_t d = tmem + TC * t + 64 * buf;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
                     tc_mma_f16(d, qd + (ks >> 2) * kQRegion + (ks & 3) * 2, kd + (ks >> 2) * kKRegion + (ks & 3) * 2, i_qk,
@@ -219,8 +226,8 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
             };
             auto issue_pv = [&](int t, int slot, int buf, bool acc) {
                 const uint64_t vd = vd0 + static_cast<uint32_t>(slot) * kStage;
-                const uint32_t p_tm = tmem + 256 * t + 64 * buf;
-                const uint32_t o_tm = tmem + 256 * t + 128;
+                const uint32_t p_tm = tmem + TC * t + 64 * buf;
+                const uint32_t o_tm = tmem + TC * t + 128;
                 tc_mma_f16_ts(o_tm, p_tm, vd, i_pv, acc);
 #pragma unroll
                 for (int i = 1; i < kParts * (TOK / 16); ++i) {  // i = part * 4 + ks: 16 tokens (128 rows of V) per step
@@ -273,7 +280,7 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
         const int qi = row / p.group;
         const int lim = p.causal ? (ir.L - p.q_len + qi) : (ir.L - 1);
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-        const uint32_t tmem_t = tmem + 256 * t + lane_base;
+        const uint32_t tmem_t = tmem + TC * t + lane_base;
         const uint32_t tmem_o = tmem_t + 128;
         const float c_log2 = p.scale_log2;
         float m = -INFINITY, l = 0.f;
@@ -447,7 +454,7 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
     }
 }
 
-template <int NT, bool BF16>
+template <int NT, int D, bool BF16>
 cudaError_t launch_split_tc_one(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
                                 cudaStream_t stream, bool launch) {
     static unsigned long long attr_done = 0;  // one bit per device
@@ -455,13 +462,13 @@ cudaError_t launch_split_tc_one(const SplitParams& p, const CUtensorMap& tk, con
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-        e = cudaFuncSetAttribute(split_tc_kernel<NT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 TcLayout<NT>::SMEM);
+        e = cudaFuncSetAttribute(split_tc_kernel<NT, D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 TcLayout<NT, D>::SMEM);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_RELEASE);
     }
     if (!launch) return cudaSuccess;
-    split_tc_kernel<NT, BF16><<<grid, TcLayout<NT>::THREADS, TcLayout<NT>::SMEM, stream>>>(p, tk, tv);
+    split_tc_kernel<NT, D, BF16><<<grid, TcLayout<NT, D>::THREADS, TcLayout<NT, D>::SMEM, stream>>>(p, tk, tv);
     return cudaGetLastError();
 }
 

@@ -105,8 +105,11 @@ def test_path_selection():
     for d in (64, 128, 192, 256, 512):
         assert fd.fdec_plan_get_info(_plan([100], head_dim=d))["path"] == fd.FDEC_PATH_MMA
         assert fd.fdec_plan_get_info(_plan([100], head_dim=d, path=fd.FDEC_PATH_SIMT))["path"] == fd.FDEC_PATH_SIMT
+    for d in (64, 128, 192, 256):
+        assert fd.fdec_plan_get_info(_plan([100], head_dim=d, path=fd.FDEC_PATH_TC))["path"] == fd.FDEC_PATH_TC
+    # head_dim 512: O alone would take all 512 tensor-memory columns
     with pytest.raises(fd.FdecError) as ei:
-        _plan([100], head_dim=64, path=fd.FDEC_PATH_TC)
+        _plan([100], head_dim=512, path=fd.FDEC_PATH_TC)
     assert ei.value.status_name == "FDEC_ERR_UNSUPPORTED"
 
 
@@ -124,8 +127,14 @@ def test_dense_query_rows_take_the_tcgen05_path():
     assert info["path"] == fd.FDEC_PATH_TC and info["rows_per_group"] == 256
     assert info["row_groups"] == 2048 * 4 // 256
     assert info["num_split_ctas"] == info["num_items"] * 8 * info["row_groups"]
-    # head_dim 64 / 192 keep the 16-row kernel at any row count
-    assert fd.fdec_plan_get_info(_plan([1000], q_len=64, head_dim=64))["path"] == fd.FDEC_PATH_MMA
+    # every head_dim the tcgen05 kernel is built for takes it above 16 rows (measured crossover);
+    # two tiles per CTA where tensor memory holds them (head_dim up to 128)
+    for d, tiles in ((64, 2), (128, 2), (192, 1), (256, 1)):
+        info = fd.fdec_plan_get_info(_plan([1000], q_len=64, head_dim=d))
+        assert info["path"] == fd.FDEC_PATH_TC and info["rows_per_group"] == 128 * tiles, (d, info)
+        assert fd.fdec_plan_get_info(_plan([1000], q_len=4, head_dim=d))["path"] == fd.FDEC_PATH_MMA
+    # head_dim 512 keeps the 16-row kernel at any row count
+    assert fd.fdec_plan_get_info(_plan([1000], q_len=64, head_dim=512))["path"] == fd.FDEC_PATH_MMA
 
 
 def test_row_groups_cover_all_query_rows():
@@ -316,7 +325,7 @@ def test_plan_invariants_hold_for_random_batches():
             assert C == bps
         nb = np.maximum(1, -(-np.asarray(lens, dtype=np.int64) // 64))
         rows = q_len * group
-        want_path = fd.FDEC_PATH_TC if (not kv8 and d == 128 and rows > 16) else fd.FDEC_PATH_MMA
+        want_path = fd.FDEC_PATH_TC if (not kv8 and d in (64, 128, 192, 256) and rows > 16) else fd.FDEC_PATH_MMA
         assert info["path"] == want_path
         # the persistent kernel (16-bit caches, head_dim 64/128/192 on the 16-row path)
         persistent = want_path == fd.FDEC_PATH_MMA and not kv8 and d in (64, 128, 192)

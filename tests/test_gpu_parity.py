@@ -148,6 +148,18 @@ TC_CASES = {
                             causal=True),
     "hnd_interleaved": lambda: W.make(2, 32, 8, 2, 128, 16, [1234, 640], dtype="bf16", device="cuda", seed=18,
                                       causal=True, layout="interleaved"),
+    # other head dims: 64 (two tiles per CTA), 192 and 256 (one tile; P V of N = 192 / 256)
+    "d64_two_tiles": lambda: W.make(2, 96, 8, 2, 64, 16, [700, 2500], dtype="bf16", device="cuda", seed=31,
+                                    causal=True),
+    "d64_f16_page64": lambda: W.make(2, 20, 16, 4, 64, 64, [4000, 130], dtype="f16", device="cuda", seed=32,
+                                     causal=True),
+    "d192_ragged_tile": lambda: W.make(2, 40, 16, 4, 192, 16, [2100, 777], dtype="f16", device="cuda", seed=33,
+                                       causal=True),
+    "d192_bf16": lambda: W.make(1, 64, 8, 2, 192, 64, [5000], dtype="bf16", device="cuda", seed=34, causal=True),
+    "d256": lambda: W.make(2, 32, 8, 2, 256, 32, [1500, 4100], dtype="bf16", device="cuda", seed=35, causal=True),
+    "d256_peaked_f16": lambda: W.make(1, 64, 8, 2, 256, 64, [3000], dtype="f16", device="cuda", seed=36,
+                                      causal=True, peaked=True),
+    "d256_not_causal": lambda: W.make(3, 8, 32, 4, 256, 16, [900, 64, 2600], dtype="bf16", device="cuda", seed=37),
 }
 
 
@@ -167,9 +179,10 @@ def test_tcgen05_kernel_under_any_split_plan(bps):
         assert pd.info["max_splits"] == 79
 
 
+@pytest.mark.parametrize("head_dim", [128, 256])
 @pytest.mark.parametrize("page_size", [1, 4, 8, 16, 64, 128, 256])
-def test_tcgen05_kernel_page_sizes_with_nan_guard(page_size):
-    w = W.make(3, 40, 16, 4, 128, page_size, [5, 333, 1000], dtype="bf16", device="cuda", seed=page_size,
+def test_tcgen05_kernel_page_sizes_with_nan_guard(page_size, head_dim):
+    w = W.make(3, 40, 16, 4, head_dim, page_size, [5, 333, 1000], dtype="bf16", device="cuda", seed=page_size,
                causal=True, nan_guard=True, pool_pages=2 * (1000 // page_size + 8))
     out, lse, pd = gpu_run(w, path=fd.FDEC_PATH_TC, blocks_per_split=3)
     assert pd.info["path"] == fd.FDEC_PATH_TC
