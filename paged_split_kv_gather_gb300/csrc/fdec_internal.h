@@ -78,7 +78,7 @@ struct ReduceParams {
     int hk, rows, group, q_len, hq, head_dim;
     int normalized_input;      // 1: sources are normalised (o, lse) states (merge_states)
     int src_rows_stride;       // rows per (slot, kv head) in the source arrays
-    int warps_per_unit;        // 1, 2, 4 or 8 (reduce_warps_per_unit of the largest task)
+    int warps_per_unit;        // 1, 2 or 4 (reduce_warps_per_unit of the largest task)
 };
 
 // Launch the split kernel for head_dim D (defined in split_d<D>.cu); rc is the

@@ -1,16 +1,23 @@
 // reduce.cu -- the log-sum-exp reduction of attention partials.
 //
-// One CTA of eight warps; each (KV head, query row, 32 head_dim elements) unit
-// of a task gets `warps_per_unit` (1, 2, 4 or 8) of them, chosen by the host
-// from the task's partial count, so that a few partials per row do not leave
-// warps idle.  A task merges `count` consecutive partial slots of one sequence.
-// Warp w of a unit takes partials w, w + wpu, ... (any number: no fixed 32-block
-// scratch), 16 at a time with all their loads in flight together (one element
+// One CTA of four warps; each (KV head, query row, 32 head_dim elements) unit
+// of a task gets `warps_per_unit` (1, 2 or 4) of them, chosen by the host from
+// the task's partial count, so that a few partials per row do not leave warps
+// idle.  A task merges `count` consecutive partial slots of one sequence.  Warp
+// w of a unit takes partials w, w + wpu, ... (any number: no fixed 32-block
+// scratch), 20 at a time with all their loads in flight together (one element
 // per lane), and keeps a running (max, sum, accumulator) merged by log-sum-exp,
-// so one round trip to memory serves up to 16 x wpu partials.  The warp states
+// so one round trip to memory serves up to 20 x wpu partials.  The warp states
 // of a unit are merged in shared memory.  The result is either one partial of
 // the next level (hierarchical passes when a sequence has more partials than
 // the fan-in) or the final out = O / L and lse = ln 2 * (M + log2 L).
+//
+// The CTA is sized to sit beside two CTAs of the persistent split kernel on one
+// SM (128 threads at <= 96 registers: the 12,288 registers those two leave free),
+// so that, launched as a programmatic dependent, every reduction CTA is resident
+// and past its prologue when the split grid completes.  (Measured: with 256-thread
+// CTAs of 78 registers, which do not fit there, the CTAs that had to wait for an
+// SM to empty made a 61-partial reduction 1.6 us slower.)
 //
 // The same kernel merges caller-given normalised (o, lse) states for
 // fdec_merge_states: there m_k = lse_k * log2(e) and l_k = 1.
@@ -21,7 +28,8 @@
 
 namespace fdec {
 
-constexpr int kReduceWarps = 8;
+constexpr int kReduceWarps = 4;
+constexpr int kReducePerWarp = 20;
 
 // (m in log2 units, l) of source row idx.
 __device__ __forceinline__ float2 source_ml(const ReduceParams& p, int64_t idx) {
@@ -30,10 +38,10 @@ __device__ __forceinline__ float2 source_ml(const ReduceParams& p, int64_t idx) 
     return p.src_ml[idx];
 }
 
-__global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceParams p, int num_tasks,
+__global__ void __launch_bounds__(kReduceWarps * 32, 5) reduce_kernel(const ReduceParams p, int num_tasks,
                                                                    ReduceTask single) {
     constexpr float kLn2 = 0.69314718055994530942f;
-    constexpr int U = 16;  // partials per warp per round trip
+    constexpr int U = kReducePerWarp;  // partials per warp per round trip
     __shared__ float s_acc[kReduceWarps][32];
     __shared__ float s_m[kReduceWarps];
     __shared__ float s_l[kReduceWarps];
@@ -125,10 +133,10 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceP
 }
 
 // Warps per unit for tasks of up to `max_count` partials: enough that each warp
-// takes at most 16 (one round trip), at most all eight.
+// takes at most kReducePerWarp (one round trip), at most all of the CTA's.
 int reduce_warps_per_unit(int max_count) {
     int w = 1;
-    while (w < kReduceWarps && w * 16 < max_count) w *= 2;
+    while (w < kReduceWarps && w * kReducePerWarp < max_count) w *= 2;
     return w;
 }
 
