@@ -421,7 +421,7 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
         delete p;
         return fail(FDEC_ERR_UNSUPPORTED, "q_len x group / rows per CTA or num_kv_heads above 65535");
     }
-    p->ctas_per_sm = p->persistent ? kPersistCtasPerSm
+    p->ctas_per_sm = p->persistent ? split_mma_persist_ctas_per_sm(head_dim)
                                    : std::max(1, std::min(static_cast<int>(233472 / (smem + 1024)), 2048 / threads));
 
     p->capacity.assign(seq_lens_host, seq_lens_host + batch);
@@ -467,7 +467,7 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
     });
     p->slots_a = next_slot;
     p->n_units = static_cast<int>(p->items.size()) * p->hk * p->row_groups;
-    p->persist_grid = std::min(p->n_units, num_sms * kPersistCtasPerSm);
+    p->persist_grid = std::min(p->n_units, num_sms * p->ctas_per_sm);
 
     // Reduction passes: level l merges groups of `fanin` slots; levels alternate
     // between region A (even) and region B (odd).

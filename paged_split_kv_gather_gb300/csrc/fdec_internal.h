@@ -100,13 +100,15 @@ cudaError_t launch_split_d512(const SplitParams& p, const CUtensorMap& tk, const
 cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int head_dim,
                              bool bf16, bool kv8, dim3 grid, cudaStream_t s, bool launch);
 size_t split_mma_smem_bytes(int head_dim, bool kv8);
-// The persistent form of the tensor-core split kernel (16-bit caches, head_dim 64, 128
-// and 192; q rows 16-byte aligned): CTAs stay resident and take work units until none
-// is left, so a unit's pipeline fill and the stragglers' tail are paid once per CTA.
+// The persistent form of the tensor-core split kernel (16-bit caches, every head_dim;
+// q rows 16-byte aligned): CTAs stay resident and take work units until none is left,
+// so a unit's pipeline fill is paid once per CTA and not once per work item.
 cudaError_t launch_split_mma_persist(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int head_dim,
                                      bool bf16, dim3 grid, cudaStream_t s, bool launch);
-inline bool split_mma_persist_supported(int head_dim) { return head_dim == 64 || head_dim == 128 || head_dim == 192; }
-constexpr int kPersistCtasPerSm = 2;
+inline bool split_mma_persist_supported(int head_dim) {
+    return head_dim == 64 || head_dim == 128 || head_dim == 192 || head_dim == 256 || head_dim == 512;
+}
+inline int split_mma_persist_ctas_per_sm(int head_dim) { return head_dim > 256 ? 1 : 2; }
 int split_mma_threads(int head_dim, bool kv8);
 inline bool split_mma_kv8_supported(int head_dim) { return head_dim == 128 || head_dim == 256; }
 constexpr int kMmaRows = 16;

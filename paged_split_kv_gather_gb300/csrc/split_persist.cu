@@ -1,5 +1,5 @@
 // split_persist.cu -- instantiations of the persistent tensor-core split kernel
-// (16-bit caches, head_dim 64, 128 and 192).
+// (16-bit caches, every head_dim).
 #include "split_persist_kernel.cuh"
 
 namespace fdec {
@@ -16,6 +16,12 @@ cudaError_t launch_split_mma_persist(const SplitParams& p, const CUtensorMap& tk
         case 192:
             return bf16 ? launch_split_mma_persist_one<192, true>(p, tk, tv, grid, s, launch)
                         : launch_split_mma_persist_one<192, false>(p, tk, tv, grid, s, launch);
+        case 256:
+            return bf16 ? launch_split_mma_persist_one<256, true>(p, tk, tv, grid, s, launch)
+                        : launch_split_mma_persist_one<256, false>(p, tk, tv, grid, s, launch);
+        case 512:
+            return bf16 ? launch_split_mma_persist_one<512, true>(p, tk, tv, grid, s, launch)
+                        : launch_split_mma_persist_one<512, false>(p, tk, tv, grid, s, launch);
         default:
             return cudaErrorInvalidValue;
     }

@@ -73,18 +73,32 @@ template <int D>
 struct PersistLayout {
     using G = StageGeom<D>;
     static constexpr int RC = 16;                      // query rows per unit (one M tile)
-    static constexpr int NP = 3;                       // consumer warps
-    static constexpr int THREADS = (NP + 1) * 32;
-    static constexpr int CTAS_PER_SM = kPersistCtasPerSm;
+    // head_dim 512: two warps share each stage, each accumulating half of O's
+    // columns (DH), as in MmaLayout; one CTA per SM (stages of 64 KB).
+    static constexpr int DSPLIT = D > 256 ? 2 : 1;
+    static constexpr int DH = D / DSPLIT;
+    static constexpr int CTAS_PER_SM = D > 256 ? 1 : 2;  // = split_mma_persist_ctas_per_sm(D)
+    // Two query buffers (the next unit's rows land while the last one still reads its
+    // own) where they fit beside enough stages; one above head_dim 192 (the producer
+    // then starts a unit once the previous one is merged).
+    static constexpr int QBUFS = D > 192 ? 1 : 2;
     static constexpr int Q_BYTES = RC * D * 2;         // one unit's query rows
     static constexpr int CTRL_BYTES = 2048;            // barriers, tags, unit records, merge scalars
     static constexpr int ALIGN_SLACK = 1024;
     static constexpr int BUDGET = 232448 / CTAS_PER_SM - 1024;
-    static constexpr int FIXED = CTRL_BYTES + 2 * Q_BYTES + ALIGN_SLACK;
+    static constexpr int FIXED = CTRL_BYTES + QBUFS * Q_BYTES + ALIGN_SLACK;
     static constexpr int S_FIT = (BUDGET - FIXED) / G::STAGE_BYTES;
     static constexpr int S = S_FIT > 16 ? 16 : S_FIT;
+    static constexpr int NP = (S - 1) < 3 ? (S - 1) : 3;  // consumer groups (one stage each at a time)
+    static constexpr int NW = NP * DSPLIT;                 // consumer warps
+    static constexpr int THREADS = (NW + 1) * 32;
     static constexpr int SMEM = FIXED + S * G::STAGE_BYTES;
-    static constexpr int O_STRIDE = D + 4;             // floats per row of a warp's O in its kept slot
+    // Where a group's O goes in its kept slot.  One warp per group: anywhere, rows of
+    // D + 4 floats (bank spread).  Two warps per group: each into its own half of the
+    // stage's V rows, which only it reads (its partner may still be reading K).
+    static constexpr int O_BASE = DSPLIT == 1 ? 0 : G::HALF_BYTES;  // bytes into the slot
+    static constexpr int O_ROW = DSPLIT == 1 ? D + 4 : DH;          // floats between rows
+    static constexpr int O_HALF = RC * DH;                          // floats between column halves
     // control area
     static constexpr int OFF_FULL = 0;                 // 2S
     static constexpr int OFF_EMPTY = OFF_FULL + 2 * S * 8;   // S
@@ -94,8 +108,9 @@ struct PersistLayout {
     static constexpr int OFF_ML = OFF_UNIT + 2 * static_cast<int>(sizeof(UnitMeta));  // [2][NP][RC] float2
     static constexpr int OFF_CNT = OFF_ML + 2 * NP * RC * 8;  // 2 ints
     static_assert(OFF_CNT + 8 <= CTRL_BYTES, "control area");
-    static_assert(RC * O_STRIDE * 4 <= G::STAGE_BYTES, "a warp's O must fit its kept slot");
-    static_assert(S >= NP + 1, "stage ring too small");
+    static_assert(DSPLIT == 1 ? RC * O_ROW * 4 <= G::STAGE_BYTES : O_HALF * 4 <= G::HALF_BYTES / 2,
+                  "a group's O must fit its kept slot");
+    static_assert(NP >= 2 && S >= NP + 1, "stage ring too small");
 };
 
 // A work unit as the producer sees it: the unit index, its work item, the run-time
@@ -139,7 +154,7 @@ __device__ __forceinline__ void punit_load_lens_pages(const SplitParams& p, PUni
 
 // The producer warp of the persistent kernel.  `first`: the CTA's first unit, its
 // loads issued before the CTA's set-up so that they overlap it.
-template <int D, int S, int NP>
+template <int D, int S, int NP, int QBUFS>
 __device__ __forceinline__ void produce_units(const SplitParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                               uint64_t* full, uint64_t* empty, uint64_t* qfree, int* tag,
                                               UnitMeta* um, uint16_t* qbuf, uint8_t* stages, bool tma_mode,
@@ -212,7 +227,7 @@ __device__ __forceinline__ void produce_units(const SplitParams& p, const CUtens
     };
 
     while (ok && cur.unit >= 0) {
-        const int cb = k & 1;
+        const int cb = k % QBUFS;
         // ---- the unit's record
         const int rem = cur.unit % upi;
         const int kvh = rem / rgc;
@@ -229,10 +244,10 @@ __device__ __forceinline__ void produce_units(const SplitParams& p, const CUtens
         }
         const int n_stage = tok_end > tok_begin ? (tok_end - tok_begin + TOK - 1) / TOK : 0;
         const int n_pad = max(NP, (n_stage + NP - 1) / NP * NP);
-        // ---- its query buffer and record are free once unit k - 2 has been merged
-        if (k >= 2) {
+        // ---- its query buffer and record are free once unit k - QBUFS has been merged
+        if (k >= QBUFS) {
             bool got = true;
-            if (lane == 0) got = mbar_wait_bounded(smem_addr(&qfree[cb]), ((k >> 1) - 1) & 1);
+            if (lane == 0) got = mbar_wait_bounded(smem_addr(&qfree[cb]), ((k / QBUFS) - 1) & 1);
             if (!__shfl_sync(0xffffffffu, got, 0)) {
                 ok = false;
                 break;
@@ -374,7 +389,7 @@ __device__ __forceinline__ void produce_units(const SplitParams& p, const CUtens
             }
         }
     } else {
-        // No unit left: one end tag per consumer warp.
+        // No unit left: one end tag per consumer group.
         for (int w = 0; w < NP; ++w, ++i) {
             if (!wait_slot(i)) {
                 ok = false;
@@ -402,12 +417,13 @@ __device__ __forceinline__ void produce_units(const SplitParams& p, const CUtens
     if (!ok && lane == 0) atomicOr(p.err, FDEC_DEVERR_TIMEOUT);
 }
 
-// Merge the NP consumer states of a unit (m, l per row in ml[NP][RC]; O rows in the
-// kept slots, [RC][O_STRIDE] floats each) and write the unit's partial or out / lse.
+// Merge the NP consumer states of a unit (m, l per row in ml[NP][RC]; O in the kept
+// slots: column c of row r at (c / DH) O_HALF + r O_ROW + c % DH floats) and write the
+// unit's partial or out / lse.
 // One warp: lane r first takes the statistics of row r (max, weights, sum), then the
 // lanes stride over (row, 4 columns) pairs with the row's values broadcast from its
 // lane.  The arithmetic and its order are those of merge_and_store.
-template <int D, int NP, int RC, int O_STRIDE>
+template <int D, int NP, int RC, int DH, int O_ROW, int O_HALF>
 __device__ __forceinline__ void merge_unit(const SplitParams& p, const UnitMeta& u, const float2* ml,
                                            const float* const (&o_w)[NP], int lane) {
     constexpr float kLn2 = 0.69314718055994530942f;
@@ -452,7 +468,8 @@ __device__ __forceinline__ void merge_unit(const SplitParams& p, const UnitMeta&
         if (Mr != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < NP; ++w) {
-                const float4 v = *reinterpret_cast<const float4*>(o_w[w] + r * O_STRIDE + 4 * c4);
+                const int c = 4 * c4;
+                const float4 v = *reinterpret_cast<const float4*>(o_w[w] + (c / DH) * O_HALF + r * O_ROW + c % DH);
                 O.x += v.x * er[w];
                 O.y += v.y * er[w];
                 O.z += v.z * er[w];
@@ -485,9 +502,12 @@ split_mma_persist_kernel(const __grid_constant__ SplitParams p, const __grid_con
     using G = StageGeom<D>;
     constexpr int S = Lay::S;
     constexpr int NP = Lay::NP;
+    constexpr int NW = Lay::NW;
+    constexpr int DSPLIT = Lay::DSPLIT;
+    constexpr int DH = Lay::DH;
+    constexpr int QBUFS = Lay::QBUFS;
     constexpr int RC = Lay::RC;
     constexpr int NT = W::NT;
-    constexpr int OS = Lay::O_STRIDE;
 
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::OFF_FULL);
@@ -497,12 +517,12 @@ split_mma_persist_kernel(const __grid_constant__ SplitParams p, const __grid_con
     UnitMeta* um = reinterpret_cast<UnitMeta*>(smem + Lay::OFF_UNIT);
     float2* mls = reinterpret_cast<float2*>(smem + Lay::OFF_ML);  // [2][NP][RC]
     int* cnt = reinterpret_cast<int*>(smem + Lay::OFF_CNT);       // [2]
-    uint16_t* qbuf = reinterpret_cast<uint16_t*>(smem + Lay::CTRL_BYTES);  // [2][RC][D]
+    uint16_t* qbuf = reinterpret_cast<uint16_t*>(smem + Lay::CTRL_BYTES);  // [QBUFS][RC][D]
     uint8_t* stages;
     {
-        const uint32_t raw = smem_addr(smem) + Lay::CTRL_BYTES + 2 * Lay::Q_BYTES;
+        const uint32_t raw = smem_addr(smem) + Lay::CTRL_BYTES + QBUFS * Lay::Q_BYTES;
         const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-        stages = smem + Lay::CTRL_BYTES + 2 * Lay::Q_BYTES + pad;
+        stages = smem + Lay::CTRL_BYTES + QBUFS * Lay::Q_BYTES + pad;
     }
 
     const int warp = threadIdx.x >> 5;
@@ -512,7 +532,7 @@ split_mma_persist_kernel(const __grid_constant__ SplitParams p, const __grid_con
     // before the set-up below, so that those round trips overlap it.
     PUnit first;
     first.unit = -1;
-    if (warp == NP) {
+    if (warp == NW) {
         first.unit = blockIdx.x;
         punit_load_item(p, first, p.hk * ((p.rows + RC - 1) / RC));
         punit_load_lens_pages(p, first, lane, tma_mode ? min(1 << p.page_shift, kStageTokens) : 1, tma_mode);
@@ -524,25 +544,25 @@ split_mma_persist_kernel(const __grid_constant__ SplitParams p, const __grid_con
         for (int x = 0; x < S; ++x) {
             mbar_init(smem_addr(&full[x]), tma_mode ? 1u : 33u);
             mbar_init(smem_addr(&full[S + x]), tma_mode ? 1u : 33u);
-            mbar_init(smem_addr(&empty[x]), 1u);
+            mbar_init(smem_addr(&empty[x]), static_cast<uint32_t>(DSPLIT));  // the warps of a group
         }
         mbar_init(smem_addr(&qfree[0]), 1);
         mbar_init(smem_addr(&qfree[1]), 1);
         fence_mbar_init();
         cnt[0] = cnt[1] = 0;
     }
-    // Query rows past a unit's group are never copied: zero both buffers once.
-    for (int x = threadIdx.x; x < 2 * Lay::Q_BYTES / 16; x += Lay::THREADS)
+    // Query rows past a unit's group are never copied: zero the buffers once.
+    for (int x = threadIdx.x; x < QBUFS * Lay::Q_BYTES / 16; x += Lay::THREADS)
         reinterpret_cast<uint4*>(qbuf)[x] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_shared();  // before the bulk copies overwrite rows of them
     __syncthreads();
 
-    if (warp == NP) {
+    if (warp == NW) {
         if (lane == 0 && tma_mode) {
             prefetch_tmap(&tmk);
             prefetch_tmap(&tmv);
         }
-        produce_units<D, S, NP>(p, &tmk, &tmv, full, empty, qfree, tag, um, qbuf, stages, tma_mode, first);
+        produce_units<D, S, NP, QBUFS>(p, &tmk, &tmv, full, empty, qfree, tag, um, qbuf, stages, tma_mode, first);
         return;
     }
 
@@ -553,7 +573,10 @@ split_mma_persist_kernel(const __grid_constant__ SplitParams p, const __grid_con
     const bool poll = p.page_shift < 5;  // stages of several boxes (see wait_stage_mode)
     int lim[2] = {0, 0};
     bool ok = true;
-    for (int i = warp;; i += NP) {
+    const int grp = warp / DSPLIT;         // consumer group: stage j of every unit goes to group j mod NP
+    const int half = warp - grp * DSPLIT;  // which DH columns of O this warp accumulates
+    const uint32_t v_half = static_cast<uint32_t>(half * (DH / 64) * G::REGION_BYTES);
+    for (int i = grp;; i += NP) {
         const int s = i % S;
         if (!wait_stage_mode<S>(full, i, poll)) {
             ok = false;
@@ -564,7 +587,7 @@ split_mma_persist_kernel(const __grid_constant__ SplitParams p, const __grid_con
         const int cb = t & 1, j = t >> 1;
         const int tok_begin = um[cb].tok_begin, tok_end = um[cb].tok_end, n_pad = um[cb].n_pad;
         const uint16_t* q_s = qbuf + cb * RC * D;
-        if (j < NP) {  // this warp's first stage of the unit
+        if (j < NP) {  // this group's first stage of the unit
             // the unit's query rows land with its stage 0 (stage i - j); that barrier is
             // still in this phase: its next use, stage i - j + 2S, cannot be issued before
             // this warp releases stage i
@@ -584,48 +607,51 @@ split_mma_persist_kernel(const __grid_constant__ SplitParams p, const __grid_con
         const int t0 = tok_begin + j * kStageTokens;
         const int nv = max(0, min(kStageTokens, tok_end - t0));
         uint8_t* st = stages + s * G::STAGE_BYTES;
-        if (nv > 0) cw.stage(q_s, st, nv, min(nv, lim[0] - t0 + 1), min(nv, lim[1] - t0 + 1), sl, 0u);
+        if (nv > 0) cw.stage(q_s, st, nv, min(nv, lim[0] - t0 + 1), min(nv, lim[1] - t0 + 1), sl, v_half);
         if (j < n_pad - NP) {
             if (nv > 0 && nv < kStageTokens) fence_proxy_async_shared();  // zeroed tail before the next TMA write
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
             continue;
         }
-        // This warp's last stage of the unit: its state goes into this (kept) slot.
+        // This group's last stage of the unit: its state goes into this (kept) slot.
         cw.finish_l();
         float2* ml = mls + cb * NP * RC;
-        if (tq == 0) {
-            ml[warp * RC + g] = make_float2(cw.mrow[0], cw.lrow[0]);
-            ml[warp * RC + g + 8] = make_float2(cw.mrow[1], cw.lrow[1]);
+        if (tq == 0 && half == 0) {  // the warps of a group hold the same m and l
+            ml[grp * RC + g] = make_float2(cw.mrow[0], cw.lrow[0]);
+            ml[grp * RC + g + 8] = make_float2(cw.mrow[1], cw.lrow[1]);
         }
-        float* o_s = reinterpret_cast<float*>(st);
+        float* o_s = reinterpret_cast<float*>(st + Lay::O_BASE) + half * Lay::O_HALF;
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-            *reinterpret_cast<float2*>(o_s + g * OS + 8 * n + 2 * tq) = make_float2(cw.o[n][0], cw.o[n][1]);
-            *reinterpret_cast<float2*>(o_s + (g + 8) * OS + 8 * n + 2 * tq) = make_float2(cw.o[n][2], cw.o[n][3]);
+            *reinterpret_cast<float2*>(o_s + g * Lay::O_ROW + 8 * n + 2 * tq) = make_float2(cw.o[n][0], cw.o[n][1]);
+            *reinterpret_cast<float2*>(o_s + (g + 8) * Lay::O_ROW + 8 * n + 2 * tq) =
+                make_float2(cw.o[n][2], cw.o[n][3]);
         }
         fence_proxy_async_shared();  // these generic writes precede the slot's next TMA fill
         __syncwarp();
         int last = 0;
         if (lane == 0) {
             __threadfence_block();
-            last = atomicAdd(&cnt[cb], 1) == NP - 1;
+            last = atomicAdd(&cnt[cb], 1) == NW - 1;
             if (last) __threadfence_block();
         }
         last = __shfl_sync(0xffffffffu, last, 0);
         if (!last) continue;
-        // The third warp of the unit: merge, store, release the kept slots and the buffer.
-        const int kept0 = i - j + n_pad - NP;  // ring index of warp 0's last stage of the unit
+        // The last warp of the unit: merge, store, release the kept slots and the buffer.
+        const int kept0 = i - j + n_pad - NP;  // ring index of group 0's last stage of the unit
         const float* o_w[NP];
 #pragma unroll
-        for (int w = 0; w < NP; ++w) o_w[w] = reinterpret_cast<const float*>(stages + ((kept0 + w) % S) * G::STAGE_BYTES);
+        for (int w = 0; w < NP; ++w)
+            o_w[w] = reinterpret_cast<const float*>(stages + ((kept0 + w) % S) * G::STAGE_BYTES + Lay::O_BASE);
         const UnitMeta u = um[cb];
-        merge_unit<D, NP, RC, OS>(p, u, ml, o_w, lane);
+        merge_unit<D, NP, RC, DH, Lay::O_ROW, Lay::O_HALF>(p, u, ml, o_w, lane);
         __syncwarp();
         if (lane == 0) {
             cnt[cb] = 0;
 #pragma unroll
-            for (int w = 0; w < NP; ++w) mbar_arrive(smem_addr(&empty[(kept0 + w) % S]));
+            for (int w = 0; w < NP; ++w)
+                for (int x = 0; x < DSPLIT; ++x) mbar_arrive(smem_addr(&empty[(kept0 + w) % S]));
             mbar_arrive(smem_addr(&qfree[cb]));
         }
     }

@@ -327,13 +327,13 @@ def test_plan_invariants_hold_for_random_batches():
         rows = q_len * group
         want_path = fd.FDEC_PATH_TC if (not kv8 and d in (64, 128, 192, 256) and rows > 16) else fd.FDEC_PATH_MMA
         assert info["path"] == want_path
-        # the persistent kernel (16-bit caches, head_dim 64/128/192 on the 16-row path)
-        persistent = want_path == fd.FDEC_PATH_MMA and not kv8 and d in (64, 128, 192)
+        # the persistent kernel (16-bit caches on the 16-row path; one CTA per SM at head_dim 512)
+        persistent = want_path == fd.FDEC_PATH_MMA and not kv8
         assert np.array_equal(splits, -(-nb // C))
         assert info["num_items"] == int(splits.sum()) and info["max_splits"] == int(splits.max())
         assert info["row_groups"] == -(-rows // info["rows_per_group"])
         units = info["num_items"] * hk * info["row_groups"]
-        assert info["num_split_ctas"] == (min(units, 152 * 2) if persistent else units)
+        assert info["num_split_ctas"] == (min(units, 152 * (1 if d == 512 else 2)) if persistent else units)
         F = fanin or 1024
         n, passes = int(splits.max()), 0
         while n > 1:

@@ -47,6 +47,19 @@ CASES = {
                                   seed=7),
     "many_sequences": lambda: W.make(40, 1, 8, 1, 128, 16, list(range(100, 40 * 997, 997)), dtype="bf16",
                                      device="cuda", seed=8),
+    # head_dim 256 (query rows re-read from shared memory, one query buffer) and 512 (two
+    # warps per stage, one CTA per SM), over more units than CTAs
+    "d256_many_units": lambda: W.make(12, 1, 16, 8, 256, 16, list(range(700, 12 * 1900, 1900)), dtype="f16",
+                                      device="cuda", seed=9),
+    "d256_page64_rows16": lambda: W.make(2, 2, 16, 2, 256, 64, [9000, 3100], dtype="bf16", causal=True,
+                                         device="cuda", seed=10),
+    "d512_many_units": lambda: W.make(10, 1, 16, 8, 512, 16, list(range(300, 10 * 2300, 2300)), dtype="bf16",
+                                      device="cuda", seed=13),
+    "d512_page32_causal": lambda: W.make(2, 3, 8, 2, 512, 32, [5000, 77], dtype="f16", causal=True,
+                                         device="cuda", seed=14),
+    # more units than CTAs at head_dim 256 and 512 (one query buffer, unit after unit)
+    "ragged_d256_interleaved": lambda: W.ragged(256, device="cuda", layout="interleaved"),
+    "ragged_d512_split2": lambda: W.ragged(512, device="cuda", layout="split2"),
 }
 
 
@@ -72,7 +85,9 @@ def test_persistent_and_grid_kernels_agree_bitwise(case):
     assert pd.device_errors() == 0
 
 
-@pytest.mark.parametrize("case", ["long_131072", "ragged_d192", "page1_f16", "many_sequences"])
+@pytest.mark.parametrize("case", ["long_131072", "ragged_d192", "page1_f16", "many_sequences", "d256_many_units",
+                                  "d512_many_units", "d512_page32_causal", "ragged_d256_interleaved",
+                                  "ragged_d512_split2"])
 def test_persistent_kernel_matches_the_oracle(case):
     w = CASES[case]()
     pd = fd.PagedDecode(w.seq_lens, w.q_len, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
@@ -86,7 +101,7 @@ def test_persistent_kernel_matches_the_oracle(case):
     assert pd.device_errors() == 0
     wc = w.to("cpu")
     rows = None
-    if case == "ragged_d192":  # a sample of output rows: two query heads of every sequence
+    if case.startswith("ragged"):  # a sample of output rows: two query heads of every sequence
         rows = [b * w.num_qo_heads + h for b in range(w.batch) for h in (0, w.num_qo_heads - 1)]
     ref_o, ref_l = oracle_run(wc, rows=rows)
     if rows is None:
