@@ -226,15 +226,14 @@ def _time_graph(torch, run, reps, flush, flush_us=None):
     return max(0.0, (res[0] - base) / reps)
 
 
-def _time_flush_graph(torch, reps, flush):
-    """µs of one L2 eviction, replayed from a CUDA graph of `reps` evictions (best of 5)."""
+def _time_graph_once(torch, run_all):
+    """µs of one replay of a CUDA graph of run_all() (best of 5)."""
     g = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
         with torch.cuda.graph(g, stream=side):
-            for _ in range(reps):
-                flush()
+            run_all()
     torch.cuda.current_stream().wait_stream(side)
     g.replay()
     torch.cuda.synchronize()
@@ -246,7 +245,8 @@ def _time_flush_graph(torch, reps, flush):
         b.record()
         torch.cuda.synchronize()
         best = min(best, a.elapsed_time(b) * 1e3)
-    return best / reps
+    del g
+    return best
 
 
 def _e4m3_point(dev, calls, hbm_peak, flush):
@@ -377,28 +377,56 @@ def _config_points(dev, calls, hbm_peak):
         del pd, run, pd1, run1, w
     points["planned_vs_single_split"] = versus
 
-    # No-cliff sweep: one pool of 8192 tokens, plans of capacity L (the page table's
-    # prefix); per-call times from graphs of 20 (eviction, call) pairs, whose
-    # resolution is finer than single-call events at these ~20 us calls.
-    w = W.long_context(8192, device=dev)
-    flush_us = min(_time_flush_graph(torch, 20, flush) for _ in range(3))
+    # No-cliff sweep over L = 1024 ... 8192 step 64.  Each timed call reads its own
+    # pages: one 512 MB pool of K/V pages, call c of a graph getting pages
+    # [c * L/64, (c + 1) * L/64) in a shuffled order, so that between two reads of a
+    # page the other calls of the graph have streamed about 512 MB (four times the
+    # L2) and every call starts from HBM.  The graph of those calls, back to back, is
+    # timed as a whole (best of 5 replays): no eviction to subtract, so the per-call
+    # figure is not lost in the jitter of a 512 MB flush.
     sweep = []
+    hk, D, P = 4, 128, 64
+    pool_pages = (512 << 20) // (2 * hk * P * D * 2)
+    kp = torch.randn(pool_pages, hk, P, D, device=dev).to(torch.bfloat16)
+    vp = torch.randn(pool_pages, hk, P, D, device=dev).to(torch.bfloat16)
+    qs = torch.randn(1, 1, 32, D, device=dev).to(torch.bfloat16)
+    out = torch.empty((1, 1, 32, D), device=dev)
+    lse = torch.empty((1, 1, 32), device=dev)
+    gen = torch.Generator(device="cpu").manual_seed(17)
     for L in range(1024, 8192 + 1, 64):
-        pd, run = runner(w, capacities=[L])
-        us = _time_graph(torch, run, 20, flush, flush_us=flush_us)
+        ppc = L // P
+        n = min(256, pool_pages // ppc)
+        perm = torch.cat([c * ppc + torch.randperm(ppc, generator=gen) for c in range(n)]).to(torch.int32)
+        tables = perm.view(n, ppc).to(dev)
+        lens = torch.full((1,), L, dtype=torch.int32, device=dev)
+        pd = fd.PagedDecode([L], 1, P, 32, hk, D, "bf16", device=dev)
+
+        def run_all(pd=pd, tables=tables, lens=lens, n=n):
+            for c in range(n):
+                pd.run(qs, kp, vp, tables[c:c + 1], lens, out, lse)
+
+        run_all()
+        torch.cuda.synchronize()
+        us = _time_graph_once(torch, run_all) / n
+        assert pd.device_errors() == 0
         sweep.append((L, us, int(pd.info["max_splits"])))
-        del pd, run
+        del pd, run_all, tables
+    del kp, vp
+    torch.cuda.empty_cache()
     ratios = [b[1] / a[1] for a, b in zip(sweep, sweep[1:])]
-    gbs = [L * w.num_kv_heads * w.head_dim * 4 / (us * 1e-6) / 1e9 for L, us, _ in sweep]
-    drops = [(sweep[i + 1][0], round(gbs[i + 1] / gbs[i], 3)) for i in range(len(sweep) - 1)
-             if sweep[i + 1][2] != sweep[i][2] and gbs[i + 1] < gbs[i]]
+    gbs = [L * hk * D * 4 / (us * 1e-6) / 1e9 for L, us, _ in sweep]
+    changes = [i for i in range(len(sweep) - 1) if sweep[i + 1][2] != sweep[i][2]]
+    drops = [(sweep[i + 1][0], round(gbs[i + 1] / gbs[i], 3)) for i in changes if gbs[i + 1] < gbs[i]]
     points["no_cliff_sweep"] = {
         "kv_lens": "1024..8192 step 64 (long-context shape: 32/4 heads, D 128, bf16, page 64)",
-        "timing": "CUDA graph of 20 (L2 eviction, call) pairs minus a graph of 20 evictions, best of 5 replays",
+        "timing": "per call: a CUDA graph of n back-to-back calls (n = min(256, 512 MB / the call's K/V bytes)), "
+                  "each call reading its own pages of a 512 MB pool, best of 5 replays / n",
         "max_adjacent_time_ratio": round(max(ratios), 3),
         "at_kv_len": sweep[int(np.argmax(ratios)) + 1][0],
+        "split_changes": len(changes),
         "gbs_drops_at_split_changes": drops,
-        "us_per_call": {str(L): round(us, 2) for L, us, _ in sweep},
+        "min_gbs_ratio_at_split_changes": round(min(gbs[i + 1] / gbs[i] for i in changes), 3) if changes else None,
+        "us_per_call": {str(L): round(us, 3) for L, us, _ in sweep},
         "splits": {str(L): sp for L, _, sp in sweep},
     }
     del flush
