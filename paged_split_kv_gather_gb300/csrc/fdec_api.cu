@@ -406,7 +406,7 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
         const int tiles = (p->rows > kTcRows && split_tc_max_tiles(head_dim) == 2) ? 2 : 1;
         p->rc = kTcRows * tiles;
         smem = split_tc_smem_bytes(tiles, head_dim);
-        threads = split_tc_threads(tiles);
+        threads = split_tc_threads(tiles, dtype == FDEC_BF16);
     } else if (p->path == FDEC_PATH_MMA) {
         p->rc = kMmaRows;
         smem = split_mma_smem_bytes(head_dim, kv8);

@@ -119,7 +119,7 @@ constexpr int kMmaRows = 16;
 cudaError_t launch_split_tc(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int tiles, int head_dim,
                             bool bf16, dim3 grid, cudaStream_t s, bool launch);
 size_t split_tc_smem_bytes(int tiles, int head_dim);
-int split_tc_threads(int tiles);
+int split_tc_threads(int tiles, bool bf16);
 inline bool split_tc_supported(int head_dim) {
     return head_dim == 64 || head_dim == 128 || head_dim == 192 || head_dim == 256;
 }

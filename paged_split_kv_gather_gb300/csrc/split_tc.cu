@@ -44,6 +44,9 @@ size_t split_tc_smem_bytes(int tiles, int head_dim) {
     }
 }
 
-int split_tc_threads(int tiles) { return tiles == 1 ? TcLayout<1, 128>::THREADS : TcLayout<2, 128>::THREADS; }
+int split_tc_threads(int tiles, bool bf16) {
+    if (bf16) return tiles == 1 ? TcLayout<1, 128, true>::THREADS : TcLayout<2, 128, true>::THREADS;
+    return tiles == 1 ? TcLayout<1, 128>::THREADS : TcLayout<2, 128>::THREADS;
+}
 
 }  // namespace fdec

@@ -22,12 +22,17 @@
 //               block's softmax, and the tiles take turns with the tensor cores.
 //   warps 2+4t..5+4t  softmax warpgroup of tile t, thread = row = tensor-memory
 //               lane: load the row of S, mask, row max in registers, exp2, and the
-//               row of P stored back into tensor memory: for bf16 a high part and
-//               a residual (both multiplied, so p keeps ~15 significant bits), for
-//               f16 one value (11 bits; the f16 P V products need half the MMAs).  The lazy rescale of the row of O (only when the
-//               max grew by more than 8 in log2 units; warp-uniform) first waits
-//               for the previous block's P V products.  After the last block:
-//               O, l, m -> one partial of the split, or out / lse.
+//               row of P stored back into tensor memory, per 16-token slice: one
+//               f16 value when the slice's V is f16 (11 significant bits, one P V
+//               product), else a bf16 high part and residual (~15 bits, two
+//               products).  The lazy rescale of the row of O (only when the max
+//               grew by more than 8 in log2 units; warp-uniform) first waits for
+//               the previous block's P V products.  After the last block: O, l,
+//               m -> one partial of the split, or out / lse.
+//   warps 2+4NT..5+4NT  (bf16 caches) V conversion: warp w rewrites token slice
+//               w of each stage as f16 in place when that is exact enough (its
+//               largest |v| is 0 or in [2^-10, 65504]) and records the slice's mode;
+//               the P V products of a stage wait for them (conv_full).
 // Synchronisation: stage full / empty mbarriers (TMA / commit of the P V MMAs),
 // and per tile s_full[2] (commit of the QK MMAs, per S buffer), p_full[2] (the
 // four softmax warps, per buffer), o_done (commit of the P V MMAs) and o_final
@@ -41,7 +46,7 @@
 
 namespace fdec {
 
-template <int NT, int D_>
+template <int NT, int D_, bool CONV = false>
 struct TcLayout {
     static constexpr int D = D_;
     static constexpr int TM = 128;                 // query rows per tile
@@ -49,22 +54,23 @@ struct TcLayout {
     static constexpr int TOK = 64;                 // tokens per stage / S tile
     using G = StageGeom<D, TOK>;
     static constexpr int Q_BYTES = TM * D * 2;     // per tile: D/64 regions x 128 rows x 128 B
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int BAR_BYTES = 512;
+    static constexpr int CONV_WARPS = CONV ? 4 : 0;  // V-slice conversion warps (bf16 caches)
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_STAGES = OFF_Q + NT * Q_BYTES;
     static constexpr int S_FIT = (232448 - 1024 - BAR_BYTES - NT * Q_BYTES) / G::STAGE_BYTES;
     static constexpr int S = S_FIT > 6 ? 6 : S_FIT;  // stages
     static constexpr int OFF_BARS = OFF_STAGES + S * G::STAGE_BYTES;
-    static constexpr int NBARS = 3 * S + 6 * NT + 1;
+    static constexpr int NBARS = 3 * S + 6 * NT + 1 + (CONV ? S : 0);
     static constexpr int SMEM = OFF_BARS + BAR_BYTES + 1024;  // + alignment slack
-    static constexpr int THREADS = (2 + 4 * NT) * 32;
+    static constexpr int THREADS = (2 + 4 * NT + CONV_WARPS) * 32;
     // tensor memory per tile t (base TILE_COLS t): S / P buffers at +0 and +64, O (D columns) at +128
     static constexpr uint32_t TILE_COLS = 128 + D;
     static constexpr uint32_t TMEM_COLS = NT * TILE_COLS <= 256 ? 256u : 512u;
     static_assert(NT * TILE_COLS <= 512, "tensor memory: two S/P buffers and O per tile");
     static_assert(S >= 2, "stages");
     static_assert(SMEM <= 232448, "shared memory");
-    static_assert(NBARS * 8 + 8 <= BAR_BYTES, "barriers");
+    static_assert(NBARS * 8 + 8 + 4 * S <= BAR_BYTES, "barriers, tensor-memory address, slice modes");
     static_assert(NT == 1 || NT == 2, "tiles per CTA");
     static_assert(D % 64 == 0 && D <= 256, "P V is one MMA of N = head_dim (at most 256)");
 };
@@ -86,6 +92,13 @@ __device__ __forceinline__ uint32_t pack_upper_halves(uint32_t x, uint32_t y) {
     return r;
 }
 
+// Per 16-bit half, the larger unsigned value.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float x, float y) {
     if constexpr (BF16) {
@@ -98,24 +111,27 @@ __device__ __forceinline__ uint32_t pack2(float x, float y) {
 }
 
 template <int NT, int D, bool BF16>
-__global__ void __launch_bounds__(TcLayout<NT, D>::THREADS, 1)
+__global__ void __launch_bounds__(TcLayout<NT, D, BF16>::THREADS, 1)
 split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv) {
-    using Lay = TcLayout<NT, D>;
+    constexpr bool CONV = BF16;  // bf16 caches: V slices converted to f16 where exact
+    using Lay = TcLayout<NT, D, CONV>;
     using G = typename Lay::G;
     constexpr int S = Lay::S;
     constexpr int TOK = Lay::TOK;
     constexpr uint32_t TC = Lay::TILE_COLS;
     constexpr float kLn2 = 0.69314718055994530942f;
     constexpr float kLazyRescale = 8.f;
-    // bf16: P = hi + lo, both bf16 (hi = p truncated to bf16, lo = the residual
-    // truncated), ~15 significant bits; split with shifts, logic ops and FMAs
-    // only (see pack_upper_halves).  f16: P is one f16 value
-    // per token (11 significant bits), scaled by 2^kPShift so that small p stay
-    // normal; l carries the same factor and the stored max drops by kPShift.
+    // P is scaled by 2^kPShift so that small p stay normal in f16; l carries the
+    // same factor and the stored max drops by kPShift.  For a 16-token slice whose V
+    // is f16 (an f16 cache, or a bf16 slice the conversion warps rewrote) P is one
+    // f16 value per token (11 significant bits) and P V one product.  For a bf16
+    // slice P = hi + lo, both bf16 (hi = p truncated to bf16, lo = the residual
+    // truncated), ~15 significant bits, and P V two products; the split uses shifts,
+    // logic ops and FMAs only (see pack_upper_halves).
     constexpr bool kSplit = BF16;
     constexpr int kParts = kSplit ? 2 : 1;
-    constexpr float kPShift = BF16 ? 0.f : 7.f;
+    constexpr float kPShift = 7.f;
 
     extern __shared__ __align__(128) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -129,7 +145,9 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
     uint64_t* o_done = p_full + 2 * NT;  // [NT]
     uint64_t* o_final = o_done + NT;     // [NT]
     uint64_t* mma_fin = o_final + NT;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_fin + 1);
+    uint64_t* conv_full = mma_fin + 1;  // [S]: the stage's V slices are converted (bf16)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(conv_full + (CONV ? S : 0));
+    uint32_t* vmode = tmem_slot + 2;    // [S]: byte w = 1 when V slice w of the stage is f16
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -165,6 +183,10 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
             mbar_init(smem_addr(&o_final[t]), 1);
         }
         mbar_init(smem_addr(mma_fin), 1);
+        if constexpr (CONV) {
+#pragma unroll
+            for (int x = 0; x < S; ++x) mbar_init(smem_addr(&conv_full[x]), 4);  // one arrival per conversion warp
+        }
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0 && tma_mode) {
@@ -207,6 +229,7 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
             bool ok = true;
             const uint32_t i_qk = idesc_f16(128, TOK, BF16, false, false);
             const uint32_t i_pv = idesc_f16(128, D, BF16, false, true);
+            const uint32_t i_pv16 = idesc_f16(128, D, false, false, true);  // f16 P times an f16 V slice
             // Descriptors are built once; a byte offset x within shared memory is
             // x >> 4 added to the start-address field (the sum stays below 2^14).
             const uint64_t qd0 = smem_desc_sw128(smem_addr(q_tiles), 16, 1024);
@@ -224,15 +247,31 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
                                ks > 0);
                 tc_commit(smem_addr(&s_full[2 * t + buf]));
             };
-            auto issue_pv = [&](int t, int slot, int buf, bool acc) {
+            // P V of one block, 16 tokens (128 rows of V) per step: one f16 product for a
+            // slice whose mode bit is set, else one product per part of P.
+            auto issue_pv = [&](int t, int slot, int buf, bool acc, uint32_t modes) {
                 const uint64_t vd = vd0 + static_cast<uint32_t>(slot) * kStage;
                 const uint32_t p_tm = tmem + TC * t + 64 * buf;
                 const uint32_t o_tm = tmem + TC * t + 128;
-                tc_mma_f16_ts(o_tm, p_tm, vd, i_pv, acc);
+                bool a = acc;
+                if (CONV && modes == 0x01010101u) {
 #pragma unroll
-                for (int i = 1; i < kParts * (TOK / 16); ++i) {  // i = part * 4 + ks: 16 tokens (128 rows of V) per step
-                    const int part = i / (TOK / 16), ks = i % (TOK / 16);
-                    tc_mma_f16_ts(o_tm, p_tm + 32 * part + 8 * ks, vd + ks * 128, i_pv, true);
+                    for (int ks = 0; ks < TOK / 16; ++ks) tc_mma_f16_ts(o_tm, p_tm + 8 * ks, vd + ks * 128, i_pv16, ks > 0 || acc);
+                    tc_commit(smem_addr(&o_done[t]));
+                    return;
+                }
+#pragma unroll
+                for (int ks = 0; ks < TOK / 16; ++ks) {
+                    if (CONV && ((modes >> (8 * ks)) & 1u)) {
+                        tc_mma_f16_ts(o_tm, p_tm + 8 * ks, vd + ks * 128, i_pv16, a);
+                        a = true;
+                    } else {
+#pragma unroll
+                        for (int part = 0; part < kParts; ++part) {
+                            tc_mma_f16_ts(o_tm, p_tm + 32 * part + 8 * ks, vd + ks * 128, i_pv, a);
+                            a = true;
+                        }
+                    }
                 }
                 tc_commit(smem_addr(&o_done[t]));
             };
@@ -255,11 +294,16 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
 #pragma unroll
                     for (int t = 0; t < NT; ++t) issue_qk(t, next_slot, (j + 1) & 1);
                 }
+                uint32_t modes = 0;
+                if constexpr (CONV) {  // the stage's V slices are final (converted or left bf16)
+                    if (!(ok = mbar_wait_bounded(smem_addr(&conv_full[slot]), (j / S) & 1))) break;
+                    modes = vmode[slot];
+                }
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
                     if (!(ok = mbar_wait_bounded(smem_addr(&p_full[2 * t + (j & 1)]), (j >> 1) & 1))) break;
                     tc_fence_after_sync();
-                    issue_pv(t, slot, j & 1, j > 0);
+                    issue_pv(t, slot, j & 1, j > 0, modes);
                     if (j + 1 == n_tiles) tc_commit(smem_addr(&o_final[t]));
                 }
                 if (!ok) break;
@@ -270,6 +314,70 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
             tc_commit(smem_addr(mma_fin));
             if (!mbar_wait_bounded(smem_addr(mma_fin), 0)) ok = false;
             if (!ok) atomicOr(p.err, FDEC_DEVERR_TIMEOUT);
+        }
+    } else if (warp >= 2 + 4 * NT) {
+        // ------------------------------------------------------------ V conversion (bf16 caches)
+        // Warp w owns token slice w (rows 16w .. 16w + 15 of every V region) of each
+        // stage.  When the slice's largest |v| is 0 or lies in [2^-10, 65504] it is
+        // rewritten in place as f16: exact for |v| >= 2^-17, and below that rounded to
+        // the f16 grid (spacing 2^-24, under 2^-14 of the slice's largest value); its
+        // P V product then runs once, with an f16 P.  Otherwise (larger or only tiny
+        // values, inf, NaN) the slice stays bf16 and takes the two products of P's
+        // parts.  Rows past the sequence's end are zeroed either way: their P is 0,
+        // and 0 x NaN would poison O.
+        if constexpr (CONV) {
+            const int w = warp - (2 + 4 * NT);
+            constexpr int CPL = D / 16;  // 16-byte chunks per lane: 16 rows x D / 8 chunks over 32 lanes
+            constexpr uint32_t kLo = 0x3a80u;  // |v| bits of 2^-10 (bf16)
+            constexpr uint32_t kHi = 0x477fu;  // 65280, the largest bf16 below the f16 maximum 65504
+            bool ok = true;
+            for (int j = 0; j < n_tiles; ++j) {
+                if (!(ok = mbar_wait_bounded(smem_addr(&full[j % (2 * S)]), (j / (2 * S)) & 1))) break;
+                const int slot = j % S;
+                uint8_t* vrows = stages + slot * G::STAGE_BYTES + G::HALF_BYTES;
+                const int nv = min(TOK, ir.tok_end - (ir.tok_begin + j * TOK));
+                uint4 x[CPL];
+                uint32_t m2 = 0u;  // per 16-bit half: the largest |v| bits seen (inf and NaN above every finite value)
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) {
+                    // chunk idx: 8 per 128-byte row, 16 rows per region (consecutive lanes
+                    // take consecutive 16 bytes of a row: conflict-free)
+                    const int idx = lane + 32 * i;
+                    const int row = 16 * w + ((idx >> 3) & 15);
+                    uint4* ptr = reinterpret_cast<uint4*>(vrows + (idx >> 7) * G::REGION_BYTES + row * 128 + (idx & 7) * 16);
+                    x[i] = row < nv ? *ptr : make_uint4(0u, 0u, 0u, 0u);
+                    m2 = max_u16x2(m2, x[i].x & 0x7fff7fffu);
+                    m2 = max_u16x2(m2, x[i].y & 0x7fff7fffu);
+                    m2 = max_u16x2(m2, x[i].z & 0x7fff7fffu);
+                    m2 = max_u16x2(m2, x[i].w & 0x7fff7fffu);
+                }
+                const uint32_t wm = __reduce_max_sync(0xffffffffu, max(m2 & 0xffffu, m2 >> 16));
+                const bool f16 = wm == 0u || (wm >= kLo && wm <= kHi);
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) {
+                    const int idx = lane + 32 * i;
+                    const int row = 16 * w + ((idx >> 3) & 15);
+                    uint4* ptr = reinterpret_cast<uint4*>(vrows + (idx >> 7) * G::REGION_BYTES + row * 128 + (idx & 7) * 16);
+                    if (f16) {
+                        uint32_t u[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const __half2 h = __floats2half2_rn(__uint_as_float(u[k] << 16), __uint_as_float(u[k] & 0xffff0000u));
+                            u[k] = *reinterpret_cast<const uint32_t*>(&h);
+                        }
+                        *ptr = make_uint4(u[0], u[1], u[2], u[3]);
+                    } else if (row >= nv) {
+                        *ptr = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                fence_proxy_async_shared();  // read by the tensor cores
+                __syncwarp();
+                if (lane == 0) {
+                    reinterpret_cast<uint8_t*>(&vmode[slot])[w] = f16 ? 1 : 0;
+                    mbar_arrive(smem_addr(&conv_full[slot]));
+                }
+            }
+            if (!ok && lane == 0) atomicOr(p.err, FDEC_DEVERR_TIMEOUT);
         }
     } else {
         // ------------------------------------------------------------ softmax warpgroups
@@ -354,44 +462,85 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
                     break;
                 }
                 tc_fence_after_sync();
-#pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    float a[32];
-                    tmem_ld32(tmem_o + c0, a);
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 16) {  // 16 columns at a time: few registers beside the row of S
+                    float a[16];
+                    tmem_ld16(tmem_o + c0, a);
                     tmem_wait_ld();
+                    uint32_t u[16];
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) a[c] *= alpha;
-                    tmem_st32(tmem_o + c0, a);
+                    for (int c = 0; c < 16; ++c) u[c] = __float_as_uint(a[c] * alpha);
+                    tmem_st16_u(tmem_o + c0, u);
                 }
                 tmem_wait_st();
             }
             const float mu = m == -INFINITY ? 0.f : m;
-            // p = exp2(s * cs - mu), its row sum, and the packed high / residual parts
-            uint32_t hi[TOK / 2], lo[kSplit ? TOK / 2 : 1];
+            // Which 16-token V slices of this block are f16 (bf16 caches: set by the
+            // conversion warps; the stage's slot is not refilled before P_t(j) is consumed).
+            uint32_t modes = 0x01010101u;
+            if constexpr (CONV) {
+                if (!mbar_wait_bounded(smem_addr(&conv_full[j % S]), (j / S) & 1)) {
+                    ok = false;
+                    break;
+                }
+                modes = vmode[j % S];
+            }
+            // p = exp2(s * cs - mu), its row sum, and P packed per slice: one f16 value
+            // per token, or (bf16 slices) the bf16 high part and residual.  P_t(j) goes
+            // over S_t(j) (f16 values or high parts in columns 0..31, residuals in
+            // 32..63), 32 tokens at a time: the row of S is already in registers.
             float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             const float2 cs2 = make_float2(cs, cs), nmu2 = make_float2(kPShift - mu, kPShift - mu);
+            if (modes == 0x01010101u) {
+                // every slice f16 (the common case): one straight-line pass, no per-slice branches
 #pragma unroll
-            for (int c = 0; c < TOK; c += 2) {
-                const float2 z = __ffma2_rn(make_float2(sv[c], sv[c + 1]), cs2, nmu2);
-                const float2 e = make_float2(exp2_approx(z.x), exp2_approx(z.y));
-                ls[(c >> 1) & 3] = __fadd2_rn(ls[(c >> 1) & 3], e);
-                if constexpr (kSplit) {
-                    const uint32_t bx = __float_as_uint(e.x), by = __float_as_uint(e.y);
-                    hi[c / 2] = pack_upper_halves(bx, by);  // truncation to bf16
-                    const float2 hf = make_float2(__uint_as_float(bx & 0xffff0000u), __uint_as_float(by & 0xffff0000u));
-                    const float2 rs = __ffma2_rn(hf, make_float2(-1.f, -1.f), e);  // exact residual
-                    lo[c / 2] = pack_upper_halves(__float_as_uint(rs.x), __float_as_uint(rs.y));
-                } else {
-                    hi[c / 2] = pack2<false>(e.x, e.y);
+                for (int h = 0; h < TOK / 32; ++h) {
+                    uint32_t hv[16];
+#pragma unroll
+                    for (int c = 32 * h; c < 32 * h + 32; c += 2) {
+                        const float2 z = __ffma2_rn(make_float2(sv[c], sv[c + 1]), cs2, nmu2);
+                        const float2 e = make_float2(exp2_approx(z.x), exp2_approx(z.y));
+                        ls[(c >> 1) & 3] = __fadd2_rn(ls[(c >> 1) & 3], e);
+                        hv[(c - 32 * h) / 2] = pack2<false>(e.x, e.y);
+                    }
+                    tmem_st16_u(buf + 16 * h, hv);
                 }
+            } else {
+#pragma unroll
+            for (int h = 0; h < TOK / 32; ++h) {
+                uint32_t hi[16], lo[kSplit ? 16 : 1];
+#pragma unroll
+                for (int ks = 2 * h; ks < 2 * h + 2; ++ks) {
+                    const bool half_p = (modes >> (8 * ks)) & 1u;
+#pragma unroll
+                    for (int c = 16 * ks; c < 16 * ks + 16; c += 2) {
+                        const int x = (c - 32 * h) / 2;  // word of this half
+                        const float2 z = __ffma2_rn(make_float2(sv[c], sv[c + 1]), cs2, nmu2);
+                        const float2 e = make_float2(exp2_approx(z.x), exp2_approx(z.y));
+                        ls[(c >> 1) & 3] = __fadd2_rn(ls[(c >> 1) & 3], e);
+                        if (!kSplit || half_p) {
+                            hi[x] = pack2<false>(e.x, e.y);
+                            if constexpr (kSplit) lo[x] = 0u;  // not read: this slice takes one product
+                        } else {
+                            const uint32_t bx = __float_as_uint(e.x), by = __float_as_uint(e.y);
+                            hi[x] = pack_upper_halves(bx, by);  // truncation to bf16
+                            const float2 hf = make_float2(__uint_as_float(bx & 0xffff0000u),
+                                                          __uint_as_float(by & 0xffff0000u));
+                            const float2 rs = __ffma2_rn(hf, make_float2(-1.f, -1.f), e);  // exact residual
+                            if constexpr (kSplit) lo[x] = pack_upper_halves(__float_as_uint(rs.x), __float_as_uint(rs.y));
+                        }
+                    }
+                }
+                tmem_st16_u(buf + 16 * h, hi);
+                if constexpr (kSplit) {
+                    if (((modes >> (16 * h)) & 0x0101u) != 0x0101u) tmem_st16_u(buf + 32 + 16 * h, lo);
+                }
+            }
             }
             const float2 l01 = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
             l = l * alpha + (l01.x + l01.y);
-            // P_t(j) over S_t(j): high parts in columns 0..31, residuals in 32..63
-            tmem_st32_u(buf + 0, hi);
-            if constexpr (kSplit) tmem_st32_u(buf + 32, lo);
             tmem_wait_st();
-            if (t == 0 && nv < TOK) {
+            if (!CONV && t == 0 && nv < TOK) {
                 // A partial stage: zero V rows past the sequence end (0 * NaN would
                 // poison O).  Tile 0's P V products come first for every stage.
                 zero_v_tail<D, TOK>(stages + (j % S) * G::STAGE_BYTES, nv, threadIdx.x - 64, 128);
@@ -463,12 +612,12 @@ cudaError_t launch_split_tc_one(const SplitParams& p, const CUtensorMap& tk, con
     if (e != cudaSuccess) return e;
     if (dev < 64 && !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & (1ull << dev))) {
         e = cudaFuncSetAttribute(split_tc_kernel<NT, D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 TcLayout<NT, D>::SMEM);
+                                 TcLayout<NT, D, BF16>::SMEM);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_RELEASE);
     }
     if (!launch) return cudaSuccess;
-    split_tc_kernel<NT, D, BF16><<<grid, TcLayout<NT, D>::THREADS, TcLayout<NT, D>::SMEM, stream>>>(p, tk, tv);
+    split_tc_kernel<NT, D, BF16><<<grid, TcLayout<NT, D, BF16>::THREADS, TcLayout<NT, D, BF16>::SMEM, stream>>>(p, tk, tv);
     return cudaGetLastError();
 }
 

@@ -170,6 +170,22 @@ def test_tcgen05_dense_query_kernel(case):
     assert pd.info["path"] == fd.FDEC_PATH_TC
 
 
+def test_tcgen05_bf16_v_slices_outside_the_f16_range():
+    # bf16 V slices (16 tokens = one page here) that f16 cannot hold within the kernel's
+    # rule -- values above 65504, a slice of values all below 2^-10, one outlier in an
+    # otherwise ordinary slice -- keep the two-product P V; the others run as f16.
+    w = W.make(2, 16, 32, 8, 128, 16, [3000, 700], dtype="bf16", device="cpu", seed=41, causal=True)
+    for k in range(3000 // 16):
+        pg = int(w.page_table[0, k])
+        if k % 5 == 1:
+            w.v[pg] *= 2.0 ** 17
+        elif k % 5 == 3:
+            w.v[pg] *= 2.0 ** -18
+    w.v[int(w.page_table[1, 2]), 0, 7, 5] = 1.0e6
+    (e_out, e_lse), pd = _check(w.to("cuda"), path=fd.FDEC_PATH_TC)
+    assert pd.info["path"] == fd.FDEC_PATH_TC
+
+
 @pytest.mark.parametrize("bps", [1, 3, 10**6])
 def test_tcgen05_kernel_under_any_split_plan(bps):
     w = W.make(2, 48, 8, 2, 128, 16, [3000, 5000], dtype="bf16", device="cuda", seed=21, causal=True,
