@@ -56,7 +56,9 @@ def _bind(path: str):
         + [P, I64, I64, I64, I64, I64]
         + [P, I64, I64, I64, I64, I64]
         + [P, I64, P]
-        + [I, I, I, I, I, I, I, I, ctypes.c_double, I, ctypes.c_double, ctypes.c_double, P, I64, P, P, I]
+        + [I, I, I, I, I, I, I, I, ctypes.c_double, I, ctypes.c_double, ctypes.c_double]
+        + [P, I64, I64, I64, I64, P, I64, I64, I64, I64]
+        + [P, I64, P, P, I]
     )
     lib.oracle_merge_states.restype = I
     lib.oracle_merge_states.argtypes = [P, P, I, I64, I, P, P]
@@ -111,19 +113,24 @@ def e4m3_to_double(bits: int) -> float:
     return _load().oracle_e4m3_to_double(int(bits) & 0xFF)
 
 
+KV_16BIT, KV_E4M3, KV_Q8_0 = 0, 1, 2  # storage formats (oracle.c)
+
+
 class Pool:
     """A K or V pool as flat storage plus element offset, page count and strides.
 
     Element (page, head, slot, dim) is at ``offset + page*stride_page +
     head*stride_head + slot*stride_token + dim``.  The storage is 16-bit (the
-    query's type) or, for a quantised cache, uint8 holding E4M3 codes.
+    query's type, or the binary16 scales of a q8_0 cache) or, for a quantised
+    cache, uint8 holding E4M3 codes or int8 holding q8_0 codes.
     """
 
     def __init__(self, storage, offset: int, num_pages: int, stride_page: int,
                  stride_head: int, stride_token: int):
         a = np.asarray(storage)
         self.fp8 = a.dtype == np.uint8
-        self.storage = np.ascontiguousarray(a).reshape(-1) if self.fp8 else _u16(storage)
+        self.fmt = KV_E4M3 if self.fp8 else (KV_Q8_0 if a.dtype == np.int8 else KV_16BIT)
+        self.storage = np.ascontiguousarray(a).reshape(-1) if self.fmt != KV_16BIT else _u16(storage)
         self.offset = int(offset)
         self.num_pages = int(num_pages)
         self.stride_page = int(stride_page)
@@ -135,18 +142,25 @@ def paged_attention(q_storage, q_offset: int, q_stride_tok: int, q_stride_head: 
                     k: Pool, v: Pool, page_table, seq_lens, *, q_len: int, num_qo_heads: int,
                     num_kv_heads: int, head_dim: int, page_size: int, is_bf16: bool,
                     causal: bool, scale: float, rows=None, n_threads: int = 0, k_scale: float = 1.0,
-                    v_scale: float = 1.0):
+                    v_scale: float = 1.0, k_scales: Pool | None = None, v_scales: Pool | None = None):
     """Return (out, lse) in float64.
 
     K and V are k_scale and v_scale times their stored values (decoded from
-    16-bit, or from E4M3 when the pools hold uint8 codes).
+    16-bit, from E4M3 when the pools hold uint8 codes, or from q8_0 when they hold
+    int8 codes: then k_scales / v_scales are the binary16 block-scale pools, scale
+    j of (page, head, slot) at the pool's address of "dim" j).
 
     Without ``rows``: out has shape [batch, q_len, Hq, D] and lse [batch, q_len, Hq].
     With ``rows`` (flat indices (b*q_len + i)*Hq + h): out is [len(rows), D], lse [len(rows)].
     """
     lib = _load()
-    if k.fp8 != v.fp8:
+    if k.fmt != v.fmt:
         raise ValueError("K and V pools must have the same storage type")
+    q8 = k.fmt == KV_Q8_0
+    if q8 and (k_scales is None or v_scales is None):
+        raise ValueError("q8_0 pools need k_scales and v_scales")
+    ks = k_scales if q8 else None
+    vs = v_scales if q8 else None
     qs = _u16(q_storage)
     table = np.ascontiguousarray(page_table, dtype=np.int32)
     if table.ndim != 2:
@@ -167,7 +181,11 @@ def paged_attention(q_storage, q_offset: int, q_stride_tok: int, q_stride_head: 
         v.storage.ctypes.data, v.offset, v.num_pages, v.stride_page, v.stride_head, v.stride_token,
         table.ctypes.data, table.shape[1], lens.ctypes.data,
         batch, q_len, num_qo_heads, num_kv_heads, head_dim, page_size, int(bool(is_bf16)),
-        int(bool(causal)), float(scale), int(k.fp8), float(k_scale), float(v_scale),
+        int(bool(causal)), float(scale), int(k.fmt), float(k_scale), float(v_scale),
+        None if ks is None else ks.storage.ctypes.data, 0 if ks is None else ks.offset,
+        0 if ks is None else ks.stride_page, 0 if ks is None else ks.stride_head, 0 if ks is None else ks.stride_token,
+        None if vs is None else vs.storage.ctypes.data, 0 if vs is None else vs.offset,
+        0 if vs is None else vs.stride_page, 0 if vs is None else vs.stride_head, 0 if vs is None else vs.stride_token,
         None if rows_arr is None else rows_arr.ctypes.data, n_rows,
         out.ctypes.data, lse.ctypes.data, int(n_threads))
     if st != 0:

@@ -43,6 +43,15 @@
  *   K_t = k_scale * e4m3(K_stored),   V_t = v_scale * e4m3(V_stored)
  * and everything above applies unchanged to these K_t, V_t.  For 16-bit caches
  * the same scales apply (1 gives the plain definition).
+ *
+ * Or K and V may be stored as q8_0, the block format of the llama.cpp caches the
+ * turboquant PR runs ("q8_0-K", and "KV cache types (q8_0 / q4_0)" in the HRX
+ * issue); the pages name it without printing it, and its public definition is:
+ * a row of d elements is d/32 blocks of 32 signed 8-bit codes, each block with one
+ * binary16 scale, and element e of the row is scale[e / 32] * code[e].  The codes
+ * live in the K / V pool at the addresses above (one byte each), the scales in a
+ * pool of their own, scale j of (page, head, slot) at
+ * base + page*stride_page + head*stride_head + slot*stride_token + j.
  */
 #include <math.h>
 #include <stdint.h>
@@ -104,10 +113,19 @@ double oracle_e4m3_to_double(uint8_t bits) {
 
 typedef double (*decode_fn)(uint16_t);
 
-/* Element idx of a K or V pool: 16-bit (decoded by dec) or E4M3. */
-static double kv_elem(const void* pool, int64_t idx, int kv_fp8, decode_fn dec) {
-    if (kv_fp8) return oracle_e4m3_to_double(((const uint8_t*)pool)[idx]);
-    return dec(((const uint16_t*)pool)[idx]);
+/* Storage formats of a K or V pool. */
+#define ORACLE_KV_16BIT 0
+#define ORACLE_KV_E4M3 1
+#define ORACLE_KV_Q8_0 2
+
+/* Element e of a K or V row whose first element is pool[idx]: 16-bit (decoded by
+ * dec), E4M3, or q8_0 with the row's scales at scales[sidx ...]. */
+static double kv_elem(const void* pool, int64_t idx, int e, int kv_fmt, decode_fn dec, const uint16_t* scales,
+                      int64_t sidx) {
+    if (kv_fmt == ORACLE_KV_E4M3) return oracle_e4m3_to_double(((const uint8_t*)pool)[idx + e]);
+    if (kv_fmt == ORACLE_KV_Q8_0)
+        return oracle_f16_to_double(scales[sidx + e / 32]) * (double)((const int8_t*)pool)[idx + e];
+    return dec(((const uint16_t*)pool)[idx + e]);
 }
 
 /* Return codes. */
@@ -121,10 +139,15 @@ int oracle_paged_attention(
     const void* v, int64_t v_off, int64_t v_pages, int64_t v_sp, int64_t v_sh, int64_t v_st,
     const int32_t* table, int64_t table_stride, const int32_t* seq_lens,
     int batch, int q_len, int hq, int hk, int d, int page_size, int is_bf16, int causal,
-    double scale, int kv_fp8, double k_scale, double v_scale, const int64_t* rows, int64_t n_rows, double* out, double* lse, int n_threads)
+    double scale, int kv_fmt, double k_scale, double v_scale,
+    const uint16_t* ksc, int64_t ksc_off, int64_t ksc_sp, int64_t ksc_sh, int64_t ksc_st,
+    const uint16_t* vsc, int64_t vsc_off, int64_t vsc_sp, int64_t vsc_sh, int64_t vsc_st,
+    const int64_t* rows, int64_t n_rows, double* out, double* lse, int n_threads)
 {
     if (batch < 0 || q_len < 1 || hq < 1 || hk < 1 || hq % hk != 0 || d < 1 || page_size < 1)
         return ORACLE_BAD_ARG;
+    if (kv_fmt < ORACLE_KV_16BIT || kv_fmt > ORACLE_KV_Q8_0) return ORACLE_BAD_ARG;
+    if (kv_fmt == ORACLE_KV_Q8_0 && (d % 32 != 0 || ksc == NULL || vsc == NULL)) return ORACLE_BAD_ARG;
     const int g = hq / hk;
     const decode_fn dec = is_bf16 ? oracle_bf16_to_double : oracle_f16_to_double;
     const int64_t total_rows = (int64_t)batch * q_len * hq;
@@ -182,8 +205,9 @@ int oracle_paged_attention(
                     continue;
                 }
                 const int64_t kp = k_off + page * k_sp + (int64_t)kvh * k_sh + slot * k_st;
+                const int64_t ks = ksc_off + page * ksc_sp + (int64_t)kvh * ksc_sh + slot * ksc_st;
                 double s = 0.0;
-                for (int e = 0; e < d; ++e) s += qd[e] * (k_scale * kv_elem(k, kp + e, kv_fp8, dec));
+                for (int e = 0; e < d; ++e) s += qd[e] * (k_scale * kv_elem(k, kp, e, kv_fmt, dec, ksc, ks));
                 z[t] = scale * s;
                 if (z[t] > zmax) zmax = z[t];
             }
@@ -196,9 +220,10 @@ int oracle_paged_attention(
                 if (page < 0 || page >= k_pages || page >= v_pages) continue;
                 const int64_t slot = t % page_size;
                 const int64_t vp = v_off + page * v_sp + (int64_t)kvh * v_sh + slot * v_st;
+                const int64_t vs = vsc_off + page * vsc_sp + (int64_t)kvh * vsc_sh + slot * vsc_st;
                 const double w = exp(z[t] - zmax);
                 denom += w;
-                for (int e = 0; e < d; ++e) acc[e] += w * (v_scale * kv_elem(v, vp + e, kv_fp8, dec));
+                for (int e = 0; e < d; ++e) acc[e] += w * (v_scale * kv_elem(v, vp, e, kv_fmt, dec, vsc, vs));
             }
             if (n_vis == 0 || denom == 0.0) {
                 for (int e = 0; e < d; ++e) o_row[e] = 0.0;

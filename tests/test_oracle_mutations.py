@@ -4,7 +4,8 @@ Each case plants one mistake in a copy of oracle/oracle.c (on the CPU),
 builds it, routes the oracle through it and runs the pin suite: at least one
 pin has to fail.  This shows the pins constrain every step of the definition
 (gather address, GQA head map, scale, causal alignment, normalisation, the
-log-sum-exp, the state merge, the 16-bit and E4M3 decoders and the K/V scales).
+log-sum-exp, the state merge, the 16-bit and E4M3 decoders, the K/V scales and the
+q8_0 block scales).
 """
 import os
 import subprocess
@@ -14,6 +15,7 @@ import pytest
 import oracle
 from tests import test_oracle_fp8 as pins_fp8
 from tests import test_oracle_pins as pins
+from tests import test_oracle_q8 as pins_q8
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -32,8 +34,13 @@ MUTATIONS = {
     "f16_subnormal_scale": ("ldexp((double)frac, -24)", "ldexp((double)frac, -25)"),
     "e4m3_bias_off_by_one": ("ldexp((double)(8 + frac), expo - 10)", "ldexp((double)(8 + frac), expo - 9)"),
     "e4m3_subnormal_scale": ("ldexp((double)frac, -9)", "ldexp((double)frac, -10)"),
-    "k_scale_dropped": ("(k_scale * kv_elem(k, kp + e", "(kv_elem(k, kp + e"),
-    "v_scale_dropped": ("(v_scale * kv_elem(v, vp + e", "(kv_elem(v, vp + e"),
+    "k_scale_dropped": ("(k_scale * kv_elem(k, kp, e", "(kv_elem(k, kp, e"),
+    "v_scale_dropped": ("(v_scale * kv_elem(v, vp, e", "(kv_elem(v, vp, e"),
+    "q8_0_block_index": ("scales[sidx + e / 32]", "scales[sidx + e / 64]"),
+    "q8_0_codes_unsigned": ("(double)((const int8_t*)pool)[idx + e]", "(double)((const uint8_t*)pool)[idx + e]"),
+    "q8_0_k_scales_from_v_pool": ("kv_elem(k, kp, e, kv_fmt, dec, ksc, ks)", "kv_elem(k, kp, e, kv_fmt, dec, vsc, ks)"),
+    "q8_0_scale_head_and_slot_strides_swapped": ("(int64_t)kvh * vsc_sh + slot * vsc_st",
+                                                 "(int64_t)kvh * vsc_st + slot * vsc_sh"),
     "last_token_dropped": ("n_vis = L;                              /* tokens", "n_vis = L - 1;                              /* tokens"),
 }
 
@@ -41,7 +48,7 @@ MUTATIONS = {
 def _pin_checks():
     """(name, callable) for every pin, with parametrised pins expanded."""
     checks = []
-    for mod in (pins, pins_fp8):
+    for mod in (pins, pins_fp8, pins_q8):
         for name in dir(mod):
             if not name.startswith("test_"):
                 continue
