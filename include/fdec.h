@@ -113,8 +113,14 @@ enum { FDEC_PATH_AUTO = 0, FDEC_PATH_SIMT = 1, FDEC_PATH_MMA = 2, FDEC_PATH_TC =
  * code (scales given to fdec_run_scaled).  E4M3 caches run on the MMA path with
  * head_dim 128 or 256; the codes are staged as they are stored and widened to
  * 16 bits in shared memory, so no dequantised copy of the cache exists anywhere.
+ * Q8_0: the llama.cpp block format the turboquant PR's caches use ("q8_0-K"; the
+ * HRX issue lists "KV cache types (q8_0 / q4_0)" as open); the pages name it and
+ * do not print it, so this is its public definition: each K/V row of head_dim
+ * elements is head_dim / 32 blocks of 32 signed 8-bit codes, one binary16 scale
+ * per block, and element e is scale[e / 32] x code[e].  Codes and scales live in
+ * separate pools (fdec_run_q8_0); MMA path, head_dim 128 or 256.
  */
-enum { FDEC_KV_SAME = 0, FDEC_KV_E4M3 = 1 };
+enum { FDEC_KV_SAME = 0, FDEC_KV_E4M3 = 1, FDEC_KV_Q8_0 = 2 };
 
 /* Plan options; pass NULL for the defaults (all fields 0). */
 typedef struct {
@@ -123,7 +129,8 @@ typedef struct {
     int path;              /* FDEC_PATH_AUTO (TC when head_dim <= 256 and q_len x group > 16, else
                               MMA), _SIMT, _MMA (every head_dim), _TC (head_dim 64, 128, 192, 256) */
     int num_sms;           /* 0 = query the current device; > 0 plans without a device */
-    int kv_dtype;          /* FDEC_KV_SAME (0) or FDEC_KV_E4M3 (head_dim 128 / 256; path AUTO or MMA) */
+    int kv_dtype;          /* FDEC_KV_SAME (0), FDEC_KV_E4M3 or FDEC_KV_Q8_0 (head_dim 128 / 256; path AUTO
+                              or MMA) */
 } fdec_plan_opts;
 
 /* What a plan decided (for logging, tests and benchmarks). */
@@ -210,6 +217,24 @@ fdec_status fdec_run_scaled(fdec_plan_t plan, const void* q, int64_t q_stride_to
                             int64_t page_table_stride, const int32_t* seq_lens_dev, float scale,
                             float k_scale, float v_scale, float* out, float* lse, void* workspace,
                             cudaStream_t stream);
+
+/*
+ * fdec_run for q8_0 caches (plans made with kv_dtype FDEC_KV_Q8_0; fdec_run and
+ * fdec_run_scaled refuse them with FDEC_ERR_INVALID_ARG).  k and v describe the
+ * code pools as for E4M3 caches: one signed byte per element, strides in
+ * elements (bytes), 16-byte aligned base and strides.  k_scales and v_scales
+ * describe the block-scale pools: binary16, scale j of (page, head, slot) at
+ * base + page*stride_page + head*stride_head + slot*stride_token + j (elements),
+ * j < head_dim / 32; base aligned to head_dim / 16 bytes and strides multiples
+ * of head_dim / 32 (FDEC_ERR_LAYOUT otherwise); a page id must be below every
+ * pool's num_pages.  Neither codes nor scales are written; the scales are staged
+ * with their tokens' codes and applied in the kernel, so no dequantised copy
+ * exists.  Otherwise as fdec_run (k_scale = v_scale = 1).
+ */
+fdec_status fdec_run_q8_0(fdec_plan_t plan, const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                          fdec_kv_desc k, fdec_kv_desc k_scales, fdec_kv_desc v, fdec_kv_desc v_scales,
+                          const int32_t* page_table, int64_t page_table_stride, const int32_t* seq_lens_dev,
+                          float scale, float* out, float* lse, void* workspace, cudaStream_t stream);
 
 /*
  * Merge n_states normalised attention states (as fdec_run writes them) over

@@ -22,7 +22,7 @@ __all__ = [
     "fdec_plan_set_split_event", "fdec_read_device_errors", "fdec_last_error", "fdec_version",
     "fdec_run_static_workspace", "fdec_append", "kv_desc", "library_path", "PagedDecode", "EXPORTED_SYMBOLS",
     "FDEC_F16", "FDEC_BF16", "FDEC_PATH_AUTO", "FDEC_PATH_SIMT", "FDEC_PATH_MMA", "FDEC_PATH_TC",
-    "FDEC_KV_SAME", "FDEC_KV_E4M3", "fdec_run_scaled", "fdec_append_e4m3",
+    "FDEC_KV_SAME", "FDEC_KV_E4M3", "FDEC_KV_Q8_0", "fdec_run_scaled", "fdec_append_e4m3", "fdec_run_q8_0",
     "DEVERR_PAGE_ID", "DEVERR_SEQ_LEN", "DEVERR_TIMEOUT",
 ]
 
@@ -31,7 +31,7 @@ _LIB_PATH = os.path.join(_HERE, "libfdec.so")
 
 FDEC_F16, FDEC_BF16 = 0, 1
 FDEC_PATH_AUTO, FDEC_PATH_SIMT, FDEC_PATH_MMA, FDEC_PATH_TC = 0, 1, 2, 3
-FDEC_KV_SAME, FDEC_KV_E4M3 = 0, 1
+FDEC_KV_SAME, FDEC_KV_E4M3, FDEC_KV_Q8_0 = 0, 1, 2
 DEVERR_PAGE_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 
 STATUS_NAMES = {
@@ -45,7 +45,7 @@ EXPORTED_SYMBOLS = (
     "fdec_plan", "fdec_plan_upload", "fdec_run", "fdec_merge_states", "fdec_plan_destroy",
     "fdec_plan_get_info", "fdec_plan_get_splits", "fdec_plan_set_split_event",
     "fdec_read_device_errors", "fdec_last_error", "fdec_version", "fdec_run_static_workspace", "fdec_append",
-    "fdec_run_scaled", "fdec_append_e4m3",
+    "fdec_run_scaled", "fdec_append_e4m3", "fdec_run_q8_0",
 )
 
 
@@ -111,6 +111,9 @@ def _load():
         lib.fdec_run_scaled.argtypes = [P, P, I64, I64, KVDesc, KVDesc, P, I64, P, ctypes.c_float, ctypes.c_float,
                                         ctypes.c_float, P, P, P, P]
         lib.fdec_run_static_workspace.restype = I
+        lib.fdec_run_q8_0.restype = I
+        lib.fdec_run_q8_0.argtypes = [P, P, I64, I64, KVDesc, KVDesc, KVDesc, KVDesc, P, I64, P, ctypes.c_float, P,
+                                      P, P, P]
         lib.fdec_run_static_workspace.argtypes = [P, P, I64, I64, KVDesc, KVDesc, P, I64, P, ctypes.c_float, P,
                                                   P, P]
         lib.fdec_merge_states.restype = I
@@ -179,10 +182,11 @@ class Plan:
 def fdec_plan(seq_lens: Sequence[int], q_len: int, page_size: int, num_qo_heads: int, num_kv_heads: int,
               head_dim: int, dtype: str = "bf16", causal: bool = False, blocks_per_split: int = 0,
               reducer_fanin: int = 0, path: int = FDEC_PATH_AUTO, num_sms: int = 0, kv_dtype: str = "") -> Plan:
-    """kv_dtype: "" (K/V in the q dtype) or "fp8" (E4M3 codes; scales go to fdec_run)."""
+    """kv_dtype: "" (K/V in the q dtype), "fp8" (E4M3 codes; scales go to fdec_run_scaled) or
+    "q8_0" (int8 codes with binary16 block scales; see fdec_run_q8_0)."""
     lib = _load()
     lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32).reshape(-1))
-    kvd = {"": FDEC_KV_SAME, "fp8": FDEC_KV_E4M3}[kv_dtype]
+    kvd = {"": FDEC_KV_SAME, "fp8": FDEC_KV_E4M3, "q8_0": FDEC_KV_Q8_0}[kv_dtype]
     opts = PlanOpts(blocks_per_split, reducer_fanin, path, num_sms, kvd)
     handle = ctypes.c_void_p()
     ws = ctypes.c_size_t()
@@ -276,7 +280,7 @@ def fdec_run(plan: Plan, q, k, v, page_table, seq_lens, out, lse, workspace, sca
 
 def _check_kv_type(plan: Plan, k, v) -> None:
     """K/V tensors must hold the element type the plan was made for (1-byte E4M3 codes or 16-bit)."""
-    want = 1 if plan.meta.get("kv_dtype") == "fp8" else 2
+    want = 1 if plan.meta.get("kv_dtype") in ("fp8", "q8_0") else 2
     for t in (k, v):
         if not isinstance(t, KVDesc) and t.element_size() != want:
             raise ValueError(f"this plan reads {want}-byte K/V elements, got {t.dtype}")
@@ -298,6 +302,28 @@ def fdec_run_scaled(plan: Plan, q, k, v, page_table, seq_lens, out, lse, workspa
                                    page_table.stride(0), seq_lens.data_ptr(), sc, float(k_scale), float(v_scale),
                                    out.data_ptr(), None if lse is None else lse.data_ptr(), workspace.data_ptr(),
                                    _stream_handle(stream)))
+
+
+def fdec_run_q8_0(plan: Plan, q, k, k_scales, v, v_scales, page_table, seq_lens, out, lse, workspace,
+                  scale: Optional[float] = None, stream=None) -> None:
+    """fdec_run over a q8_0 cache: k / v int8 code views [page, kv_head, slot, D], k_scales /
+    v_scales binary16 views [page, kv_head, slot, D / 32] (element e of a row is
+    scale[e // 32] * code[e])."""
+    descs = [t if isinstance(t, KVDesc) else kv_desc(t) for t in (k, k_scales, v, v_scales)]
+    if not out.is_contiguous() or (lse is not None and not lse.is_contiguous()):
+        raise ValueError("out and lse must be contiguous")
+    tok, head = _q_strides(q)
+    if page_table.stride(1) != 1:
+        raise ValueError("page_table rows must be contiguous")
+    sc = 1.0 / math.sqrt(plan.meta["head_dim"]) if scale is None else float(scale)
+    _check_kv_type(plan, k, v)
+    for t in (k_scales, v_scales):
+        if not isinstance(t, KVDesc) and t.element_size() != 2:
+            raise ValueError(f"q8_0 scales are binary16, got {t.dtype}")
+    _check(_load().fdec_run_q8_0(plan.handle, q.data_ptr(), tok, head, *descs, page_table.data_ptr(),
+                                 page_table.stride(0), seq_lens.data_ptr(), sc, out.data_ptr(),
+                                 None if lse is None else lse.data_ptr(), workspace.data_ptr(),
+                                 _stream_handle(stream)))
 
 
 def fdec_run_static_workspace(plan: Plan, q, k, v, page_table, seq_lens, out, lse, scale: Optional[float] = None,
@@ -375,8 +401,13 @@ class PagedDecode:
         fdec_plan_upload(self.plan, self.workspace, stream)
 
     def run(self, q, k, v, page_table, seq_lens, out, lse=None, scale=None, stream=None, k_scale=None,
-            v_scale=None):
-        if k_scale is None and v_scale is None:
+            v_scale=None, k_scales=None, v_scales=None):
+        if k_scales is not None or v_scales is not None:  # q8_0 block scales
+            if k_scale is not None or v_scale is not None:
+                raise ValueError("q8_0 caches take block scales, not k_scale / v_scale")
+            fdec_run_q8_0(self.plan, q, k, k_scales, v, v_scales, page_table, seq_lens, out, lse, self.workspace,
+                          scale, stream)
+        elif k_scale is None and v_scale is None:
             fdec_run(self.plan, q, k, v, page_table, seq_lens, out, lse, self.workspace, scale, stream)
         else:
             fdec_run_scaled(self.plan, q, k, v, page_table, seq_lens, out, lse, self.workspace, scale,

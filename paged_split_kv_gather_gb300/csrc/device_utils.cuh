@@ -143,6 +143,11 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// 8-byte asynchronous copy global -> shared (both addresses 8-byte aligned).
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+
 // Arrive on `bar` once this thread's earlier cp.async copies have landed (the
 // barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {

@@ -117,7 +117,8 @@ struct fdec_plan_s {
     int batch = 0, q_len = 1, page_size = 1, page_shift = 0;
     int hq = 0, hk = 0, head_dim = 0, group = 1, rows = 1;
     fdec_dtype dtype = FDEC_BF16;
-    bool kv8 = false;  // K/V stored as E4M3 codes
+    bool kv8 = false;  // K/V stored as 8-bit codes (E4M3, or q8_0 with q8 set)
+    bool q8 = false;   // q8_0: int8 codes in blocks of 32 with a binary16 scale each
     int causal = 0;
     int path = FDEC_PATH_SIMT;
     bool persistent = false;  // MMA path over 16-bit caches: resident CTAs take work units
@@ -230,7 +231,8 @@ cudaError_t dispatch_split(const fdec_plan_s* p, const SplitParams& sp, dim3 gri
     if (p->path == FDEC_PATH_TC)
         return launch_split_tc(sp, tk, tv, p->rc / kTcRows, p->head_dim, bf16, grid, stream, launch);
     if (p->path == FDEC_PATH_MMA)
-        return launch_split_mma(sp, tk, tv, p->head_dim, bf16, p->kv8, grid, stream, launch);
+        return p->q8 ? launch_split_mma_q8(sp, tk, tv, p->head_dim, bf16, grid, stream, launch)
+                     : launch_split_mma(sp, tk, tv, p->head_dim, bf16, p->kv8, grid, stream, launch);
     switch (p->head_dim) {
         case 64: return launch_split_d64(sp, tk, tv, p->rc, bf16, grid, stream, launch);
         case 128: return launch_split_d128(sp, tk, tv, p->rc, bf16, grid, stream, launch);
@@ -341,13 +343,14 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
         return fail(FDEC_ERR_INVALID_ARG, "invalid plan options");
     if (o.path != FDEC_PATH_AUTO && o.path != FDEC_PATH_SIMT && o.path != FDEC_PATH_MMA && o.path != FDEC_PATH_TC)
         return fail(FDEC_ERR_INVALID_ARG, "invalid path option");
-    if (o.kv_dtype != FDEC_KV_SAME && o.kv_dtype != FDEC_KV_E4M3)
-        return fail(FDEC_ERR_INVALID_ARG, "kv_dtype must be FDEC_KV_SAME or FDEC_KV_E4M3");
-    const bool kv8 = o.kv_dtype == FDEC_KV_E4M3;
+    if (o.kv_dtype != FDEC_KV_SAME && o.kv_dtype != FDEC_KV_E4M3 && o.kv_dtype != FDEC_KV_Q8_0)
+        return fail(FDEC_ERR_INVALID_ARG, "kv_dtype must be FDEC_KV_SAME, FDEC_KV_E4M3 or FDEC_KV_Q8_0");
+    const bool q8 = o.kv_dtype == FDEC_KV_Q8_0;
+    const bool kv8 = o.kv_dtype == FDEC_KV_E4M3 || q8;
     if (kv8 && !split_mma_kv8_supported(head_dim))
-        return fail(FDEC_ERR_UNSUPPORTED, "E4M3 caches support head_dim 128 and 256");
+        return fail(FDEC_ERR_UNSUPPORTED, "E4M3 and q8_0 caches support head_dim 128 and 256");
     if (kv8 && o.path != FDEC_PATH_AUTO && o.path != FDEC_PATH_MMA)
-        return fail(FDEC_ERR_UNSUPPORTED, "E4M3 caches run on the MMA path only");
+        return fail(FDEC_ERR_UNSUPPORTED, "E4M3 and q8_0 caches run on the MMA path only");
     const bool mma_ok = head_dim_supported(head_dim);  // every supported head_dim
     const bool tc_ok = split_tc_supported(head_dim);
     if (o.path == FDEC_PATH_MMA && !mma_ok)
@@ -383,6 +386,7 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
     p->rows = static_cast<int>(rows_ll);
     p->dtype = dtype;
     p->kv8 = kv8;
+    p->q8 = q8;
     p->causal = (causal != 0 && q_len > 1) ? 1 : 0;
     // The warp-level tensor-core kernel by default (every head_dim; see
     // split_mma_kernel.cuh for why tensor cores pay off even when bandwidth-bound);
@@ -409,8 +413,8 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
         threads = split_tc_threads(tiles, dtype == FDEC_BF16);
     } else if (p->path == FDEC_PATH_MMA) {
         p->rc = kMmaRows;
-        smem = split_mma_smem_bytes(head_dim, kv8);
-        threads = split_mma_threads(head_dim, kv8);
+        smem = q8 ? split_mma_q8_smem_bytes(head_dim) : split_mma_smem_bytes(head_dim, kv8);
+        threads = q8 ? split_mma_q8_threads(head_dim) : split_mma_threads(head_dim, kv8);
     } else {
         p->rc = std::min(next_pow2(p->rows), split_max_rc(head_dim));
         smem = split_smem_bytes(head_dim, p->rc);
@@ -621,12 +625,12 @@ fdec_status fdec_run(fdec_plan_t p, const void* q, int64_t q_stride_tok, int64_t
                            1.f, 1.f, out, lse, workspace, stream);
 }
 
-fdec_status fdec_run_scaled(fdec_plan_t p, const void* q, int64_t q_stride_tok, int64_t q_stride_head,
-                            fdec_kv_desc k, fdec_kv_desc v, const int32_t* page_table, int64_t page_table_stride,
+// fdec_run_scaled and fdec_run_q8_0 (ks / vs: the q8_0 block-scale pools, else null).
+static fdec_status run_impl(fdec_plan_t p, const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                            const fdec_kv_desc& k, const fdec_kv_desc& v, const fdec_kv_desc* ks,
+                            const fdec_kv_desc* vs, const int32_t* page_table, int64_t page_table_stride,
                             const int32_t* seq_lens_dev, float scale, float k_scale, float v_scale, float* out,
                             float* lse, void* workspace, cudaStream_t stream) {
-    g_last_error.clear();
-    if (p == nullptr) return fail(FDEC_ERR_INVALID_ARG, "null plan");
     if (q == nullptr || k.base == nullptr || v.base == nullptr || page_table == nullptr || seq_lens_dev == nullptr ||
         out == nullptr)
         return fail(FDEC_ERR_INVALID_ARG, "null q, K, V, page_table, seq_lens or out");
@@ -684,6 +688,20 @@ fdec_status fdec_run_scaled(fdec_plan_t p, const void* q, int64_t q_stride_tok, 
     sp.v_sp = v.stride_page * eb;
     sp.v_sh = v.stride_head * eb;
     sp.v_st = v.stride_token * eb;
+    sp.ks_base = sp.vs_base = nullptr;
+    sp.ks_sp = sp.ks_sh = sp.ks_st = sp.vs_sp = sp.vs_sh = sp.vs_st = 0;
+    if (ks != nullptr && vs != nullptr) {  // binary16 elements -> bytes; page ids must fit every pool
+        sp.ks_base = static_cast<const uint8_t*>(ks->base);
+        sp.ks_sp = ks->stride_page * 2;
+        sp.ks_sh = ks->stride_head * 2;
+        sp.ks_st = ks->stride_token * 2;
+        sp.vs_base = static_cast<const uint8_t*>(vs->base);
+        sp.vs_sp = vs->stride_page * 2;
+        sp.vs_sh = vs->stride_head * 2;
+        sp.vs_st = vs->stride_token * 2;
+        sp.k_pages = std::min(sp.k_pages, ks->num_pages);
+        sp.v_pages = std::min(sp.v_pages, vs->num_pages);
+    }
     sp.page_table = page_table;
     sp.pt_stride = page_table_stride;
     sp.seq_lens = seq_lens_dev;
@@ -747,6 +765,40 @@ fdec_status fdec_run_scaled(fdec_plan_t p, const void* q, int64_t q_stride_tok, 
         if (e != cudaSuccess) return fail_cuda(e, "launching the reduction");
     }
     return FDEC_OK;
+}
+
+fdec_status fdec_run_scaled(fdec_plan_t p, const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                            fdec_kv_desc k, fdec_kv_desc v, const int32_t* page_table, int64_t page_table_stride,
+                            const int32_t* seq_lens_dev, float scale, float k_scale, float v_scale, float* out,
+                            float* lse, void* workspace, cudaStream_t stream) {
+    g_last_error.clear();
+    if (p == nullptr) return fail(FDEC_ERR_INVALID_ARG, "null plan");
+    if (p->q8) return fail(FDEC_ERR_INVALID_ARG, "q8_0 plans run through fdec_run_q8_0 (it takes the block scales)");
+    return run_impl(p, q, q_stride_tok, q_stride_head, k, v, nullptr, nullptr, page_table, page_table_stride,
+                    seq_lens_dev, scale, k_scale, v_scale, out, lse, workspace, stream);
+}
+
+fdec_status fdec_run_q8_0(fdec_plan_t p, const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                          fdec_kv_desc k, fdec_kv_desc k_scales, fdec_kv_desc v, fdec_kv_desc v_scales,
+                          const int32_t* page_table, int64_t page_table_stride, const int32_t* seq_lens_dev,
+                          float scale, float* out, float* lse, void* workspace, cudaStream_t stream) {
+    g_last_error.clear();
+    if (p == nullptr) return fail(FDEC_ERR_INVALID_ARG, "null plan");
+    if (!p->q8) return fail(FDEC_ERR_INVALID_ARG, "fdec_run_q8_0 needs a plan made with kv_dtype FDEC_KV_Q8_0");
+    const int64_t row = p->head_dim / 32;  // binary16 scales per (page, head, slot)
+    const fdec_kv_desc* descs[2] = {&k_scales, &v_scales};
+    for (const fdec_kv_desc* d : descs) {
+        if (d->base == nullptr) return fail(FDEC_ERR_INVALID_ARG, "null q8_0 scale pool");
+        if (d->num_pages < 1 || d->num_pages > INT32_MAX)
+            return fail(FDEC_ERR_INVALID_ARG, "q8_0 scale pools need 1 .. 2^31 - 1 pages");
+        if (reinterpret_cast<uintptr_t>(d->base) % (2 * row) != 0)
+            return fail(FDEC_ERR_LAYOUT, "q8_0 scale pool base must be aligned to head_dim / 16 bytes");
+        if (d->stride_page < 0 || d->stride_head < 0 || d->stride_token < 0 || d->stride_page % row != 0 ||
+            d->stride_head % row != 0 || d->stride_token % row != 0)
+            return fail(FDEC_ERR_LAYOUT, "q8_0 scale strides must be non-negative multiples of head_dim / 32");
+    }
+    return run_impl(p, q, q_stride_tok, q_stride_head, k, v, &k_scales, &v_scales, page_table, page_table_stride,
+                    seq_lens_dev, scale, 1.f, 1.f, out, lse, workspace, stream);
 }
 
 }  // extern "C"

@@ -43,6 +43,11 @@ struct SplitParams {
     int64_t k_pages, k_sp, k_sh, k_st;
     const uint8_t* v_base;
     int64_t v_pages, v_sp, v_sh, v_st;
+    // q8_0 caches: the binary16 block-scale rows (head_dim / 32 per token), byte strides
+    const uint8_t* ks_base;
+    int64_t ks_sp, ks_sh, ks_st;
+    const uint8_t* vs_base;
+    int64_t vs_sp, vs_sh, vs_st;
     const int32_t* page_table;
     int64_t pt_stride;
     const int32_t* seq_lens;
@@ -111,6 +116,12 @@ inline bool split_mma_persist_supported(int head_dim) {
 inline int split_mma_persist_ctas_per_sm(int head_dim) { return head_dim > 256 ? 1 : 2; }
 int split_mma_threads(int head_dim, bool kv8);
 inline bool split_mma_kv8_supported(int head_dim) { return head_dim == 128 || head_dim == 256; }
+// q8_0 caches (int8 codes in blocks of 32 with one binary16 scale each) on the
+// one-CTA-per-item tensor-core kernel, head_dim 128 and 256.
+cudaError_t launch_split_mma_q8(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int head_dim,
+                                bool bf16, dim3 grid, cudaStream_t s, bool launch);
+size_t split_mma_q8_smem_bytes(int head_dim);
+int split_mma_q8_threads(int head_dim);
 constexpr int kMmaRows = 16;
 
 // The tcgen05 dense-query split kernel (head_dim 64, 128, 192, 256; `tiles` 128-row

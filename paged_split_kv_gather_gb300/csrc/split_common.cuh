@@ -109,12 +109,13 @@ struct QChunks {
 };
 
 // Initialise the 2S full and S empty barriers (thread 0).  Pages of >= 8 tokens
-// complete a stage with one expect-tx arrival (TMA); smaller pages with the 32
-// cp.async arrivals of the producer lanes.
+// complete a stage with one expect-tx arrival (TMA; tma_full_count 33 when the 32
+// producer lanes also arrive after copying q8_0 scale rows); smaller pages with the
+// 32 cp.async arrivals of the producer lanes.
 template <int S>
 __device__ __forceinline__ void init_stage_barriers(uint64_t* full, uint64_t* empty, bool tma_mode,
-                                                    uint32_t empty_count = 1) {
-    const uint32_t full_count = tma_mode ? 1u : 32u;
+                                                    uint32_t empty_count = 1, uint32_t tma_full_count = 1) {
+    const uint32_t full_count = tma_mode ? tma_full_count : 32u;
 #pragma unroll
     for (int s = 0; s < S; ++s) {
         mbar_init(smem_addr(&full[s]), full_count);
@@ -124,14 +125,36 @@ __device__ __forceinline__ void init_stage_barriers(uint64_t* full, uint64_t* em
     fence_mbar_init();
 }
 
+// Copy the block-scale rows (SCB bytes each, K then V) of token `tok` (page, slot) into
+// row `row` of a stage's scale area [K: TOK rows][V: TOK rows].
+template <int TOK, int SCB>
+__device__ __forceinline__ void copy_scale_rows(const SplitParams& p, uint8_t* sc, int row, int64_t page, int kvh,
+                                                int slot) {
+    static_assert(SCB == 8 || SCB == 16, "scale rows of 8 or 16 bytes");
+    const uint8_t* ks = p.ks_base + page * p.ks_sp + kvh * p.ks_sh + slot * p.ks_st;
+    const uint8_t* vs = p.vs_base + page * p.vs_sp + kvh * p.vs_sh + slot * p.vs_st;
+    if constexpr (SCB == 16) {
+        cp_async_16(smem_addr(sc + row * SCB), ks);
+        cp_async_16(smem_addr(sc + (TOK + row) * SCB), vs);
+    } else {
+        cp_async_8(smem_addr(sc + row * SCB), ks);
+        cp_async_8(smem_addr(sc + (TOK + row) * SCB), vs);
+    }
+}
+
 // The producer warp: fills stage i (TOK tokens) into slot i % S once the slot is released.
-// EB: bytes per stored K/V element (2: 16-bit, 1: E4M3 codes).
-template <int D, int S, int TOK = kStageTokens, int EB = 2>
+// EB: bytes per stored K/V element (2: 16-bit, 1: E4M3 or q8_0 codes).  SCB > 0 (q8_0
+// caches): each stage also gets its tokens' K and V block-scale rows (SCB bytes each) in
+// the slot's area of sc_ring (2 TOK SCB bytes per slot); in TMA mode every lane then
+// arrives once on the stage's full barrier after its copies (which counts those 32
+// arrivals besides the expect-tx one).
+template <int D, int S, int TOK = kStageTokens, int EB = 2, int SCB = 0>
 __device__ __forceinline__ void produce_stages(const SplitParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv, uint64_t* full,
                                uint64_t* empty, uint8_t* stages, int b, int kvh, const ItemRange& ir,
-                               bool tma_mode) {
+                               bool tma_mode, uint8_t* sc_ring = nullptr) {
     using G = StageGeom<D, TOK, EB>;
     static_assert(TOK % 32 == 0 && TOK <= 256, "stage rows");
+    static_assert(SCB == 0 || TOK == 32, "scale rows: one token per lane");
     static_assert(G::ROW_BYTES % 128 == 0, "rows of whole 128-byte regions");
     const int lane = threadIdx.x & 31;
     const int tok_begin = ir.tok_begin;
@@ -197,6 +220,13 @@ __device__ __forceinline__ void produce_stages(const SplitParams& p, const CUten
                     }
                 }
             }
+            if constexpr (SCB > 0) {
+                const int tok = tok_begin + i * TOK + lane;  // lane = row of the stage
+                const int spage = __shfl_sync(0xffffffffu, pid, (box0 + lane / BR) & 31);
+                if (tok < tok_end && spage >= 0 && spage < p.k_pages && spage < p.v_pages)
+                    copy_scale_rows<TOK, SCB>(p, sc_ring + s * (2 * TOK * SCB), lane, spage, kvh, tok & page_mask);
+                cp_async_arrive_noinc(fbar);
+            }
             issued = i + 1;
         }
     } else {
@@ -235,6 +265,10 @@ __device__ __forceinline__ void produce_stages(const SplitParams& p, const CUten
                         cp_async_16(smem_addr(sbase + G::HALF_BYTES + off),
                                     p.v_base + page * p.v_sp + kvh * p.v_sh + slot * p.v_st + c * 16);
                     }
+                }
+                if constexpr (SCB > 0) {
+                    if (valid) copy_scale_rows<TOK, SCB>(p, sc_ring + s * (2 * TOK * SCB), rb + lane, my_page, kvh,
+                                                         t_lane & page_mask);
                 }
             }
             cp_async_arrive_noinc(smem_addr(&full[i % (2 * S)]));

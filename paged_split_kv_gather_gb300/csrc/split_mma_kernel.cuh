@@ -56,7 +56,7 @@
 
 namespace fdec {
 
-template <int D, bool KV8 = false>
+template <int D, bool KV8 = false, bool Q8 = false>
 struct MmaLayout {
     using G = StageGeom<D>;                                   // 16-bit tile: what the consumers read
     using GS = StageGeom<D, kStageTokens, KV8 ? 1 : 2>;       // what the producer stages
@@ -69,7 +69,7 @@ struct MmaLayout {
     // memory and four warps (3 consumers + the producer), 255 registers each.
     // head_dim 256 fits three stages and two consumers per CTA; head_dim 512
     // runs one CTA per SM (stages of 64 KB).
-    static constexpr int CTAS_PER_SM = (KV8 && D <= 128) ? 3 : (D <= 256 ? 2 : 1);
+    static constexpr int CTAS_PER_SM = (KV8 && !Q8 && D <= 128) ? 3 : (D <= 256 ? 2 : 1);
     // head_dim 512: the O accumulators of all 512 columns would need 256
     // registers, so two consumer warps share each stage, both computing S and
     // each accumulating P V for one half of the columns (DH).
@@ -82,12 +82,17 @@ struct MmaLayout {
     static constexpr int BUDGET = 232448 / CTAS_PER_SM - 1024;
     static constexpr int NP_MAX = 3;
     static constexpr int FIXED = BAR_BYTES + Q_BYTES + ALIGN_SLACK;
-    static constexpr int S_FIT = (BUDGET - FIXED) / GS::STAGE_BYTES;
+    // q8_0 caches: each slot also holds its tokens' K and V block-scale rows
+    // (head_dim / 32 binary16 values each), after the S stages.
+    static constexpr int SCB = Q8 ? D / 16 : 0;              // bytes of one token's scale row
+    static constexpr int SC_STAGE = 2 * kStageTokens * SCB;  // per slot: K rows, then V rows
+    static constexpr int S_FIT = (BUDGET - FIXED) / (GS::STAGE_BYTES + SC_STAGE);
     static constexpr int S = S_FIT > 16 ? 16 : S_FIT;
     static constexpr int NP = (S - 1) < NP_MAX ? (S - 1) : NP_MAX;  // consumer groups (stages in flight at once)
     static constexpr int NW = NP * DSPLIT;                 // consumer warps
     static constexpr int THREADS = (NW + 1) * 32;
-    static constexpr int SMEM = FIXED + S * GS::STAGE_BYTES;
+    static constexpr int SMEM = FIXED + S * (GS::STAGE_BYTES + SC_STAGE);
+    static_assert(!Q8 || KV8, "q8_0 codes are staged as bytes");
     static_assert(S >= NP + 1, "stage ring too small");
     static_assert(!KV8 || DSPLIT == 1, "E4M3 caches: one warp per stage");
     static constexpr int QMAX_OFFSET = BAR_BYTES - RC * 4;  // E4M3 caches: query row maxima
@@ -102,6 +107,19 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& p01, uint32_
         "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
         : "=r"(p01), "=r"(p23)
         : "r"(w));
+}
+
+// Four signed 8-bit codes (w's bytes, lowest first) -> two packed f16 pairs, exact:
+// the f16 with bits 0x6400 | u is 1024 + u for a byte u, so code c (u = c + 128,
+// the byte with its top bit flipped) is that value minus 1152.
+__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& p01, uint32_t& p23) {
+    const uint32_t u = w ^ 0x80808080u;
+    const __half2 bias = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6480u)));  // 1152
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140u), b = __byte_perm(u, 0x64646464u, 0x4342u);
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+    p01 = *reinterpret_cast<const uint32_t*>(&ha);
+    p23 = *reinterpret_cast<const uint32_t*>(&hb);
 }
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -172,9 +190,9 @@ __device__ __forceinline__ float q_row_factor(uint32_t mbits, bool forward) {
 // the swizzled stages, its query fragments, its running state (O accumulators
 // of this warp's DH columns; row max m and sum l of rows g and g + 8, in log2
 // units) and the work of one 32-token stage.
-template <int D, bool BF16, bool KV8>
+template <int D, bool BF16, bool KV8, bool Q8 = false>
 struct MmaWarp {
-    using Lay = MmaLayout<D, KV8>;
+    using Lay = MmaLayout<D, KV8, Q8>;
     using G = StageGeom<D>;
     using GS = typename Lay::GS;
     static constexpr int RC = Lay::RC;
@@ -257,19 +275,66 @@ struct MmaWarp {
     // One 32-token stage: S = Q K^T, masked online softmax in log2 units, O += P V.
     // nv: tokens of the stage that exist (the V rows past them are zeroed here);
     // vis0 / vis1: tokens rows g / g + 8 may see; sl: their logit scales; v_half:
-    // byte offset of this warp's DH columns of V.
+    // byte offset of this warp's DH columns of V; scl (q8_0): the stage's block-scale
+    // rows, [32 tokens][D / 32] binary16 for K, then the same for V.
     __device__ __forceinline__ void stage(const uint16_t* q_s, uint8_t* stage_ptr, int nv, int vis0, int vis1,
-                                          const float (&sl)[2], uint32_t v_half) {
+                                          const float (&sl)[2], uint32_t v_half, uint8_t* scl = nullptr) {
+        constexpr int NB = D / 32;  // q8_0 blocks per row
         const uint32_t kbase = smem_addr(stage_ptr);
         const uint32_t vbase = kbase + GS::HALF_BYTES;
-        if (nv < kStageTokens) zero_v_tail<D, kStageTokens, KV8 ? 1 : 2>(stage_ptr, nv);
+        if (nv < kStageTokens) {
+            if constexpr (Q8) {  // V scale rows past the end: 0 (their P is 0, and 0 x NaN is NaN)
+                if (lane >= nv) {
+                    if constexpr (Lay::SCB == 16)
+                        *reinterpret_cast<uint4*>(scl + (kStageTokens + lane) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    else
+                        *reinterpret_cast<uint2*>(scl + (kStageTokens + lane) * 8) = make_uint2(0u, 0u);
+                }
+            }
+            zero_v_tail<D, kStageTokens, KV8 ? 1 : 2>(stage_ptr, nv);
+        }
         const uint32_t ql = Lay::Q_IN_REGS ? 0u : q_lane(q_s);
+        const __half* sck = reinterpret_cast<const __half*>(scl);  // q8_0: K scales [32][NB], V scales after
+        const __half* scv = sck + kStageTokens * NB;
 
         // S = Q K^T for the stage's 32 tokens (4 n-tiles of 8)
         float sc[4][4];
 #pragma unroll
         for (int n = 0; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-        static_for<0, KSTEPS>([&](auto kk_) {
+        if constexpr (Q8) {
+            // q8_0: each 32-dim block (k-steps 2 blk, 2 blk + 1) into an accumulator of its
+            // own, then times the block scale of each token column (exact products: the
+            // codes and the query are exact in f16) and added to S
+            static_for<0, NB>([&](auto b_) {
+                constexpr int blk = decltype(b_)::value;
+                float acc[4][4];
+#pragma unroll
+                for (int n = 0; n < 4; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+                static_for<0, 2>([&](auto h_) {
+                    constexpr int kk = 2 * blk + decltype(h_)::value;
+                    constexpr int qk = Lay::Q_IN_REGS ? kk : 0;
+                    if constexpr (!Lay::Q_IN_REGS) load_q8(q_s, kk, qa[0]);
+                    uint32_t r[4];
+                    ldmatrix_x4(kbase + (kk >> 3) * GS::REGION_BYTES + k8_row + ((static_cast<uint32_t>(kk & 7) << 4) ^ k8_x),
+                                r[0], r[1], r[2], r[3]);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t b0, b1;
+                        i8x4_to_f16(r[j], b0, b1);
+                        mma_16816<false>(acc[j], qa[qk], b0, b1);
+                    }
+                });
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {  // columns: tokens 8 n + 2 tq and 8 n + 2 tq + 1
+                    const float d0 = __half2float(sck[(8 * n + 2 * tq) * NB + blk]);
+                    const float d1 = __half2float(sck[(8 * n + 2 * tq + 1) * NB + blk]);
+                    sc[n][0] = fmaf(acc[n][0], d0, sc[n][0]);
+                    sc[n][1] = fmaf(acc[n][1], d1, sc[n][1]);
+                    sc[n][2] = fmaf(acc[n][2], d0, sc[n][2]);
+                    sc[n][3] = fmaf(acc[n][3], d1, sc[n][3]);
+                }
+            });
+        } else static_for<0, KSTEPS>([&](auto kk_) {
             constexpr int kk = decltype(kk_)::value;
             constexpr int qk = Lay::Q_IN_REGS ? kk : 0;
             if constexpr (KV8) {
@@ -349,7 +414,7 @@ struct MmaWarp {
         // p 2^7 <= 2^15 fits f16, and small p stay normal); O then carries 2^7.
         uint32_t ph[2][4], pl[2][4];
 #pragma unroll
-        for (int k2 = 0; k2 < 2; ++k2) {
+        for (int k2 = 0; k2 < 2 && !Q8; ++k2) {
             if constexpr (P1) {
                 ph[k2][0] = pack_f16x2(sc[2 * k2][0] * kP1Scale, sc[2 * k2][1] * kP1Scale);
                 ph[k2][1] = pack_f16x2(sc[2 * k2][2] * kP1Scale, sc[2 * k2][3] * kP1Scale);
@@ -363,6 +428,60 @@ struct MmaWarp {
             }
         }
         // O += P V
+        if constexpr (Q8) {
+            // q8_0: output block blk (dims 32 blk .. + 31, chunks c = 2 blk and c + 1) takes
+            // P' = p x (V scale of the token's block blk) x 2^(7 - ex), ex such that the
+            // stage's largest |scale| of that block is below 2^ex (so |P'| <= p 2^7 <=
+            // 2^15 fits f16; the quad's lanes cover all 32 tokens), into an accumulator of
+            // its own that is added to O times 2^ex.  This lane's tokens of k-step k2:
+            // 16 k2 + 2 tq, + 1 (A registers 0, 1) and 16 k2 + 8 + 2 tq, + 1 (2, 3).
+            static_for<0, NB>([&](auto b_) {
+                constexpr int blk = decltype(b_)::value;
+                constexpr int c = 2 * blk;
+                float dv[2][4];
+                float mx = 0.f;
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        dv[k2][j] = __half2float(scv[(16 * k2 + 8 * (j >> 1) + 2 * tq + (j & 1)) * NB + blk]);
+                        mx = fmaxf(mx, fabsf(dv[k2][j]));
+                    }
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const int ex = mx > 0.f ? ((__float_as_int(mx) >> 23) & 0xff) - 126 : 0;  // mx < 2^ex
+                const float down = __int_as_float((127 - ex) << 23) * kP1Scale;
+                const float up = __int_as_float((127 + ex) << 23);
+                float acc[4][4];
+#pragma unroll
+                for (int n = 0; n < 4; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const float w0 = dv[k2][0] * down, w1 = dv[k2][1] * down;
+                    const float w2 = dv[k2][2] * down, w3 = dv[k2][3] * down;
+                    uint32_t a[4];
+                    a[0] = pack_f16x2(sc[2 * k2][0] * w0, sc[2 * k2][1] * w1);
+                    a[1] = pack_f16x2(sc[2 * k2][2] * w0, sc[2 * k2][3] * w1);
+                    a[2] = pack_f16x2(sc[2 * k2 + 1][0] * w2, sc[2 * k2 + 1][1] * w3);
+                    a[3] = pack_f16x2(sc[2 * k2 + 1][2] * w2, sc[2 * k2 + 1][3] * w3);
+                    uint32_t r[4];
+                    ldmatrix_x4_trans(vbase + (c >> 3) * GS::REGION_BYTES + v8_row[k2] +
+                                          ((static_cast<uint32_t>(c & 7) << 4) ^ v8_x),
+                                      r[0], r[1], r[2], r[3]);
+                    uint32_t ev[4], od[4];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) i8x4_to_f16(__byte_perm(r[m], 0u, 0x3120u), ev[m], od[m]);
+                    mma_16816<false>(acc[0], a, ev[0], ev[1]);
+                    mma_16816<false>(acc[1], a, od[0], od[1]);
+                    mma_16816<false>(acc[2], a, ev[2], ev[3]);
+                    mma_16816<false>(acc[3], a, od[2], od[3]);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[2 * c + i][e] = fmaf(acc[i][e], up, o[2 * c + i][e]);
+            });
+        } else
 #pragma unroll
         for (int k2 = 0; k2 < 2; ++k2) {
             if constexpr (KV8) {
@@ -406,12 +525,12 @@ struct MmaWarp {
     }
 };
 
-template <int D, bool BF16, bool KV8>
-__global__ void __launch_bounds__(MmaLayout<D, KV8>::THREADS, MmaLayout<D, KV8>::CTAS_PER_SM)
+template <int D, bool BF16, bool KV8, bool Q8 = false>
+__global__ void __launch_bounds__(MmaLayout<D, KV8, Q8>::THREADS, MmaLayout<D, KV8, Q8>::CTAS_PER_SM)
 split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
                  const __grid_constant__ CUtensorMap tmv) {
-    using Lay = MmaLayout<D, KV8>;
-    using W = MmaWarp<D, BF16, KV8>;
+    using Lay = MmaLayout<D, KV8, Q8>;
+    using W = MmaWarp<D, BF16, KV8, Q8>;
     using G = StageGeom<D>;
     using GS = typename Lay::GS;
     constexpr int NW = Lay::NW;
@@ -434,6 +553,7 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
         const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
         stages = smem + Lay::BAR_BYTES + Lay::Q_BYTES + pad;
     }
+    uint8_t* sc_ring = stages + S * GS::STAGE_BYTES;  // q8_0: [S][SC_STAGE] block-scale rows
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -442,7 +562,7 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
     const int kvh = blockIdx.y;
     const int row0 = blockIdx.z * RC;
     const bool tma_mode = p.page_shift >= 3;
-    if (threadIdx.x == 0) init_stage_barriers<S>(full, empty, tma_mode, DSPLIT);
+    if (threadIdx.x == 0) init_stage_barriers<S>(full, empty, tma_mode, DSPLIT, Q8 ? 33u : 1u);
     __syncthreads();  // barriers initialised (nothing before this waits on memory)
     const ItemRange ir = item_range(p, it);
 
@@ -452,7 +572,8 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
             prefetch_tmap(&tmk);
             prefetch_tmap(&tmv);
         }
-        produce_stages<D, S, kStageTokens, KV8 ? 1 : 2>(p, &tmk, &tmv, full, empty, stages, b, kvh, ir, tma_mode);
+        produce_stages<D, S, kStageTokens, KV8 ? 1 : 2, Lay::SCB>(p, &tmk, &tmv, full, empty, stages, b, kvh, ir,
+                                                                tma_mode, sc_ring);
         return;
     }
     if (threadIdx.x == 0) report_item_range(p, ir);
@@ -533,7 +654,7 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
         const int t0 = ir.tok_begin + i * kStageTokens;
         const int nv = min(kStageTokens, ir.tok_end - t0);
         cw.stage(q_s, stages + s * GS::STAGE_BYTES, nv, min(nv, lim[0] - t0 + 1), min(nv, lim[1] - t0 + 1), sl,
-                 v_half);
+                 v_half, Q8 ? sc_ring + s * Lay::SC_STAGE : nullptr);
         if (nv < kStageTokens) fence_proxy_async_shared();  // generic zeroing before the slot's next TMA write
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
@@ -578,22 +699,22 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
     merge_and_store<NP, RC, D, NW * 32>(p, it, kvh, row0, sm_m, sm_l, sm_o);
 }
 
-template <int D, bool BF16, bool KV8 = false>
+template <int D, bool BF16, bool KV8 = false, bool Q8 = false>
 cudaError_t launch_split_mma_one(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
                                  cudaStream_t stream, bool launch) {
-    using Lay = MmaLayout<D, KV8>;
+    using Lay = MmaLayout<D, KV8, Q8>;
     static unsigned long long attr_done = 0;  // one bit per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-        e = cudaFuncSetAttribute(split_mma_kernel<D, BF16, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(split_mma_kernel<D, BF16, KV8, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Lay::SMEM);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_RELEASE);
     }
     if (!launch) return cudaSuccess;
-    split_mma_kernel<D, BF16, KV8><<<grid, Lay::THREADS, Lay::SMEM, stream>>>(p, tk, tv);
+    split_mma_kernel<D, BF16, KV8, Q8><<<grid, Lay::THREADS, Lay::SMEM, stream>>>(p, tk, tv);
     return cudaGetLastError();
 }
 

@@ -19,7 +19,12 @@ Recipe (all draws seeded):
   * "peaked": q multiplied by 8 (exact in 16-bit), so the softmax is sharp and
     a misread key or value moves the output well past the tolerance;
   * quantised caches (kv_dtype "fp8"): K and V drawn the same way and rounded
-    to 8-bit E4M3 (torch.float8_e4m3fn), q stays 16-bit.
+    to 8-bit E4M3 (torch.float8_e4m3fn), q stays 16-bit;
+  * q8_0 caches (kv_dtype "q8_0"): K codes, V codes (uniform int8 in
+    [-128, 127]), then K and V block scales (log-uniform in [0.005, 0.05],
+    stored as binary16: the size of max|x| / 127 for unit-variance values), each
+    pool in the same layout as the codes with head_dim / 32 scales per row.  No
+    quantisation is done: codes and scales are drawn as they are stored.
 
 The five named workloads follow the shapes of the pages' workloads: a tiny
 decode, a batched GQA decode at exactly 32 blocks of 64 tokens, the 32q/4kv/128
@@ -40,7 +45,8 @@ LONG_CONTEXT_LENGTHS = (1900, 2000, 2100, 3000, 4800, 32768, 131072, 262144)
 RAGGED_HEAD_DIMS = (192, 256, 512)
 MULTI_TOKEN_Q_LENS = (4, 8, 2048)
 
-_TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16, "fp8": torch.float8_e4m3fn}
+_TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16, "fp8": torch.float8_e4m3fn, "q8_0": torch.int8,
+                "q8_0_scale": torch.float16}
 _NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0, "fp8": 0x7F}
 
 
@@ -65,7 +71,9 @@ class Workload:
     v: torch.Tensor               # [pages, Hk, P, D] view
     layout: str = "hnd"
     keep: List[torch.Tensor] = field(default_factory=list)
-    kv_dtype: str = ""            # "" = the q dtype; "fp8" = E4M3 K/V codes
+    kv_dtype: str = ""            # "" = the q dtype; "fp8" = E4M3 K/V codes; "q8_0" = int8 codes + block scales
+    k_scales: Optional[torch.Tensor] = None  # q8_0: binary16 [pages, Hk, P, D / 32] views
+    v_scales: Optional[torch.Tensor] = None
 
     @property
     def kv_fp8(self) -> bool:
@@ -77,9 +85,12 @@ class Workload:
 
     @property
     def kv_bytes(self) -> int:
-        """Algorithmic K+V bytes one call reads: sum_b L_b * Hk * D * 2 (K and V) * element bytes."""
-        eb = 1 if self.kv_fp8 else 2
-        return int(np.sum(self.seq_lens.astype(np.int64))) * self.num_kv_heads * self.head_dim * 2 * eb
+        """Algorithmic K+V bytes one call reads: sum_b L_b * Hk * 2 (K and V) * (D * element bytes, plus
+        D / 32 binary16 block scales for q8_0)."""
+        row = self.head_dim * (1 if self.kv_dtype in ("fp8", "q8_0") else 2)
+        if self.kv_dtype == "q8_0":
+            row += (self.head_dim // 32) * 2
+        return int(np.sum(self.seq_lens.astype(np.int64))) * self.num_kv_heads * 2 * row
 
     def to(self, device) -> "Workload":
         """Copy every tensor to ``device`` keeping views and strides (storage is copied whole)."""
@@ -93,10 +104,12 @@ class Workload:
             nb = memo[key]
             return nb.as_strided(t.shape, t.stride(), t.storage_offset())
 
+        ks = None if self.k_scales is None else move(self.k_scales)
+        vs = None if self.v_scales is None else move(self.v_scales)
         return Workload(self.name, self.dtype, self.batch, self.q_len, self.num_qo_heads,
                         self.num_kv_heads, self.head_dim, self.page_size, self.causal, self.scale,
                         self.seq_lens.copy(), self.page_table.copy(), move(self.q), move(self.k),
-                        move(self.v), self.layout, list(memo.values()), self.kv_dtype)
+                        move(self.v), self.layout, list(memo.values()), self.kv_dtype, ks, vs)
 
 
 def _flat_storage(t: torch.Tensor) -> torch.Tensor:
@@ -121,6 +134,11 @@ def storage_view(t: torch.Tensor):
 
 
 def _randn(gen: torch.Generator, shape, device, dtype: str) -> torch.Tensor:
+    if dtype == "q8_0":          # codes, uniform over the signed bytes
+        return torch.randint(-128, 128, shape, generator=gen, device=device, dtype=torch.int8)
+    if dtype == "q8_0_scale":    # block scales, log-uniform in [0.005, 0.05]
+        u = torch.rand(shape, generator=gen, device=device, dtype=torch.float32)
+        return torch.exp(math.log(0.005) + u * (math.log(0.05) - math.log(0.005))).to(torch.float16)
     x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
     return x.to(_TORCH_DTYPE[dtype])
 
@@ -187,7 +205,8 @@ def make(batch: int, q_len: int, num_qo_heads: int, num_kv_heads: int, head_dim:
     "head_major" (a [Hq, B*Q, D] tensor viewed as [B,Q,Hq,D]).
     nan_guard: fill every K/V element that must never be read (slots past L in a
     sequence's last page, and pages no sequence references) with NaN.
-    kv_dtype: "" (K/V in the q dtype) or "fp8" (E4M3 K/V codes).
+    kv_dtype: "" (K/V in the q dtype), "fp8" (E4M3 K/V codes) or "q8_0" (int8 codes and
+    binary16 block-scale pools in the same layout).
     """
     rng = np.random.Generator(np.random.PCG64(seed))
     lens = np.asarray(seq_lens, dtype=np.int64).reshape(-1)
@@ -220,14 +239,25 @@ def make(batch: int, q_len: int, num_qo_heads: int, num_kv_heads: int, head_dim:
 
     kvd = kv_dtype or dtype
     k, v, keep = _alloc_pool(pool, hk, page_size, d, layout, gen, device, kvd)
+    ks = vs = None
+    if kvd == "q8_0":
+        if d % 32 != 0:
+            raise ValueError("q8_0 rows are blocks of 32")
+        if spikes > 0:
+            raise ValueError("spikes are drawn into 16-bit or E4M3 keys only")
+        ks, vs, skeep = _alloc_pool(pool, hk, page_size, d // 32, layout, gen, device, "q8_0_scale")
+        keep = keep + skeep
 
     if spikes > 0:
         _add_spikes(rng, k, q, table, lens, page_size, sc, spikes, hq // hk)
     if nan_guard:
-        _nan_fill_unread(k, v, table, lens, page_size, kvd)
+        if kvd == "q8_0":  # int8 codes have no NaN: the scales of unread rows carry it
+            _nan_fill_unread(ks, vs, table, lens, page_size, "f16")
+        else:
+            _nan_fill_unread(k, v, table, lens, page_size, kvd)
 
     return Workload(name, dtype, batch, q_len, hq, hk, d, page_size, causal, sc,
-                    lens.astype(np.int32), table, q, k, v, layout, q_keep + keep, kv_dtype)
+                    lens.astype(np.int32), table, q, k, v, layout, q_keep + keep, kv_dtype, ks, vs)
 
 
 def _add_spikes(rng, k, q, table, lens, page_size, scale, frac, g):

@@ -10,10 +10,12 @@ from paged_split_kv_gather_gb300.workloads import Workload, q_token_stride, stor
 
 def np_storage(t: torch.Tensor):
     """(numpy array over t's whole CPU storage, element offset): uint16 for 16-bit
-    tensors, uint8 (E4M3 codes) for float8_e4m3fn."""
+    tensors, uint8 (E4M3 codes) for float8_e4m3fn, int8 (q8_0 codes) for int8."""
     flat, off, _ = storage_view(t)
     if t.dtype == torch.float8_e4m3fn:
         return flat.view(torch.uint8).numpy(), off
+    if t.dtype == torch.int8:
+        return flat.numpy(), off
     return flat.view(torch.int16).numpy().view(np.uint16), off
 
 
@@ -27,12 +29,14 @@ def oracle_run(w: Workload, rows=None, n_threads: int = 0, seq_lens=None, k_scal
     assert w.q.device.type == "cpu"
     q_arr, q_off = np_storage(w.q)
     lens = w.seq_lens if seq_lens is None else seq_lens
+    q8 = w.kv_dtype == "q8_0"
     return oracle.paged_attention(
         q_arr, q_off, q_token_stride(w.q), w.q.stride(2), oracle_pool(w.k), oracle_pool(w.v),
         w.page_table, lens, q_len=w.q_len, num_qo_heads=w.num_qo_heads,
         num_kv_heads=w.num_kv_heads, head_dim=w.head_dim, page_size=w.page_size,
         is_bf16=(w.dtype == "bf16"), causal=w.causal, scale=w.scale, rows=rows,
-        n_threads=n_threads, k_scale=k_scale, v_scale=v_scale)
+        n_threads=n_threads, k_scale=k_scale, v_scale=v_scale,
+        k_scales=oracle_pool(w.k_scales) if q8 else None, v_scales=oracle_pool(w.v_scales) if q8 else None)
 
 
 def gather_tokens(w: Workload, pool: torch.Tensor, b: int, kvh: int, n: int) -> np.ndarray:
@@ -94,7 +98,12 @@ def gpu_run(w: Workload, capacities=None, seq_lens=None, stream=None, k_scale=No
     lens = torch.as_tensor(w.seq_lens if seq_lens is None else seq_lens, dtype=torch.int32, device=dev)
     # every storage the workload holds (q and the K/V pools) must come back bit-identical
     before = [t.clone() for t in w.keep]
-    pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale, stream=stream, k_scale=k_scale, v_scale=v_scale)
+    if w.kv_dtype == "q8_0":
+        pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale, stream=stream, k_scales=w.k_scales,
+               v_scales=w.v_scales)
+    else:
+        pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale, stream=stream, k_scale=k_scale,
+               v_scale=v_scale)
     for a, b in zip(before, w.keep):
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), "an input buffer changed"
     return out, lse, pd

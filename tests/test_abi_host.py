@@ -283,6 +283,43 @@ def test_e4m3_strides_are_checked_in_bytes_and_scales_must_be_finite():
         assert _run_scaled_raw(plan, good, good, ks, vs) == "FDEC_ERR_INVALID_ARG"
 
 
+def test_q8_0_cache_plans_on_the_mma_path_only():
+    for d in (128, 256):
+        info = fd.fdec_plan_get_info(_plan([1000], head_dim=d, kv_dtype="q8_0"))
+        assert info["path"] == fd.FDEC_PATH_MMA
+        assert info["num_split_ctas"] == info["num_items"] * info["row_groups"] * 8  # one CTA per unit (8 KV heads)
+    for kw in (dict(head_dim=64), dict(head_dim=192), dict(head_dim=512), dict(path=fd.FDEC_PATH_TC),
+               dict(path=fd.FDEC_PATH_SIMT)):
+        with pytest.raises(fd.FdecError) as ei:
+            _plan([1000], kv_dtype="q8_0", **kw)
+        assert ei.value.status_name == "FDEC_ERR_UNSUPPORTED"
+
+
+def _run_q8_raw(plan, k, ks, v, vs):
+    lib = fd._load()
+    st = lib.fdec_run_q8_0(plan.handle, 0x10000, 128, 128 * 8, k, ks, v, vs, 0x40000, 256, 0x50000,
+                           ctypes.c_float(0.1), 0x20000, None, 0x30000, None)
+    return fd.STATUS_NAMES[st]
+
+
+def test_q8_0_entry_points_and_scale_pool_layout_checks():
+    plan = _plan([2048], num_qo_heads=8, num_kv_heads=1, head_dim=128, kv_dtype="q8_0")
+    codes = fd.KVDesc(0x100000, 10, 16 * 128, 0, 128)
+    scales = fd.KVDesc(0x200000, 10, 16 * 4, 0, 4)  # [pages, 1, 16, 4] binary16
+    assert _run_q8_raw(plan, codes, scales, codes, scales) == "FDEC_ERR_WORKSPACE"  # valid, never uploaded
+    # the 16-bit entry points refuse a q8_0 plan (they have no scale pools)
+    assert _run_scaled_raw(plan, codes, codes) == "FDEC_ERR_INVALID_ARG"
+    # scale rows must start on head_dim / 16 bytes: base, then each stride
+    assert _run_q8_raw(plan, codes, fd.KVDesc(0x200004, 10, 64, 0, 4), codes, scales) == "FDEC_ERR_LAYOUT"
+    assert _run_q8_raw(plan, codes, scales, codes, fd.KVDesc(0x200000, 10, 66, 0, 4)) == "FDEC_ERR_LAYOUT"
+    assert _run_q8_raw(plan, codes, fd.KVDesc(0x200000, 10, 64, 0, 6), codes, scales) == "FDEC_ERR_LAYOUT"
+    assert _run_q8_raw(plan, codes, fd.KVDesc(0x200000, 0, 64, 0, 4), codes, scales) == "FDEC_ERR_INVALID_ARG"
+    assert _run_q8_raw(plan, codes, fd.KVDesc(0, 10, 64, 0, 4), codes, scales) == "FDEC_ERR_INVALID_ARG"
+    # the q8_0 entry point refuses a plan of another cache type
+    plan16 = _plan([2048], num_qo_heads=8, num_kv_heads=1, head_dim=128)
+    assert _run_q8_raw(plan16, codes, scales, codes, scales) == "FDEC_ERR_INVALID_ARG"
+
+
 def test_binding_refuses_k_v_of_the_wrong_element_size():
     import torch
 
