@@ -280,6 +280,38 @@ def _e4m3_point(dev, calls, hbm_peak, flush):
             "scales": {"k_scale": 0.5, "v_scale": 2.0}}
 
 
+def _q8_point(dev, calls, hbm_peak, flush):
+    """q8_0 cache: the long-context shape (262144 tokens, 32/4 heads, D 128, page 64,
+    bf16 queries) over int8 codes with binary16 block scales (no spikes: the keys are
+    drawn as codes); kv_bytes counts the codes and the scales."""
+    import torch
+
+    import paged_split_kv_gather_gb300 as fd
+    from paged_split_kv_gather_gb300 import workloads as W
+
+    w = W.make(1, 1, 32, 4, 128, 64, [262144], dtype="bf16", seed=0, device=dev, kv_dtype="q8_0",
+               name="long_context_q8_0_L262144")
+    pd = fd.PagedDecode(w.seq_lens, 1, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
+                        device=dev, kv_dtype="q8_0")
+    table = torch.as_tensor(w.page_table, device=dev)
+    lens = torch.as_tensor(w.seq_lens, device=dev)
+    out = torch.empty((1, 1, w.num_qo_heads, w.head_dim), device=dev)
+    lse = torch.empty((1, 1, w.num_qo_heads), device=dev)
+
+    def run():
+        pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale, k_scales=w.k_scales, v_scales=w.v_scales)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    med, mn = _time_calls(torch, run, calls, flush)
+    assert pd.device_errors() == 0
+    gbs = w.kv_bytes / (med * 1e-6) / 1e9
+    return {"us_per_call": round(med, 2), "us_min": round(mn, 2), "kv_bytes": int(w.kv_bytes),
+            "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / hbm_peak, 4), "path": int(pd.info["path"]),
+            "launches": int(pd.info["launches"]), "max_splits": int(pd.info["max_splits"])}
+
+
 def _config_points(dev, calls, hbm_peak):
     """The other workloads' µs/call and GB/s (tiny decode, batched GQA decode, the
     ragged serving batch at head_dim 192/256/512), a no-cliff sweep of the long-context
@@ -354,6 +386,8 @@ def _config_points(dev, calls, hbm_peak):
     torch.cuda.empty_cache()
 
     points["long_context_e4m3_L262144"] = _e4m3_point(dev, calls, hbm_peak, flush)
+    torch.cuda.empty_cache()
+    points["long_context_q8_0_L262144"] = _q8_point(dev, calls, hbm_peak, flush)
     torch.cuda.empty_cache()
 
     # Graph-replayed long-context points where launch latency matters.
@@ -576,6 +610,15 @@ def _run_fdec(args):
         # Several replicas: the headline step, its roofline and end-to-end numbers only.  The
         # per-workload points characterise one GPU and would hold every GPU for another minute.
         args.no_sweep = args.no_configs = args.no_dense = True
+    if args.only_q8:
+        # The q8_0 long-context point alone (profiling the q8_0 kernel); not a bench line.
+        peak, _ = _peaks()
+        pt = _q8_point(dev, args.sweep_calls, peak, L2Flush(torch, dev))
+        if rank == 0:
+            print(json.dumps({"long_context_q8_0_L262144": pt}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     if args.only_e4m3:
         # The quantised-cache long-context point alone (profiling the E4M3 kernel); not a bench line.
         peak, _ = _peaks()
@@ -1006,6 +1049,8 @@ def main():
     ap.add_argument("--only-long", type=int, default=0, metavar="L",
                     help="run only flushed calls of the long-context shape at L tokens and print them "
                          "(profiling; no bench line)")
+    ap.add_argument("--only-q8", action="store_true",
+                    help="time only the q8_0 long-context point (for profiling); prints that point, not a bench line")
     ap.add_argument("--only-e4m3", action="store_true",
                     help="run only the E4M3 (fp8) long-context point and print it (profiling; no bench line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -186,6 +186,29 @@ __device__ __forceinline__ float q_row_factor(uint32_t mbits, bool forward) {
     return __int_as_float((127 + (forward ? sh : -sh)) << 23);
 }
 
+// q8_0: the NB binary16 block scales of tokens t and t + 1 (rows of NB values, consecutive
+// in shared memory) as NB 32-bit words: token t's in words 0 .. NB/2 - 1, t + 1's after.
+template <int NB>
+__device__ __forceinline__ void load_scale_pair(const __half* rows, int t, uint32_t (&w)[NB]) {
+    static_assert(NB % 4 == 0, "two rows of NB binary16 values: whole 16-byte chunks");
+    const uint4* src = reinterpret_cast<const uint4*>(rows + t * NB);
+#pragma unroll
+    for (int i = 0; i < NB / 4; ++i) {
+        const uint4 x = src[i];
+        w[4 * i] = x.x;
+        w[4 * i + 1] = x.y;
+        w[4 * i + 2] = x.z;
+        w[4 * i + 3] = x.w;
+    }
+}
+
+// Scale of block blk of the first (u = 0) or second (u = 1) token of a pair from load_scale_pair.
+template <int NB>
+__device__ __forceinline__ float pair_scale(const uint32_t (&w)[NB], int u, int blk) {
+    const uint32_t word = w[u * (NB / 2) + (blk >> 1)];
+    return __half2float(__ushort_as_half(static_cast<unsigned short>((blk & 1) ? (word >> 16) : (word & 0xFFFFu))));
+}
+
 // One consumer warp of the tensor-core split kernels: its lane addressing into
 // the swizzled stages, its query fragments, its running state (O accumulators
 // of this warp's DH columns; row max m and sum l of rows g and g + 8, in log2
@@ -305,6 +328,9 @@ struct MmaWarp {
             // q8_0: each 32-dim block (k-steps 2 blk, 2 blk + 1) into an accumulator of its
             // own, then times the block scale of each token column (exact products: the
             // codes and the query are exact in f16) and added to S
+            uint32_t ksc[4][NB];  // n-tile n: scales of tokens 8 n + 2 tq and 8 n + 2 tq + 1
+#pragma unroll
+            for (int n = 0; n < 4; ++n) load_scale_pair<NB>(sck, 8 * n + 2 * tq, ksc[n]);
             static_for<0, NB>([&](auto b_) {
                 constexpr int blk = decltype(b_)::value;
                 float acc[4][4];
@@ -326,8 +352,8 @@ struct MmaWarp {
                 });
 #pragma unroll
                 for (int n = 0; n < 4; ++n) {  // columns: tokens 8 n + 2 tq and 8 n + 2 tq + 1
-                    const float d0 = __half2float(sck[(8 * n + 2 * tq) * NB + blk]);
-                    const float d1 = __half2float(sck[(8 * n + 2 * tq + 1) * NB + blk]);
+                    const float d0 = pair_scale<NB>(ksc[n], 0, blk);
+                    const float d1 = pair_scale<NB>(ksc[n], 1, blk);
                     sc[n][0] = fmaf(acc[n][0], d0, sc[n][0]);
                     sc[n][1] = fmaf(acc[n][1], d1, sc[n][1]);
                     sc[n][2] = fmaf(acc[n][2], d0, sc[n][2]);
@@ -435,6 +461,11 @@ struct MmaWarp {
             // 2^15 fits f16; the quad's lanes cover all 32 tokens), into an accumulator of
             // its own that is added to O times 2^ex.  This lane's tokens of k-step k2:
             // 16 k2 + 2 tq, + 1 (A registers 0, 1) and 16 k2 + 8 + 2 tq, + 1 (2, 3).
+            uint32_t vsc[2][2][NB];  // [k2][h]: scales of tokens 16 k2 + 8 h + 2 tq and + 1
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) load_scale_pair<NB>(scv, 16 * k2 + 8 * h + 2 * tq, vsc[k2][h]);
             static_for<0, NB>([&](auto b_) {
                 constexpr int blk = decltype(b_)::value;
                 constexpr int c = 2 * blk;
@@ -444,7 +475,7 @@ struct MmaWarp {
                 for (int k2 = 0; k2 < 2; ++k2)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        dv[k2][j] = __half2float(scv[(16 * k2 + 8 * (j >> 1) + 2 * tq + (j & 1)) * NB + blk]);
+                        dv[k2][j] = pair_scale<NB>(vsc[k2][j >> 1], j & 1, blk);
                         mx = fmaxf(mx, fabsf(dv[k2][j]));
                     }
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
