@@ -321,7 +321,8 @@ fdec_status fdec_read_device_errors(fdec_plan_t plan, void* workspace, uint32_t*
  * cudaMalloc because it may synchronise the device.  Inputs and outputs are
  * as for fdec_run, and so is the result: the cache is read unscaled
  * (k_scale = v_scale = 1), as fdec_run reads it; scaled caches go through
- * fdec_run_scaled with a workspace.  The partials and work lists live in a
+ * fdec_run_scaled with a workspace, and q8_0 plans are refused as fdec_run
+ * refuses them (they need fdec_run_q8_0 with a workspace).  The partials and work lists live in a
  * 16 MiB array built into the library, which every GPU that loads the library
  * keeps until the process exits.  A plan whose workspace_bytes exceeds 16 MiB
  * is rejected with FDEC_ERR_WORKSPACE (use fdec_run with your own workspace).
