@@ -70,7 +70,7 @@ def _attention_flops(w) -> float:
 def _dense_query(dev, calls, hbm_peak, q_lens=(4, 8, 2048)):
     """Multi-token queries over the paged cache (batch 4, 32/8 heads, D 128, bf16,
     page 16, prefix 8192 + q_len, causal): q_len 4 and 8 (speculative decode) and
-    2048 (a prefill chunk).  q_len x group > 16 takes the tcgen05 path, also
+    2048 (a prefill chunk).  q_len x group > 16 takes the tcgen05 path (> 32 at head_dim 256), also
     timed on the 16-row warp-level kernel for comparison."""
     import torch
 
@@ -130,7 +130,7 @@ def _dense_query(dev, calls, hbm_peak, q_lens=(4, 8, 2048)):
 def _crossover(dev, calls):
     """16-row warp-level kernel against the tcgen05 kernel per head_dim and row count
     (rows = q_len x group): batch 4, 32/8 heads, KV 8192 + q_len, causal, bf16, page 16.
-    The planner's AUTO rule takes tcgen05 above 16 rows for head_dim 64-256."""
+    The planner's AUTO rule takes tcgen05 above 16 rows for head_dim 64-192 and above 32 at 256."""
     import torch
 
     import paged_split_kv_gather_gb300 as fd

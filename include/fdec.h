@@ -96,12 +96,12 @@ typedef struct fdec_plan_s* fdec_plan_t;
  * default.  TC: 5th-generation tensor cores (tcgen05, accumulators in tensor
  * memory) on 128-row query tiles, head_dim 64, 128, 192 and 256 (at 512 the
  * output accumulator alone would fill tensor memory); chosen by AUTO when q_len
- * x group > 16, where attention over the gathered pages turns into a dense
- * contraction (speculative-decode and prefill chunks) and the 16-row kernel
- * would stream K/V once per 16-row group.  Up to 16 rows the work is bound by
- * streaming K/V and the 16-row kernel wastes no tensor-core tile (measured
- * crossover: the 16-row kernel is faster at 16 rows and slower at 32 for every
- * head_dim the TC path is built for).
+ * x group > 16 (> 32 at head_dim 256), where attention over the gathered pages
+ * turns into a dense contraction (speculative-decode and prefill chunks) and the
+ * 16-row kernel would stream K/V once per 16-row group.  Up to 16 rows the work
+ * is bound by streaming K/V and the 16-row kernel wastes no tensor-core tile
+ * (measured crossover: the 16-row kernel is faster at 16 rows for every head_dim
+ * the TC path is built for, and at 32 rows for head_dim 256; slower above).
  */
 enum { FDEC_PATH_AUTO = 0, FDEC_PATH_SIMT = 1, FDEC_PATH_MMA = 2, FDEC_PATH_TC = 3 };
 
@@ -125,8 +125,8 @@ enum { FDEC_KV_SAME = 0, FDEC_KV_E4M3 = 1, FDEC_KV_Q8_0 = 2 };
 /* Plan options; pass NULL for the defaults (all fields 0). */
 typedef struct {
     int blocks_per_split;  /* 64-token blocks per split; 0 = auto; 1 = one partial per block */
-    int reducer_fanin;     /* partials merged per reduction task; 0 = auto (256); >= 2 */
-    int path;              /* FDEC_PATH_AUTO (TC when head_dim <= 256 and q_len x group > 16, else
+    int reducer_fanin;     /* partials merged per reduction task; 0 = auto (1024); >= 2 */
+    int path;              /* FDEC_PATH_AUTO (TC when head_dim <= 256 and q_len x group > 16, > 32 at 256, else
                               MMA), _SIMT, _MMA (every head_dim), _TC (head_dim 64, 128, 192, 256) */
     int num_sms;           /* 0 = query the current device; > 0 plans without a device */
     int kv_dtype;          /* FDEC_KV_SAME (0), FDEC_KV_E4M3 or FDEC_KV_Q8_0 (head_dim 128 / 256; path AUTO

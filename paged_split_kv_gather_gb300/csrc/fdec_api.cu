@@ -396,7 +396,7 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
     if (kv8)
         p->path = FDEC_PATH_MMA;
     else if (o.path == FDEC_PATH_AUTO)
-        p->path = (tc_ok && p->rows > kMmaRows) ? FDEC_PATH_TC : (mma_ok ? FDEC_PATH_MMA : FDEC_PATH_SIMT);
+        p->path = (tc_ok && p->rows > tc_min_rows(head_dim)) ? FDEC_PATH_TC : (mma_ok ? FDEC_PATH_MMA : FDEC_PATH_SIMT);
     else
         p->path = o.path;
     p->persistent = p->path == FDEC_PATH_MMA && !kv8 && split_mma_persist_supported(head_dim);

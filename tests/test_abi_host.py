@@ -362,7 +362,8 @@ def test_plan_invariants_hold_for_random_batches():
             assert C == bps
         nb = np.maximum(1, -(-np.asarray(lens, dtype=np.int64) // 64))
         rows = q_len * group
-        want_path = fd.FDEC_PATH_TC if (not kv8 and d in (64, 128, 192, 256) and rows > 16) else fd.FDEC_PATH_MMA
+        want_path = (fd.FDEC_PATH_TC if (not kv8 and d in (64, 128, 192, 256) and rows > (32 if d == 256 else 16))
+                     else fd.FDEC_PATH_MMA)
         assert info["path"] == want_path
         # the persistent kernel (16-bit caches on the 16-row path; one CTA per SM at head_dim 512)
         persistent = want_path == fd.FDEC_PATH_MMA and not kv8
