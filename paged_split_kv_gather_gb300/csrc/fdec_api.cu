@@ -314,6 +314,12 @@ void log_plan(const fdec_plan_s* p) {
 
 }  // namespace
 
+// AUTO takes the tcgen05 kernel above this many rows (q_len x group): measured per
+// head_dim, the 16-row kernel is faster at 16 rows everywhere and, at head_dim 256,
+// still at 32 rows (102 against 120 us); the tcgen05 kernel from 32 rows below 256
+// and from 64 at 256.
+static int tc_min_rows(int head_dim) { return head_dim >= 256 ? 32 : kMmaRows; }
+
 extern "C" {
 
 const char* fdec_last_error(void) { return g_last_error.c_str(); }

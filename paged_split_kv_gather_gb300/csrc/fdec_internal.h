@@ -123,11 +123,6 @@ cudaError_t launch_split_mma_q8(const SplitParams& p, const CUtensorMap& tk, con
 size_t split_mma_q8_smem_bytes(int head_dim);
 int split_mma_q8_threads(int head_dim);
 constexpr int kMmaRows = 16;
-// AUTO takes the tcgen05 kernel above this many rows (q_len x group): measured per
-// head_dim, the 16-row kernel is faster at 16 rows everywhere and, at head_dim 256,
-// still at 32 rows (102 against 120 us); the tcgen05 kernel from 32 rows below 256
-// and from 64 at 256.
-inline int tc_min_rows(int head_dim) { return head_dim >= 256 ? 32 : kMmaRows; }
 
 // The tcgen05 dense-query split kernel (head_dim 64, 128, 192, 256; `tiles` 128-row
 // query tiles per CTA: 1 or 2 for head_dim 64 and 128, 1 above; 64-token stages: its
