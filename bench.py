@@ -259,21 +259,22 @@ def _time_graph_once(torch, run_all):
 
 def _back_to_back_us(torch, w, run_kv, reps_min=20):
     """µs per call back to back: a CUDA graph of calls rotating over n copies of the
-    K/V pools (n such that ~256 MB, twice the L2, are streamed between two reads of
-    one copy), best of 5 replays / calls.  run_kv(k, v) runs one call on given pools."""
+    K/V pools (and of q8_0 scale pools; n such that ~256 MB, twice the L2, are
+    streamed between two reads of one copy), best of 5 replays / calls.
+    run_kv(k, v, *scale_pools) runs one call on given pools."""
     n = 1 + -(-(256 << 20) // int(w.kv_bytes))
-    kc = [w.k] + [w.k.clone() for _ in range(n - 1)]
-    vc = [w.v] + [w.v.clone() for _ in range(n - 1)]
+    pools = [w.k, w.v] + ([w.k_scales, w.v_scales] if w.kv_dtype == "q8_0" else [])
+    copies = [[t] + [t.clone() for _ in range(n - 1)] for t in pools]
     reps = n * max(1, -(-reps_min // n))
 
     def run_all():
         for c in range(reps):
-            run_kv(kc[c % n], vc[c % n])
+            run_kv(*(cp[c % n] for cp in copies))
 
     run_all()
     torch.cuda.synchronize()
     us = _time_graph_once(torch, run_all) / reps
-    del kc, vc
+    del copies
     return us, n
 
 
@@ -301,10 +302,15 @@ def _e4m3_point(dev, calls, hbm_peak, flush):
     torch.cuda.synchronize()
     med, mn = _time_calls(torch, run, calls, flush)
     gbs = w.kv_bytes / (med * 1e-6) / 1e9
+    b2b, n = _back_to_back_us(torch, w, lambda k, v: pd.run(w.q, k, v, table, lens, out, lse, scale=w.scale,
+                                                            k_scale=0.5, v_scale=2.0))
+    g_b = w.kv_bytes / (b2b * 1e-6) / 1e9
     return {"us_per_call": round(med, 2), "us_min": round(mn, 2), "kv_bytes": int(w.kv_bytes),
-            "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / hbm_peak, 4), "path": int(pd.info["path"]),
-            "launches": int(pd.info["launches"]), "max_splits": int(pd.info["max_splits"]),
-            "scales": {"k_scale": 0.5, "v_scale": 2.0}}
+            "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / hbm_peak, 4),
+            "back_to_back_us_per_call": round(b2b, 2), "back_to_back_GB_per_s": round(g_b, 1),
+            "back_to_back_frac_of_peak": round(g_b / hbm_peak, 4), "back_to_back_pool_copies": n,
+            "path": int(pd.info["path"]), "launches": int(pd.info["launches"]),
+            "max_splits": int(pd.info["max_splits"]), "scales": {"k_scale": 0.5, "v_scale": 2.0}}
 
 
 def _q8_point(dev, calls, hbm_peak, flush):
@@ -334,9 +340,15 @@ def _q8_point(dev, calls, hbm_peak, flush):
     med, mn = _time_calls(torch, run, calls, flush)
     assert pd.device_errors() == 0
     gbs = w.kv_bytes / (med * 1e-6) / 1e9
+    b2b, n = _back_to_back_us(torch, w, lambda k, v, ks, vs: pd.run(w.q, k, v, table, lens, out, lse, scale=w.scale,
+                                                                    k_scales=ks, v_scales=vs))
+    g_b = w.kv_bytes / (b2b * 1e-6) / 1e9
     return {"us_per_call": round(med, 2), "us_min": round(mn, 2), "kv_bytes": int(w.kv_bytes),
-            "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / hbm_peak, 4), "path": int(pd.info["path"]),
-            "launches": int(pd.info["launches"]), "max_splits": int(pd.info["max_splits"])}
+            "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / hbm_peak, 4),
+            "back_to_back_us_per_call": round(b2b, 2), "back_to_back_GB_per_s": round(g_b, 1),
+            "back_to_back_frac_of_peak": round(g_b / hbm_peak, 4), "back_to_back_pool_copies": n,
+            "path": int(pd.info["path"]), "launches": int(pd.info["launches"]),
+            "max_splits": int(pd.info["max_splits"])}
 
 
 def _config_points(dev, calls, hbm_peak):
