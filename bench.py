@@ -6,8 +6,10 @@ headline workload is the long-context decode at 262144 tokens (batch 1,
 32 query / 4 KV heads, head_dim 128, bf16, page 64, 537 MB of K/V per call,
 more than the 129 MB L2, so consecutive steps do not hit in L2).  The same line
 carries the whole long-context sweep (1900 ... 262144 tokens), each point
-timed per call with an L2 flush before it, and back to back in a CUDA graph
-whose calls rotate over copies of the K/V pools (each call's pages out of L2).
+timed per call with an L2 flush before it (eagerly between CUDA events, and
+replayed from a CUDA graph of (flush, call) pairs minus the flushes), and back
+to back in a CUDA graph whose calls rotate over copies of the K/V pools (each
+call's pages out of L2).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fdec|reference]
 
@@ -839,10 +841,16 @@ def _run_fdec(args):
             # of the pools, every call starting with its pages out of L2 (no per-call events).
             b2b, n = _back_to_back_us(torch, ws, lambda k, v: pds.run(ws.q, k, v, tb, ln, out, lse, scale=ws.scale))
             gbs_b2b = ws.kv_bytes / (b2b * 1e-6) / 1e9
+            # Graph-replayed after an L2 eviction: a CUDA graph of 20 (eviction, call) pairs minus a graph of
+            # the 20 evictions alone (every call cold, no per-call launch or event).
+            gf = _time_graph(torch, lambda: pds.run(ws.q, ws.k, ws.v, tb, ln, out, lse, scale=ws.scale), 20, flush)
+            gbs_gf = ws.kv_bytes / (gf * 1e-6) / 1e9
             sweep.append({"kv_len": length, "us_per_call": round(us, 2), "us_min": round(min(times), 2),
                           "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
                           "back_to_back_us_per_call": round(b2b, 2), "back_to_back_GB_per_s": round(gbs_b2b, 1),
                           "back_to_back_frac_of_peak": round(gbs_b2b / peak, 4), "back_to_back_pool_copies": n,
+                          "graph_flushed_us_per_call": round(gf, 2), "graph_flushed_GB_per_s": round(gbs_gf, 1),
+                          "graph_flushed_frac_of_peak": round(gbs_gf / peak, 4),
                           "splits": int(pds.info["max_splits"]), "launches": int(pds.info["launches"])})
             if ws is not w:
                 del pds, ws
