@@ -158,3 +158,29 @@ def test_permuting_physical_pages_leaves_the_result():
     kc2[perm], vc2[perm], ks2[perm], vs2[perm] = kc, vc, ks, vs
     o2, l2 = _run(q, kc2, ks2, vc2, vs2, perm[None, :].astype(np.int32), np.array([18], np.int32), causal=True)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("layout", ["hnd", "nhd", "interleaved", "split2", "mixed", "interleaved_nhd"])
+def test_q8_0_workloads_through_the_helpers_match_a_float64_softmax(layout):
+    # the seeded q8_0 workloads and the test helpers that hand their pools to the oracle
+    # (code and scale strides of every layout) against a float64 softmax over rows
+    # gathered and dequantised here by plain indexing
+    from paged_split_kv_gather_gb300 import workloads as W
+    from tests.helpers import gather_tokens, oracle_run, visible
+
+    w = W.make(2, 3, 8, 2, 64, 4, [30, 9], dtype="f16", seed=5, kv_dtype="q8_0", layout=layout, causal=True)
+    out, lse = oracle_run(w)
+    q = w.q.double().numpy()
+    for b in range(w.batch):
+        for kvh in range(w.num_kv_heads):
+            n = int(w.seq_lens[b])
+            k = gather_tokens(w, w.k, b, kvh, n) * np.repeat(gather_tokens(w, w.k_scales, b, kvh, n), 32, axis=1)
+            v = gather_tokens(w, w.v, b, kvh, n) * np.repeat(gather_tokens(w, w.v_scales, b, kvh, n), 32, axis=1)
+            for i in range(w.q_len):
+                m = visible(w, b, i)
+                for h in range(kvh * w.group, (kvh + 1) * w.group):
+                    z = w.scale * (k[:m] @ q[b, i, h])
+                    zm = z.max()
+                    p = np.exp(z - zm)
+                    assert np.allclose(out[b, i, h], p @ v[:m] / p.sum(), rtol=0, atol=1e-12)
+                    assert abs(lse[b, i, h] - (zm + np.log(p.sum()))) < 1e-12
