@@ -411,7 +411,11 @@ struct MmaWarp {
         constexpr float kLazyRescale = 8.f;
         if (__any_sync(0xffffffffu, mx0 > mrow[0] + kLazyRescale || mx1 > mrow[1] + kLazyRescale)) {
             const float n0 = fmaxf(mrow[0], mx0), n1 = fmaxf(mrow[1], mx1);
-            const float a0 = exp2_approx(mrow[0] - n0), a1 = exp2_approx(mrow[1] - n1);  // 0 when m was -inf
+            // 0 when m was -inf and the row now sees a token; 1 for a row that still has seen
+            // nothing (the branch is taken for the whole warp when any row grows, and
+            // -inf - -inf would be NaN and poison its l)
+            const float a0 = n0 == -INFINITY ? 1.f : exp2_approx(mrow[0] - n0);
+            const float a1 = n1 == -INFINITY ? 1.f : exp2_approx(mrow[1] - n1);
             lrow[0] *= a0;
             lrow[1] *= a1;
 #pragma unroll

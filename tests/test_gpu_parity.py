@@ -448,3 +448,21 @@ def test_two_runs_over_disjoint_ranges_merge_to_the_whole():
                          torch.stack([l1.reshape(8), l2.reshape(8)]).contiguous(), oo, lo)
     assert torch.max(torch.abs(oo - full_o.reshape(8, 128))) / torch.max(torch.abs(full_o)) < 1e-4
     assert torch.max(torch.abs(lo - full_l.reshape(8))) < 1e-5
+
+
+@pytest.mark.parametrize("kv_dtype", ["", "fp8", "q8_0"])
+def test_rows_that_see_nothing_of_a_consumer_groups_only_stage(kv_dtype):
+    # One 64-token block per split, run-time lengths below capacity and a causal
+    # 5-token query: the last split of a sequence has a stage past the early rows'
+    # limits that is its consumer group's only stage, while later rows of the same
+    # warp see tokens there.  Those early rows must keep an empty state (their
+    # running max is still -inf), not a NaN sum that empties the whole row.
+    w = W.make(2, 5, 4, 1, 128, 8, [617, 1452], dtype="bf16", causal=True, seed=6, kv_dtype=kv_dtype,
+               q_layout="fused_qkv").to("cuda")
+    run_lens = np.asarray([580, 1378], dtype=np.int32)
+    out, lse, pd = gpu_run(w, capacities=np.asarray([617, 1452], dtype=np.int32), seq_lens=run_lens,
+                           blocks_per_split=1, path=fd.FDEC_PATH_MMA if not kv_dtype else fd.FDEC_PATH_AUTO)
+    torch.cuda.synchronize()
+    assert pd.device_errors() == 0 and pd.info["path"] == fd.FDEC_PATH_MMA
+    ro, rl = oracle_run(w.to("cpu"), seq_lens=run_lens)
+    assert_parity(out.cpu(), lse.cpu(), ro, rl, kv_dtype or "16-bit")
