@@ -122,7 +122,8 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int 
 // When the box spans a whole stage's token rows, its region extent is every region
 // of the row and one instruction lands [region][row][128 B] (region-major,
 // 128B-swizzled), the stage layout; shorter boxes (pages smaller than a stage)
-// take one region each (`region`), placed by the caller.  A TMA instruction costs
+// either span every region too and land one after another (the tensor-core split
+// kernels' box-major stages) or take one region each (`region`), placed by the caller.  A TMA instruction costs
 // ~50-60 ns of issue time whatever its size (measured on sm_103a), hence the
 // widest box the page size allows.  Completion is counted in bytes on `bar`.
 __device__ __forceinline__ void tma_load_kv_box(uint32_t dst, const void* tmap, int slot, int region, int kvh, int page,

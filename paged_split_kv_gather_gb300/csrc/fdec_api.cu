@@ -263,13 +263,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // elements or 128 E4M3 codes; eb = element bytes), slot, 128-byte region of the
 // row, KV head, page), 128-byte swizzle; box (128 bytes, box_rows slots, R, 1, 1)
 // with R = every region when a box spans a whole stage (box_rows == the stage's
-// token rows), else 1.  With the region dim after the slot dim a whole-stage box
-// lands region-major in shared memory, [region][slot][128 B], the stage layout
-// every split kernel reads.  The strides need not increase with the dim index (the
-// region stride is 128 bytes, the slot stride a whole row); dims of one index take
-// any stride.
+// token rows) or the kernel stages small pages box-major (all_regions), else 1.
+// With the region dim after the slot dim a box of every region lands region-major
+// in shared memory, [region][slot][128 B]: a whole-stage box is the stage layout
+// every split kernel reads; a box-major stage is a run of such boxes, one per page.
+// The strides need not increase with the dim index (the region stride is 128 bytes,
+// the slot stride a whole row); dims of one index take any stride.
 fdec_status encode_kv_map(CUtensorMap* map, const fdec_kv_desc& d, int head_dim, int page_size, int hk,
-                          int box_rows, int stage_rows, int eb) {
+                          int box_rows, int stage_rows, int eb, bool all_regions) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr) return fail(FDEC_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const int regions = head_dim * eb / 128;
@@ -283,7 +284,7 @@ fdec_status encode_kv_map(CUtensorMap* map, const fdec_kv_desc& d, int head_dim,
                              stride_of(hk, d.stride_head * eb), stride_of(d.num_pages, d.stride_page * eb)};
     if (regions == 1) gstride[1] = 16;  // a single region: any stride
     cuuint32_t box[5] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(box_rows),
-                         static_cast<cuuint32_t>(box_rows == stage_rows ? regions : 1), 1, 1};
+                         static_cast<cuuint32_t>((box_rows == stage_rows || all_regions) ? regions : 1), 1, 1};
     cuuint32_t estride[5] = {1, 1, 1, 1, 1};
     CUresult r = enc(map, eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 5,
                      const_cast<void*>(d.base), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -668,9 +669,11 @@ static fdec_status run_impl(fdec_plan_t p, const void* q, int64_t q_stride_tok, 
     if (p->page_size >= 8 && !(p->maps_valid && same_desc(p->map_k, k) && same_desc(p->map_v, v))) {
         const int stage_rows = p->path == FDEC_PATH_TC ? kTcStageTokens : kStageTokens;
         const int box_rows = std::min(p->page_size, stage_rows);
-        fdec_status st = encode_kv_map(&p->tmap_k, k, p->head_dim, p->page_size, p->hk, box_rows, stage_rows, eb);
+        const bool all_regions = p->path == FDEC_PATH_MMA && split_mma_box_major(p->head_dim, p->kv8);
+        fdec_status st =
+            encode_kv_map(&p->tmap_k, k, p->head_dim, p->page_size, p->hk, box_rows, stage_rows, eb, all_regions);
         if (st == FDEC_OK)
-            st = encode_kv_map(&p->tmap_v, v, p->head_dim, p->page_size, p->hk, box_rows, stage_rows, eb);
+            st = encode_kv_map(&p->tmap_v, v, p->head_dim, p->page_size, p->hk, box_rows, stage_rows, eb, all_regions);
         if (st != FDEC_OK) {
             p->maps_valid = false;
             return st;

@@ -116,6 +116,10 @@ inline bool split_mma_persist_supported(int head_dim) {
 inline int split_mma_persist_ctas_per_sm(int head_dim) { return head_dim > 256 ? 1 : 2; }
 int split_mma_threads(int head_dim, bool kv8);
 inline bool split_mma_kv8_supported(int head_dim) { return head_dim == 128 || head_dim == 256; }
+// Whether the tensor-core split kernels stage pages smaller than a stage one box per
+// page ([box][region][rows][128 B]) rather than region-major: all but 16-bit head_dim
+// 512 (MmaLayout / PersistLayout BOXMAJ); their tensor maps then take every region.
+inline bool split_mma_box_major(int head_dim, bool kv8) { return kv8 || head_dim <= 256; }
 // q8_0 caches (int8 codes in blocks of 32 with one binary16 scale each) on the
 // one-CTA-per-item tensor-core kernel, head_dim 128 and 256.
 cudaError_t launch_split_mma_q8(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int head_dim,

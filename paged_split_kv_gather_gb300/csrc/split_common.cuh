@@ -37,6 +37,22 @@ struct StageGeom {
     static constexpr int STAGE_BYTES = 2 * HALF_BYTES;         // K regions then V regions
 };
 
+// Byte offset of token row t of a stage's K (or V) half whose rows were staged in
+// boxes of br rows (br divides the stage's rows; br = the stage's rows: the
+// region-major layout [region][row][128 B]).  Box n = t / br holds rows n br .. + br - 1
+// as [region][br rows][128 B], so region r of row t is at this offset + r br 128.  With
+// br a multiple of 8, the 128-byte swizzle of row t still XORs by t & 7.
+template <int ROW_BYTES>
+__device__ __forceinline__ uint32_t stage_row_offset(int t, int br) {
+    return static_cast<uint32_t>((t / br) * (br * ROW_BYTES) + (t % br) * 128);
+}
+
+// Token rows per staged box of a 32-token stage as the producers stage it: pages of 8
+// or 16 tokens in box-major kernels (TMA mode), the whole stage otherwise.
+__device__ __forceinline__ int staged_box_rows(int page_shift, bool box_major) {
+    return (box_major && page_shift >= 3 && page_shift < 5) ? (1 << page_shift) : kStageTokens;
+}
+
 // Token range of a work item, with the run-time length clamped to the planned
 // capacity.  tok_end_alloc is the item's range by plan (its blocks), known
 // before the run-time length arrives; bad records a length outside [0, capacity]
@@ -148,7 +164,12 @@ __device__ __forceinline__ void copy_scale_rows(const SplitParams& p, uint8_t* s
 // the slot's area of sc_ring (2 TOK SCB bytes per slot); in TMA mode every lane then
 // arrives once on the stage's full barrier after its copies (which counts those 32
 // arrivals besides the expect-tx one).
-template <int D, int S, int TOK = kStageTokens, int EB = 2, int SCB = 0>
+// BOXMAJ: when a page holds fewer tokens than a stage, each page's rows land as one box
+// of every region ([box][region][BR rows][128 B], see stage_row_offset; the tensor map's
+// box spans all regions) instead of one box per region into the region-major layout:
+// a TMA instruction costs about the same whatever its size, and with one box per region
+// the producer's issue time bounded the stream at page sizes 8 and 16.
+template <int D, int S, int TOK = kStageTokens, int EB = 2, int SCB = 0, bool BOXMAJ = false>
 __device__ __forceinline__ void produce_stages(const SplitParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv, uint64_t* full,
                                uint64_t* empty, uint8_t* stages, int b, int kvh, const ItemRange& ir,
                                bool tma_mode, uint8_t* sc_ring = nullptr) {
@@ -209,8 +230,8 @@ __device__ __forceinline__ void produce_stages(const SplitParams& p, const CUten
             __syncwarp();
             if (valid) {  // lane j issues box j (every region in one instruction when the box spans the stage)
                 const int slot0 = (tok_begin + (box0 + lane) * BR) & page_mask;
-                const uint32_t kdst = smem_addr(stages + s * G::STAGE_BYTES + lane * BR * 128);
-                if (NB == 1) {
+                const uint32_t kdst = smem_addr(stages + s * G::STAGE_BYTES + lane * BR * (BOXMAJ ? G::ROW_BYTES : 128));
+                if (NB == 1 || BOXMAJ) {
                     tma_load_kv_box(kdst, tmk, slot0, 0, kvh, my_page, fbar);
                     tma_load_kv_box(kdst + G::HALF_BYTES, tmv, slot0, 0, kvh, my_page, fbar);
                 } else {
@@ -301,14 +322,16 @@ __device__ __forceinline__ bool wait_stage(uint64_t* full, int i) {
 // held; zero its V rows [nv, TOK) so that a fixed-size p.V loop adds 0 * 0.
 // `threads` consecutive threads (from `tid` 0) share the work.
 template <int D, int TOK = kStageTokens, int EB = 2>
-__device__ __forceinline__ void zero_v_tail(uint8_t* stage, int nv, int tid = threadIdx.x & 31, int threads = 32) {
+__device__ __forceinline__ void zero_v_tail(uint8_t* stage, int nv, int tid = threadIdx.x & 31, int threads = 32,
+                                            int br = TOK) {
     using G = StageGeom<D, TOK, EB>;
     uint8_t* vrows = stage + G::HALF_BYTES;
     for (int idx = tid; idx < (TOK - nv) * G::REGIONS * 8; idx += threads) {
         const int row = nv + idx / (G::REGIONS * 8);
         const int rem = idx % (G::REGIONS * 8);
-        *reinterpret_cast<uint4*>(vrows + (rem >> 3) * G::REGION_BYTES + row * 128 + (rem & 7) * 16) =
-            make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t off = br == TOK ? (rem >> 3) * G::REGION_BYTES + row * 128
+                                       : stage_row_offset<G::ROW_BYTES>(row, br) + (rem >> 3) * (br * 128);
+        *reinterpret_cast<uint4*>(vrows + off + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
     if (threads == 32) __syncwarp();
 }

@@ -95,6 +95,10 @@ struct MmaLayout {
     static_assert(!Q8 || KV8, "q8_0 codes are staged as bytes");
     static_assert(S >= NP + 1, "stage ring too small");
     static_assert(!KV8 || DSPLIT == 1, "E4M3 caches: one warp per stage");
+    // Pages smaller than a stage land one box per page (all regions; see produce_stages)
+    // except at head_dim 512 over 16-bit caches, whose warp pairs split each stage's V by
+    // regions.
+    static constexpr bool BOXMAJ = DSPLIT == 1;
     static constexpr int QMAX_OFFSET = BAR_BYTES - RC * 4;  // E4M3 caches: query row maxima
     static_assert(3 * S * 8 <= QMAX_OFFSET, "barrier area too small");
     static_assert(NP * RC * (D + 2) * 4 <= S * GS::STAGE_BYTES, "merge scratch must fit the stage area");
@@ -228,6 +232,7 @@ struct MmaWarp {
     static constexpr int QREGS = Lay::Q_IN_REGS ? KSTEPS : 1;
 
     int lane, g, tq, mi;  // g: fragment row (and row + 8); tq: column pair; mi: ldmatrix matrix
+    uint32_t rs_;         // box-major stages: bytes between two 128-byte regions of a row
     // 16-bit stages: ldmatrix row addresses within a stage (chunk c of row r at c ^ (r & 7)).
     uint32_t kb_row[2], kb_x[4], vb_row[2], vb_x[4];
     // KV8 ldmatrix addresses in a code stage (32 token rows of D/128 regions of 128 bytes).
@@ -238,17 +243,33 @@ struct MmaWarp {
     float o[NT][4];
     float mrow[2], lrow[2];
 
-    __device__ __forceinline__ explicit MmaWarp(int lane_) : lane(lane_), g(lane_ >> 2), tq(lane_ & 3), mi(lane_ >> 3) {
-        k8_row = static_cast<uint32_t>(lane * 128);
+    // Bytes between two 128-byte regions of a token row in the stage.
+    __device__ __forceinline__ uint32_t rs() const {
+        if constexpr (Lay::BOXMAJ)
+            return rs_;
+        else
+            return GS::REGION_BYTES;
+    }
+
+    // br: token rows per staged box (kStageTokens: the region-major layout; see
+    // stage_row_offset); only box-major kernels stage boxes of fewer rows.
+    __device__ __forceinline__ explicit MmaWarp(int lane_, int br = kStageTokens)
+        : lane(lane_), g(lane_ >> 2), tq(lane_ & 3), mi(lane_ >> 3), rs_(static_cast<uint32_t>(br * 128)) {
+        auto row_off = [&](int t) -> uint32_t {
+            if constexpr (Lay::BOXMAJ)
+                return stage_row_offset<GS::ROW_BYTES>(t, br);
+            else
+                return static_cast<uint32_t>(t * 128);
+        };
+        k8_row = row_off(lane);
         k8_x = static_cast<uint32_t>((lane & 7) << 4);
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
-            v8_row[j] = static_cast<uint32_t>((16 * j + 8 * ((lane >> 3) & 1) + (lane & 7)) * 128);
+        for (int j = 0; j < 2; ++j) v8_row[j] = row_off(16 * j + 8 * ((lane >> 3) & 1) + (lane & 7));
         v8_x = static_cast<uint32_t>((((lane >> 4) & 1) ^ (lane & 7)) << 4);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            kb_row[j] = static_cast<uint32_t>((8 * (2 * j + (mi >> 1)) + (lane & 7)) * 128);
-            vb_row[j] = static_cast<uint32_t>((16 * j + 8 * (mi & 1) + (lane & 7)) * 128);
+            kb_row[j] = row_off(8 * (2 * j + (mi >> 1)) + (lane & 7));
+            vb_row[j] = row_off(16 * j + 8 * (mi & 1) + (lane & 7));
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -314,7 +335,10 @@ struct MmaWarp {
                         *reinterpret_cast<uint2*>(scl + (kStageTokens + lane) * 8) = make_uint2(0u, 0u);
                 }
             }
-            zero_v_tail<D, kStageTokens, KV8 ? 1 : 2>(stage_ptr, nv);
+            if constexpr (Lay::BOXMAJ)
+                zero_v_tail<D, kStageTokens, KV8 ? 1 : 2>(stage_ptr, nv, lane, 32, static_cast<int>(rs_ >> 7));
+            else
+                zero_v_tail<D, kStageTokens, KV8 ? 1 : 2>(stage_ptr, nv);
         }
         const uint32_t ql = Lay::Q_IN_REGS ? 0u : q_lane(q_s);
         const __half* sck = reinterpret_cast<const __half*>(scl);  // q8_0: K scales [32][NB], V scales after
@@ -341,7 +365,7 @@ struct MmaWarp {
                     constexpr int qk = Lay::Q_IN_REGS ? kk : 0;
                     if constexpr (!Lay::Q_IN_REGS) load_q8(q_s, kk, qa[0]);
                     uint32_t r[4];
-                    ldmatrix_x4(kbase + (kk >> 3) * GS::REGION_BYTES + k8_row + ((static_cast<uint32_t>(kk & 7) << 4) ^ k8_x),
+                    ldmatrix_x4(kbase + (kk >> 3) * rs() + k8_row + ((static_cast<uint32_t>(kk & 7) << 4) ^ k8_x),
                                 r[0], r[1], r[2], r[3]);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -366,7 +390,7 @@ struct MmaWarp {
             if constexpr (KV8) {
                 if constexpr (!Lay::Q_IN_REGS) load_q8(q_s, kk, qa[0]);
                 uint32_t r[4];
-                ldmatrix_x4(kbase + (kk >> 3) * GS::REGION_BYTES + k8_row + ((static_cast<uint32_t>(kk & 7) << 4) ^ k8_x),
+                ldmatrix_x4(kbase + (kk >> 3) * rs() + k8_row + ((static_cast<uint32_t>(kk & 7) << 4) ^ k8_x),
                             r[0], r[1], r[2], r[3]);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -380,7 +404,7 @@ struct MmaWarp {
 #pragma unroll
                 for (int pr = 0; pr < 2; ++pr) {
                     uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4(kbase + (kk >> 2) * G::REGION_BYTES + kb_row[pr] + kb_x[kk & 3], b0, b1, b2, b3);
+                    ldmatrix_x4(kbase + (kk >> 2) * rs() + kb_row[pr] + kb_x[kk & 3], b0, b1, b2, b3);
                     mma_16816<MB>(sc[2 * pr], qa[qk], b0, b1);
                     mma_16816<MB>(sc[2 * pr + 1], qa[qk], b2, b3);
                 }
@@ -500,7 +524,7 @@ struct MmaWarp {
                     a[2] = pack_f16x2(sc[2 * k2 + 1][0] * w2, sc[2 * k2 + 1][1] * w3);
                     a[3] = pack_f16x2(sc[2 * k2 + 1][2] * w2, sc[2 * k2 + 1][3] * w3);
                     uint32_t r[4];
-                    ldmatrix_x4_trans(vbase + (c >> 3) * GS::REGION_BYTES + v8_row[k2] +
+                    ldmatrix_x4_trans(vbase + (c >> 3) * rs() + v8_row[k2] +
                                           ((static_cast<uint32_t>(c & 7) << 4) ^ v8_x),
                                       r[0], r[1], r[2], r[3]);
                     uint32_t ev[4], od[4];
@@ -524,7 +548,7 @@ struct MmaWarp {
                 static_for<0, D / 32>([&](auto cp_) {
                     constexpr int c = 2 * decltype(cp_)::value;
                     uint32_t r[4];
-                    ldmatrix_x4_trans(vbase + (c >> 3) * GS::REGION_BYTES + v8_row[k2] +
+                    ldmatrix_x4_trans(vbase + (c >> 3) * rs() + v8_row[k2] +
                                           ((static_cast<uint32_t>(c & 7) << 4) ^ v8_x),
                                       r[0], r[1], r[2], r[3]);
                     uint32_t ev[4], od[4];  // by matrix: (tokens 0-7 | 8-15) x (chunk c | c + 1)
@@ -539,7 +563,7 @@ struct MmaWarp {
                 static_for<0, DH / 16>([&](auto jp_) {
                     constexpr int jp = decltype(jp_)::value;  // 16-column group of this warp's half
                     uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4_trans(vbase + v_half + (jp >> 2) * G::REGION_BYTES + vb_row[k2] + vb_x[jp & 3], b0, b1,
+                    ldmatrix_x4_trans(vbase + v_half + (jp >> 2) * rs() + vb_row[k2] + vb_x[jp & 3], b0, b1,
                                       b2, b3);
                     mma_16816<MB>(o[2 * jp], ph[k2], b0, b1);
                     if constexpr (!P1) mma_16816<MB>(o[2 * jp], pl[k2], b0, b1);
@@ -607,8 +631,8 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
             prefetch_tmap(&tmk);
             prefetch_tmap(&tmv);
         }
-        produce_stages<D, S, kStageTokens, KV8 ? 1 : 2, Lay::SCB>(p, &tmk, &tmv, full, empty, stages, b, kvh, ir,
-                                                                tma_mode, sc_ring);
+        produce_stages<D, S, kStageTokens, KV8 ? 1 : 2, Lay::SCB, Lay::BOXMAJ>(p, &tmk, &tmv, full, empty, stages, b,
+                                                                              kvh, ir, tma_mode, sc_ring);
         return;
     }
     if (threadIdx.x == 0) report_item_range(p, ir);
@@ -660,7 +684,7 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
     named_barrier(1, NW * 32);
 
     // ---------------------------------------------------------------------- consumers
-    W cw(lane);
+    W cw(lane, staged_box_rows(p.page_shift, Lay::BOXMAJ));
     const int g = cw.g, tq = cw.tq;
     cw.load_q(q_s);
     int lim[2];
@@ -679,6 +703,7 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
 
     const int grp = warp / DSPLIT;             // consumer group: stages grp, grp + NP, ...
     const int half = warp - grp * DSPLIT;      // which DH columns of O this warp accumulates
+    static_assert(DSPLIT == 1 || !Lay::BOXMAJ, "warp pairs split V by regions of the region-major layout");
     const uint32_t v_half = static_cast<uint32_t>(half * (DH / 64) * G::REGION_BYTES);
     for (int i = grp; i < ir.n_stage; i += NP) {
         const int s = i % S;

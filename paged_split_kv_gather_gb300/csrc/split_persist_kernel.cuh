@@ -1,5 +1,5 @@
 // split_persist_kernel.cuh -- the persistent form of the tensor-core split kernel
-// (16-bit caches, head_dim 64 / 128 / 192).
+// (16-bit caches, every head_dim).
 //
 // Why: with one CTA per work item, every CTA pays a pipeline fill (work item,
 // length, page ids, first TMA: three dependent memory round trips) and the
@@ -11,10 +11,11 @@
 //
 // Here the CTAs stay resident (two per SM) and take work units (a work item x
 // a KV head x a 16-row query group) until none is left: CTA c starts with unit
-// c, and the units past the grid are handed out by one 64-bit ticket counter.
-// The planner orders the items big first (a first wave sized to ~80 % of an
-// even share) and cuts the rest of each sequence into small items, so the
-// dynamic tail balances the CTAs to within one small item.  Results do not
+// c, and the units past the grid are handed out by one 64-bit ticket counter, so
+// a CTA that streams faster takes more of them.  (The planner keeps uniform runs
+// of blocks: a first wave of big items with a tail of small ones, which balances
+// the CTAs to within one small item, measured slower, as every unit adds a
+// partial, a merge and a hand-over of the pipeline.)  Results do not
 // depend on which CTA takes a unit: every unit has its fixed partial slot and
 // is computed by the same code in the same order (its stage j by consumer warp
 // j mod 3, the three warp states merged in warp order), so a fixed plan stays
@@ -78,6 +79,7 @@ struct PersistLayout {
     static constexpr int DSPLIT = D > 256 ? 2 : 1;
     static constexpr int DH = D / DSPLIT;
     static constexpr int CTAS_PER_SM = D > 256 ? 1 : 2;  // = split_mma_persist_ctas_per_sm(D)
+    static constexpr bool BOXMAJ = DSPLIT == 1;          // as MmaLayout: one box per small page
     // Two query buffers (the next unit's rows land while the last one still reads its
     // own) where they fit beside enough stages; one above head_dim 192 (the producer
     // then starts a unit once the previous one is merged).
@@ -154,7 +156,7 @@ __device__ __forceinline__ void punit_load_lens_pages(const SplitParams& p, PUni
 
 // The producer warp of the persistent kernel.  `first`: the CTA's first unit, its
 // loads issued before the CTA's set-up so that they overlap it.
-template <int D, int S, int NP, int QBUFS>
+template <int D, int S, int NP, int QBUFS, bool BOXMAJ>
 __device__ __forceinline__ void produce_units(const SplitParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                               uint64_t* full, uint64_t* empty, uint64_t* qfree, int* tag,
                                               UnitMeta* um, uint16_t* qbuf, uint8_t* stages, bool tma_mode,
@@ -318,10 +320,11 @@ __device__ __forceinline__ void produce_units(const SplitParams& p, const CUtens
                                           static_cast<int64_t>(h) * p.q_stride_head;
                     bulk_g2s(smem_addr(q_dst + lane * D), src, q_row_bytes, fbar);
                 }
-                if (valid) {  // lane j issues box j (every region in one instruction when the box spans the stage)
+                if (valid) {  // lane j issues box j (every region in one instruction when the box spans the
+                              // stage or the layout is box-major)
                     const int slot0 = (tok_begin + (box0 + lane) * BR) & page_mask;
-                    const uint32_t kdst = smem_addr(sbase + lane * BR * 128);
-                    if (NB == 1) {
+                    const uint32_t kdst = smem_addr(sbase + lane * BR * (BOXMAJ ? G::ROW_BYTES : 128));
+                    if (NB == 1 || BOXMAJ) {
                         tma_load_kv_box(kdst, tmk, slot0, 0, kvh, my_page, fbar);
                         tma_load_kv_box(kdst + G::HALF_BYTES, tmv, slot0, 0, kvh, my_page, fbar);
                     } else {
@@ -562,12 +565,13 @@ split_mma_persist_kernel(const __grid_constant__ SplitParams p, const __grid_con
             prefetch_tmap(&tmk);
             prefetch_tmap(&tmv);
         }
-        produce_units<D, S, NP, QBUFS>(p, &tmk, &tmv, full, empty, qfree, tag, um, qbuf, stages, tma_mode, first);
+        produce_units<D, S, NP, QBUFS, Lay::BOXMAJ>(p, &tmk, &tmv, full, empty, qfree, tag, um, qbuf, stages, tma_mode,
+                                                    first);
         return;
     }
 
     // ---------------------------------------------------------------------- consumers
-    W cw(lane);
+    W cw(lane, staged_box_rows(p.page_shift, Lay::BOXMAJ));
     const int g = cw.g, tq = cw.tq;
     const float sl[2] = {p.scale_log2, p.scale_log2};
     const bool poll = p.page_shift < 5;  // stages of several boxes (see wait_stage_mode)
@@ -575,6 +579,7 @@ split_mma_persist_kernel(const __grid_constant__ SplitParams p, const __grid_con
     bool ok = true;
     const int grp = warp / DSPLIT;         // consumer group: stage j of every unit goes to group j mod NP
     const int half = warp - grp * DSPLIT;  // which DH columns of O this warp accumulates
+    static_assert(DSPLIT == 1 || !Lay::BOXMAJ, "warp pairs split V by regions of the region-major layout");
     const uint32_t v_half = static_cast<uint32_t>(half * (DH / 64) * G::REGION_BYTES);
     for (int i = grp;; i += NP) {
         const int s = i % S;

@@ -77,7 +77,7 @@ def test_forced_one_block_per_split_uses_two_reduction_passes():
     p = _plan([262144], num_qo_heads=32, num_kv_heads=4, page_size=64, blocks_per_split=1)
     info = fd.fdec_plan_get_info(p)
     assert info["max_splits"] == 4096
-    assert info["reduce_passes"] == 2          # 4096 -> 16 -> 1 with the default fan-in 256
+    assert info["reduce_passes"] == 2          # 4096 -> 4 -> 1 with the default fan-in 1024
     assert info["launches"] == 3
     p = _plan([262144], num_qo_heads=32, num_kv_heads=4, page_size=64, blocks_per_split=1, reducer_fanin=4)
     assert fd.fdec_plan_get_info(p)["reduce_passes"] == 6   # 4096 = 4^6
