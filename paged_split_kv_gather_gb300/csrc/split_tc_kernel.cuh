@@ -64,10 +64,18 @@ struct TcLayout {
     static constexpr int NBARS = 3 * S + 6 * NT + 1 + (CONV ? S : 0);
     static constexpr int SMEM = OFF_BARS + BAR_BYTES + 1024;  // + alignment slack
     static constexpr int THREADS = (2 + 4 * NT + CONV_WARPS) * 32;
-    // tensor memory per tile t (base TILE_COLS t): S / P buffers at +0 and +64, O (D columns) at +128
-    static constexpr uint32_t TILE_COLS = 128 + D;
+    // Two tiles per CTA: Q in tensor memory as the A operand of Q K^T (the N = 64
+    // products then read only K from shared memory, so they run at the full rate) and
+    // one S / P buffer per tile.  One tile: Q in shared memory, two S / P buffers.
+    static constexpr bool QTM = NT == 2;
+    static constexpr int NSB = QTM ? 1 : 2;        // S / P buffers per tile
+    // tensor memory per tile t (base TILE_COLS t): S / P buffers at +0 (and +64), O (D
+    // columns) after them, then (QTM) Q as D / 2 columns of two 16-bit values
+    static constexpr uint32_t O_COL = 64 * NSB;
+    static constexpr uint32_t Q_COL = O_COL + D;
+    static constexpr uint32_t TILE_COLS = Q_COL + (QTM ? D / 2 : 0);
     static constexpr uint32_t TMEM_COLS = NT * TILE_COLS <= 256 ? 256u : 512u;
-    static_assert(NT * TILE_COLS <= 512, "tensor memory: two S/P buffers and O per tile");
+    static_assert(NT * TILE_COLS <= 512, "tensor memory: S/P buffers, O (and Q) per tile");
     static_assert(S >= 2, "stages");
     static_assert(SMEM <= 232448, "shared memory");
     static_assert(NBARS * 8 + 8 + 4 * S <= BAR_BYTES, "barriers, tensor-memory address, slice modes");
@@ -218,6 +226,32 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    if constexpr (Lay::QTM) {
+        // Q into tensor memory: softmax thread r copies row r of its tile (lane r; dims
+        // 2k, 2k + 1 in column Q_COL + k, the lower dim in the low half).
+        if (warp >= 2 && warp < 2 + 4 * NT) {
+            const int t = (warp - 2) >> 2, wq = warp & 3, r = wq * 32 + lane;
+            const uint8_t* qt = q_tiles + t * Lay::Q_BYTES;
+            const uint32_t dst = tmem + TC * t + (static_cast<uint32_t>(wq * 32) << 16) + Lay::Q_COL;
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) {  // one 64-dim region: 32 columns
+                uint32_t w[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(qt + h * (Lay::TM * 128) + sw128_offset(r, c));
+                    w[4 * c] = v.x;
+                    w[4 * c + 1] = v.y;
+                    w[4 * c + 2] = v.z;
+                    w[4 * c + 3] = v.w;
+                }
+                tmem_st32_u(dst + 32 * h, w);
+            }
+            tmem_wait_st();
+        }
+        tc_fence_before_sync();
+        __syncthreads();
+        tc_fence_after_sync();
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -242,9 +276,14 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
                 const uint64_t kd = kd0 + static_cast<uint32_t>(slot) * kStage;
                 const uint32_t d = tmem + TC * t + 64 * buf;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks)
-                    tc_mma_f16(d, qd + (ks >> 2) * kQRegion + (ks & 3) * 2, kd + (ks >> 2) * kKRegion + (ks & 3) * 2, i_qk,
-                               ks > 0);
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    if constexpr (Lay::QTM)  // A = Q from tensor memory: 16 dims = 8 columns per step
+                        tc_mma_f16_ts(d, tmem + TC * t + Lay::Q_COL + 8 * ks, kd + (ks >> 2) * kKRegion + (ks & 3) * 2,
+                                      i_qk, ks > 0);
+                    else
+                        tc_mma_f16(d, qd + (ks >> 2) * kQRegion + (ks & 3) * 2, kd + (ks >> 2) * kKRegion + (ks & 3) * 2,
+                                   i_qk, ks > 0);
+                }
                 tc_commit(smem_addr(&s_full[2 * t + buf]));
             };
             // P V of one block, 16 tokens (128 rows of V) per step: one f16 product for a
@@ -252,7 +291,7 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
             auto issue_pv = [&](int t, int slot, int buf, bool acc, uint32_t modes) {
                 const uint64_t vd = vd0 + static_cast<uint32_t>(slot) * kStage;
                 const uint32_t p_tm = tmem + TC * t + 64 * buf;
-                const uint32_t o_tm = tmem + TC * t + 128;
+                const uint32_t o_tm = tmem + TC * t + Lay::O_COL;
                 bool a = acc;
                 if (CONV && modes == 0x01010101u) {
 #pragma unroll
@@ -286,6 +325,35 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
             int slot = 0;  // stage slot of block j
             for (int j = 0; j < n_tiles && ok; ++j) {
                 const int next_slot = slot + 1 == S ? 0 : slot + 1;
+                if constexpr (Lay::QTM) {
+                    // One S / P buffer per tile: S_t(j + 1) is issued right after the P V
+                    // products of block j, which read P_t(j) from that buffer first (in-order
+                    // execution); the commit on s_full_t then also covers those products, so a
+                    // row of O_t may be rescaled once S_t(j + 1) has landed.
+                    uint32_t modes = 0;
+                    if constexpr (CONV) {
+                        if (!(ok = mbar_wait_bounded(smem_addr(&conv_full[slot]), (j / S) & 1))) break;
+                        modes = vmode[slot];
+                    }
+                    for (int t = 0; t < NT; ++t) {
+                        if (!(ok = mbar_wait_bounded(smem_addr(&p_full[2 * t]), j & 1))) break;
+                        tc_fence_after_sync();
+                        issue_pv(t, slot, 0, j > 0, modes);
+                        if (j + 1 == n_tiles) {
+                            tc_commit(smem_addr(&o_final[t]));
+                            continue;
+                        }
+                        if (t == 0) {
+                            if (!(ok = wait_full(j + 1))) break;
+                            tc_fence_after_sync();
+                        }
+                        issue_qk(t, next_slot, 0);
+                    }
+                    if (!ok) break;
+                    tc_commit(smem_addr(&empty[slot]));  // the stage is free once these MMAs completed
+                    slot = next_slot;
+                    continue;
+                }
                 if (j + 1 < n_tiles) {
                     // S_t(j + 1) goes to the other buffer, whose P_t(j - 1) the P V
                     // products issued before have consumed by then (in-order execution).
@@ -389,13 +457,14 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
         const int lim = p.causal ? (ir.L - p.q_len + qi) : (ir.L - 1);
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tmem_t = tmem + TC * t + lane_base;
-        const uint32_t tmem_o = tmem_t + 128;
+        const uint32_t tmem_o = tmem_t + Lay::O_COL;
         const float c_log2 = p.scale_log2;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
-            const uint32_t buf = tmem_t + 64 * (j & 1);
-            if (!mbar_wait_bounded(smem_addr(&s_full[2 * t + (j & 1)]), (j >> 1) & 1)) {
+            constexpr int NSB = Lay::NSB;
+            const uint32_t buf = tmem_t + 64 * (j % NSB);
+            if (!mbar_wait_bounded(smem_addr(&s_full[2 * t + (j % NSB)]), (j / NSB) & 1)) {
                 ok = false;
                 break;
             }
@@ -457,7 +526,9 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
                 // phase j - 1 or j here: S_t(j) has landed, so the products of
                 // block j - 2 (issued before it) have completed, and those of
                 // block j wait for this warp's P_t(j).  The parity test is exact.
-                if (!mbar_wait_bounded(smem_addr(&o_done[t]), (j - 1) & 1)) {
+                // (One S / P buffer: S_t(j) was committed after the products of block
+                // j - 1, so they have completed.)
+                if (!Lay::QTM && !mbar_wait_bounded(smem_addr(&o_done[t]), (j - 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -549,7 +620,7 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&p_full[2 * t + (j & 1)]));
+            if (lane == 0) mbar_arrive(smem_addr(&p_full[2 * t + (j % NSB)]));
         }
         // The last P V products: o_done_t may be anywhere from phase n - 2 to n
         // here, so the MMA thread signals them on a barrier of their own.
