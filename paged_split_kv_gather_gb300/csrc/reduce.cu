@@ -60,6 +60,9 @@ __global__ void __launch_bounds__(kReduceWarps * 32, 5) reduce_kernel(const Redu
     // The first task is plan data (not written by the split kernel): read it early.
     ReduceTask task = single;
     if (p.tasks != nullptr && static_cast<int>(blockIdx.y) < num_tasks) task = p.tasks[blockIdx.y];
+    // The next kernel in the stream may be scheduled now (a split kernel of the next
+    // decode step waits for this one's completion before it reads or writes anything).
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // Launched as a programmatic dependent of the split kernel: everything above
     // overlaps its tail; wait here until its partials are complete and visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");

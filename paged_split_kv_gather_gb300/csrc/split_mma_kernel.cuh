@@ -217,7 +217,9 @@ __device__ __forceinline__ float pair_scale(const uint32_t (&w)[NB], int u, int 
 // the swizzled stages, its query fragments, its running state (O accumulators
 // of this warp's DH columns; row max m and sum l of rows g and g + 8, in log2
 // units) and the work of one 32-token stage.
-template <int D, bool BF16, bool KV8, bool Q8 = false>
+// BM: the stages are box-major (see stage_row_offset) with boxes of fewer rows than a
+// stage possible; false: region-major only, with the row addresses fixed at compile time.
+template <int D, bool BF16, bool KV8, bool Q8 = false, bool BM = MmaLayout<D, KV8, Q8>::BOXMAJ>
 struct MmaWarp {
     using Lay = MmaLayout<D, KV8, Q8>;
     using G = StageGeom<D>;
@@ -245,7 +247,7 @@ struct MmaWarp {
 
     // Bytes between two 128-byte regions of a token row in the stage.
     __device__ __forceinline__ uint32_t rs() const {
-        if constexpr (Lay::BOXMAJ)
+        if constexpr (BM)
             return rs_;
         else
             return GS::REGION_BYTES;
@@ -256,7 +258,7 @@ struct MmaWarp {
     __device__ __forceinline__ explicit MmaWarp(int lane_, int br = kStageTokens)
         : lane(lane_), g(lane_ >> 2), tq(lane_ & 3), mi(lane_ >> 3), rs_(static_cast<uint32_t>(br * 128)) {
         auto row_off = [&](int t) -> uint32_t {
-            if constexpr (Lay::BOXMAJ)
+            if constexpr (BM)
                 return stage_row_offset<GS::ROW_BYTES>(t, br);
             else
                 return static_cast<uint32_t>(t * 128);
@@ -335,7 +337,7 @@ struct MmaWarp {
                         *reinterpret_cast<uint2*>(scl + (kStageTokens + lane) * 8) = make_uint2(0u, 0u);
                 }
             }
-            if constexpr (Lay::BOXMAJ)
+            if constexpr (BM)
                 zero_v_tail<D, kStageTokens, KV8 ? 1 : 2>(stage_ptr, nv, lane, 32, static_cast<int>(rs_ >> 7));
             else
                 zero_v_tail<D, kStageTokens, KV8 ? 1 : 2>(stage_ptr, nv);

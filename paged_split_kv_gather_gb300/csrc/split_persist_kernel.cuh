@@ -70,7 +70,11 @@ struct UnitMeta {
     int n_pad;                 // ring stages of the unit: a multiple of NP, at least NP
 };
 
-template <int D>
+// BM: stages of pages smaller than a stage land box-major (one TMA box per page); the
+// launch takes the BM = false instantiation for every other page size, whose row
+// addresses are fixed at compile time (measured: the box-major build, identical in
+// what it does at 64-token pages, ran 10 % slower there at 66-76 splits).
+template <int D, bool BM = true>
 struct PersistLayout {
     using G = StageGeom<D>;
     static constexpr int RC = 16;                      // query rows per unit (one M tile)
@@ -79,7 +83,7 @@ struct PersistLayout {
     static constexpr int DSPLIT = D > 256 ? 2 : 1;
     static constexpr int DH = D / DSPLIT;
     static constexpr int CTAS_PER_SM = D > 256 ? 1 : 2;  // = split_mma_persist_ctas_per_sm(D)
-    static constexpr bool BOXMAJ = DSPLIT == 1;          // as MmaLayout: one box per small page
+    static constexpr bool BOXMAJ = BM && DSPLIT == 1;    // one box per small page
     // Two query buffers (the next unit's rows land while the last one still reads its
     // own) where they fit beside enough stages; one above head_dim 192 (the producer
     // then starts a unit once the previous one is merged).
@@ -496,12 +500,12 @@ __device__ __forceinline__ void merge_unit(const SplitParams& p, const UnitMeta&
     }
 }
 
-template <int D, bool BF16>
-__global__ void __launch_bounds__(PersistLayout<D>::THREADS, PersistLayout<D>::CTAS_PER_SM)
+template <int D, bool BF16, bool BM>
+__global__ void __launch_bounds__(PersistLayout<D, BM>::THREADS, PersistLayout<D, BM>::CTAS_PER_SM)
 split_mma_persist_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv) {
-    using Lay = PersistLayout<D>;
-    using W = MmaWarp<D, BF16, false>;
+    using Lay = PersistLayout<D, BM>;
+    using W = MmaWarp<D, BF16, false, false, Lay::BOXMAJ>;
     using G = StageGeom<D>;
     constexpr int S = Lay::S;
     constexpr int NP = Lay::NP;
@@ -537,7 +541,12 @@ split_mma_persist_kernel(const __grid_constant__ SplitParams p, const __grid_con
     first.unit = -1;
     if (warp == NW) {
         first.unit = blockIdx.x;
-        punit_load_item(p, first, p.hk * ((p.rows + RC - 1) / RC));
+        punit_load_item(p, first, p.hk * ((p.rows + RC - 1) / RC));  // plan data
+        // Launched as a programmatic dependent of the kernel before it in the stream (a
+        // no-op without one): every input (lengths, page table, q, K, V) and every output
+        // it may still read or write is touched only after that kernel has completed.  The
+        // consumers' reads and writes follow the producer's stages.
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         punit_load_lens_pages(p, first, lane, tma_mode ? min(1 << p.page_shift, kStageTokens) : 1, tma_mode);
     }
     if (threadIdx.x == 0) {
@@ -663,23 +672,34 @@ split_mma_persist_kernel(const __grid_constant__ SplitParams p, const __grid_con
     if (!ok && lane == 0) atomicOr(p.err, FDEC_DEVERR_TIMEOUT);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool BM>
 cudaError_t launch_split_mma_persist_one(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                          dim3 grid, cudaStream_t stream, bool launch) {
-    using Lay = PersistLayout<D>;
+    using Lay = PersistLayout<D, BM>;
     static unsigned long long attr_done = 0;  // one bit per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-        e = cudaFuncSetAttribute(split_mma_persist_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(split_mma_persist_kernel<D, BF16, BM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Lay::SMEM);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_RELEASE);
     }
     if (!launch) return cudaSuccess;
-    split_mma_persist_kernel<D, BF16><<<grid, Lay::THREADS, Lay::SMEM, stream>>>(p, tk, tv);
-    return cudaGetLastError();
+    // A programmatic dependent of the previous kernel in the stream: its CTAs may become
+    // resident while that kernel finishes (the producer waits for it before any input).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(Lay::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Lay::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, split_mma_persist_kernel<D, BF16, BM>, p, tk, tv);
 }
 
 }  // namespace fdec
