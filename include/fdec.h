@@ -181,7 +181,11 @@ fdec_status fdec_plan_upload(fdec_plan_t plan, void* workspace, cudaStream_t str
 /*
  * Run the planned attention.  Kernel launches only (no allocation, no copy, no
  * synchronisation), so it may be captured in a CUDA graph once the plan is
- * uploaded.
+ * uploaded.  The decode kernel (16-bit caches, up to 16 rows per KV head) is a
+ * programmatic dependent of the kernel before it on `stream`: its CTAs may start
+ * while that kernel finishes, but it reads and writes nothing (inputs, outputs,
+ * workspace) until that kernel has completed, so stream order holds as for an
+ * ordinary launch.
  *   q: [batch, q_len, Hq, head_dim] 16-bit, element (b, i, h, d) at
  *      q + (b*q_len + i)*q_stride_tok + h*q_stride_head + d.  Covers a packed q,
  *      a head slice of a fused QKV tensor, and a head-major q (FlashInfer PR,
