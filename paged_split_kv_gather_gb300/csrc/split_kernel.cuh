@@ -123,6 +123,9 @@ split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUte
     const bool tma_mode = p.page_shift >= 3;  // pages of >= 8 tokens
     if (threadIdx.x == 0) init_stage_barriers<S>(full, empty, tma_mode);
     __syncthreads();  // barriers initialised (nothing before this waits on memory)
+    // Launched as a programmatic dependent of the kernel before it in the stream: read
+    // and write nothing but plan data before that kernel has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const ItemRange ir = item_range(p, it);
 
     if (warp == NW) {
@@ -335,8 +338,17 @@ cudaError_t launch_split_one(const SplitParams& p, const CUtensorMap& tk, const 
         __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_RELEASE);
     }
     if (!launch) return cudaSuccess;
-    split_kernel<D, RC, BF16><<<grid, Lay::THREADS, Lay::SMEM, stream>>>(p, tk, tv);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(Lay::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Lay::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait in the kernel
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, split_kernel<D, RC, BF16>, p, tk, tv);
 }
 
 template <int D, bool BF16>

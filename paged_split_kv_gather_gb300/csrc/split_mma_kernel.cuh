@@ -625,6 +625,9 @@ split_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ 
     const bool tma_mode = p.page_shift >= 3;
     if (threadIdx.x == 0) init_stage_barriers<S>(full, empty, tma_mode, DSPLIT, Q8 ? 33u : 1u);
     __syncthreads();  // barriers initialised (nothing before this waits on memory)
+    // Launched as a programmatic dependent of the kernel before it in the stream: read
+    // and write nothing but plan data before that kernel has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const ItemRange ir = item_range(p, it);
 
     if (warp == NW) {
@@ -776,8 +779,17 @@ cudaError_t launch_split_mma_one(const SplitParams& p, const CUtensorMap& tk, co
         __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_RELEASE);
     }
     if (!launch) return cudaSuccess;
-    split_mma_kernel<D, BF16, KV8, Q8><<<grid, Lay::THREADS, Lay::SMEM, stream>>>(p, tk, tv);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(Lay::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Lay::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait in the kernel
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, split_mma_kernel<D, BF16, KV8, Q8>, p, tk, tv);
 }
 
 }  // namespace fdec

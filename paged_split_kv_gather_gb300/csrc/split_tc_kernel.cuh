@@ -168,6 +168,9 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
     const int b = it.seq;
     const int row0 = cta_tile * Lay::ROWS;
 
+    // Launched as a programmatic dependent of the kernel before it in the stream: read
+    // and write nothing but plan data before that kernel has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     ItemRange ir = item_range<TOK>(p, it);
     if (p.causal) {  // no row of this CTA sees past L - Q + (its last q position)
         const int last_row = min(row0 + Lay::ROWS, p.rows) - 1;
@@ -688,8 +691,17 @@ cudaError_t launch_split_tc_one(const SplitParams& p, const CUtensorMap& tk, con
         __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_RELEASE);
     }
     if (!launch) return cudaSuccess;
-    split_tc_kernel<NT, D, BF16><<<grid, TcLayout<NT, D, BF16>::THREADS, TcLayout<NT, D, BF16>::SMEM, stream>>>(p, tk, tv);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(TcLayout<NT, D, BF16>::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = TcLayout<NT, D, BF16>::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait in the kernel
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, split_tc_kernel<NT, D, BF16>, p, tk, tv);
 }
 
 }  // namespace fdec

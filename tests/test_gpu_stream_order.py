@@ -1,0 +1,78 @@
+"""Stream order around the decode kernel's programmatic dependent launch: inputs that
+the kernel just before the call writes on the same stream (q, lengths, page table)
+are the ones the call reads, and back-to-back calls into the same out / lse leave
+the last call's result.  Each call is compared bitwise with the same call made after
+a device synchronisation (a fixed plan is deterministic)."""
+import numpy as np
+import pytest
+import torch
+
+import paged_split_kv_gather_gb300 as fd
+from paged_split_kv_gather_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _cases():
+    return {
+        "long_context_page64": lambda: W.long_context(4224, device="cuda"),   # region-major stages
+        "batched_gqa_page16": lambda: W.batched_gqa(device="cuda"),           # box-major stages
+    }
+
+
+@pytest.mark.parametrize("case", list(_cases()))
+def test_inputs_written_just_before_the_call_are_read(case):
+    w = _cases()[case]()
+    pd = fd.PagedDecode(w.seq_lens, w.q_len, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
+                        w.causal, device="cuda")
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    n = 12
+    qs = [torch.randn(w.q.shape, generator=gen, device="cuda").to(w.q.dtype) for _ in range(n)]
+    caps = np.asarray(w.seq_lens, dtype=np.int32)
+    lens_k = [torch.as_tensor(np.maximum(caps - 3 * k, 0).astype(np.int32), device="cuda") for k in range(n)]
+    table0 = torch.as_tensor(w.page_table, device="cuda")
+    tables = [table0.clone() for _ in range(n)]
+    for k in range(1, n, 3):  # some steps permute two pages of sequence 0 (K/V follow the table)
+        t = tables[k]
+        t[0, 0], t[0, 1] = table0[0, 1].item(), table0[0, 0].item()
+    q = torch.empty_like(w.q)
+    lens = torch.empty_like(lens_k[0])
+    table = torch.empty_like(table0)
+    out = torch.empty((w.batch, w.q_len, w.num_qo_heads, w.head_dim), device="cuda")
+    lse = torch.empty((w.batch, w.q_len, w.num_qo_heads), device="cuda")
+
+    refs = []
+    for k in range(n):
+        q.copy_(qs[k])
+        lens.copy_(lens_k[k])
+        table.copy_(tables[k])
+        torch.cuda.synchronize()
+        pd.run(q, w.k, w.v, table, lens, out, lse, scale=w.scale)
+        torch.cuda.synchronize()
+        refs.append((out.clone(), lse.clone()))
+
+    # the same steps with no synchronisation: each copy kernel runs right before its call
+    got = []
+    for k in range(n):
+        q.copy_(qs[k])
+        lens.copy_(lens_k[k])
+        table.copy_(tables[k])
+        pd.run(q, w.k, w.v, table, lens, out, lse, scale=w.scale)
+        got.append((out.clone(), lse.clone()))
+    torch.cuda.synchronize()
+    assert pd.device_errors() == 0
+    for k in range(n):
+        assert torch.equal(got[k][0], refs[k][0]), (case, k)
+        assert torch.equal(got[k][1], refs[k][1]), (case, k)
+
+    # back-to-back calls into the same out / lse: the last one's result stays
+    for k in range(n):
+        q.copy_(qs[k])
+        pd.run(q, w.k, w.v, table0, torch.as_tensor(caps, device="cuda"), out, lse, scale=w.scale)
+    torch.cuda.synchronize()
+    q.copy_(qs[n - 1])
+    out2 = torch.empty_like(out)
+    lse2 = torch.empty_like(lse)
+    pd.run(q, w.k, w.v, table0, torch.as_tensor(caps, device="cuda"), out2, lse2, scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
