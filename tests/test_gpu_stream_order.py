@@ -17,14 +17,21 @@ def _cases():
     return {
         "long_context_page64": lambda: W.long_context(4224, device="cuda"),   # region-major stages
         "batched_gqa_page16": lambda: W.batched_gqa(device="cuda"),           # box-major stages
+        # the tcgen05 kernel (32 rows per KV head) and the one-CTA-per-item kernel (E4M3 codes)
+        "spec_decode_q8_tcgen05": lambda: W.make(2, 8, 32, 8, 128, 16, [3000, 1700], dtype="bf16", causal=True,
+                                                 device="cuda", seed=31),
+        "e4m3_page32": lambda: W.make(2, 1, 16, 2, 128, 32, [5000, 2222], dtype="bf16", kv_dtype="fp8",
+                                      device="cuda", seed=32),
     }
 
 
 @pytest.mark.parametrize("case", list(_cases()))
 def test_inputs_written_just_before_the_call_are_read(case):
     w = _cases()[case]()
+    opts = {"kv_dtype": w.kv_dtype} if w.kv_dtype else {}
     pd = fd.PagedDecode(w.seq_lens, w.q_len, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
-                        w.causal, device="cuda")
+                        w.causal, device="cuda", **opts)
+    sc = {"k_scale": 0.5, "v_scale": 2.0} if w.kv_dtype == "fp8" else {}
     gen = torch.Generator(device="cuda").manual_seed(5)
     n = 12
     qs = [torch.randn(w.q.shape, generator=gen, device="cuda").to(w.q.dtype) for _ in range(n)]
@@ -47,7 +54,7 @@ def test_inputs_written_just_before_the_call_are_read(case):
         lens.copy_(lens_k[k])
         table.copy_(tables[k])
         torch.cuda.synchronize()
-        pd.run(q, w.k, w.v, table, lens, out, lse, scale=w.scale)
+        pd.run(q, w.k, w.v, table, lens, out, lse, scale=w.scale, **sc)
         torch.cuda.synchronize()
         refs.append((out.clone(), lse.clone()))
 
@@ -57,7 +64,7 @@ def test_inputs_written_just_before_the_call_are_read(case):
         q.copy_(qs[k])
         lens.copy_(lens_k[k])
         table.copy_(tables[k])
-        pd.run(q, w.k, w.v, table, lens, out, lse, scale=w.scale)
+        pd.run(q, w.k, w.v, table, lens, out, lse, scale=w.scale, **sc)
         got.append((out.clone(), lse.clone()))
     torch.cuda.synchronize()
     assert pd.device_errors() == 0
@@ -68,11 +75,11 @@ def test_inputs_written_just_before_the_call_are_read(case):
     # back-to-back calls into the same out / lse: the last one's result stays
     for k in range(n):
         q.copy_(qs[k])
-        pd.run(q, w.k, w.v, table0, torch.as_tensor(caps, device="cuda"), out, lse, scale=w.scale)
+        pd.run(q, w.k, w.v, table0, torch.as_tensor(caps, device="cuda"), out, lse, scale=w.scale, **sc)
     torch.cuda.synchronize()
     q.copy_(qs[n - 1])
     out2 = torch.empty_like(out)
     lse2 = torch.empty_like(lse)
-    pd.run(q, w.k, w.v, table0, torch.as_tensor(caps, device="cuda"), out2, lse2, scale=w.scale)
+    pd.run(q, w.k, w.v, table0, torch.as_tensor(caps, device="cuda"), out2, lse2, scale=w.scale, **sc)
     torch.cuda.synchronize()
     assert torch.equal(out, out2) and torch.equal(lse, lse2)
