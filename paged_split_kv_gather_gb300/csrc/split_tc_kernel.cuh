@@ -13,13 +13,17 @@
 //                 S_t  = Q_t K^T            M 128 rows, N 64 tokens, K = D dims  (D / 16 MMAs)
 //                 O_t += P_t,hi V + P_t,lo V  M 128, N = D dims, K 64 tokens      (2 x 4 MMAs)
 //               Q and K are K-major and V MN-major, 128B-swizzled in shared
-//               memory; S_t, P_t and O_t live in tensor memory.  S_t has two
-//               buffers (block parity); P_t overwrites the S_t it came from (hi
-//               in the first 32 columns, lo in the next 32, two 16-bit values per
-//               column) and is the A operand of the P V products, so P never
-//               goes through shared memory.  S_t of block j + 1 is issued before
+//               memory; S_t, P_t and O_t live in tensor memory.  One tile: S_t has
+//               two buffers (block parity), and S_t of block j + 1 is issued before
 //               the P V products of block j wait for P_t, so it overlaps this
-//               block's softmax, and the tiles take turns with the tensor cores.
+//               block's softmax.  Two tiles: Q_t is copied into tensor memory too
+//               and is the A operand of Q K^T (so those products read only K from
+//               shared memory), and each tile has one S_t buffer, S_t(j + 1) issued
+//               after the P V products of block j; the tiles take turns with the
+//               tensor cores.  P_t overwrites the S_t it came from (hi in the first
+//               32 columns, lo in the next 32, two 16-bit values per column) and is
+//               the A operand of the P V products, so P never goes through shared
+//               memory.
 //   warps 2+4t..5+4t  softmax warpgroup of tile t, thread = row = tensor-memory
 //               lane: load the row of S, mask, row max in registers, exp2, and the
 //               row of P stored back into tensor memory, per 16-token slice: one
