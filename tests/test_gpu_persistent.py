@@ -126,3 +126,29 @@ def test_run_time_lengths_below_capacity_and_empty_sequences():
         assert torch.equal(out, grid[0]) and torch.equal(lse, grid[1])
         ref_o, ref_l = oracle_run(wc, seq_lens=np.asarray(run_lens, dtype=np.int32))
         assert_parity(out.cpu(), lse.cpu(), ref_o, ref_l, str(run_lens))
+
+
+def test_many_more_units_than_ctas():
+    # 1024 short sequences (GQA 8/2, page 16): about 7 units per resident CTA, all but the
+    # first of each CTA handed out by the ticket counter; sampled rows against the oracle,
+    # bitwise against one CTA per item
+    n = 1024
+    lens = np.random.default_rng(41).integers(1, 400, n).astype(np.int32).tolist()
+    w = W.make(n, 1, 8, 2, 128, 16, lens, dtype="bf16", device="cuda", seed=41)
+    pd = fd.PagedDecode(w.seq_lens, 1, 16, 8, 2, 128, "bf16", device="cuda")
+    info = pd.info
+    assert info["num_items"] * 2 > 4 * info["num_split_ctas"]
+    table = torch.as_tensor(w.page_table, device="cuda")
+    lens_d = torch.as_tensor(w.seq_lens, device="cuda")
+    out, lse = _run(pd, w, w.q, table, lens_d)
+    grid = _run(pd, w, _misaligned_copy(w.q), table, lens_d)
+    torch.cuda.synchronize()
+    assert pd.device_errors() == 0
+    assert torch.equal(out, grid[0]) and torch.equal(lse, grid[1])
+    for _ in range(3):  # the counter stays in step
+        again = _run(pd, w, w.q, table, lens_d)
+        assert torch.equal(out, again[0]) and torch.equal(lse, again[1])
+    rows = [b * 8 + h for b in range(0, n, 17) for h in (0, 7)]
+    ref_o, ref_l = oracle_run(w.to("cpu"), rows=rows)
+    idx = torch.as_tensor(np.asarray(rows, dtype=np.int64))
+    assert_parity(out.reshape(-1, 128).cpu()[idx], lse.reshape(-1).cpu()[idx], ref_o, ref_l, "1024 sequences")
