@@ -466,6 +466,10 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
         const uint32_t tmem_t = tmem + TC * t + lane_base;
         const uint32_t tmem_o = tmem_t + Lay::O_COL;
         const float c_log2 = p.scale_log2;
+        // Every row of this warp past the CTA's query rows (a tile of few rows): its rows of
+        // P are never used for a stored row (row m of O depends on row m of P alone), so the
+        // warp only keeps the barriers in step.  Its issue slots go to the other warps.
+        const bool idle = row0 + t * Lay::TM + wq * 32 >= p.rows;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
@@ -476,6 +480,18 @@ split_tc_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ C
                 break;
             }
             tc_fence_after_sync();
+            if (idle) {
+                if (!CONV && t == 0 && ir.tok_end - (ir.tok_begin + j * TOK) < TOK) {  // the tail rows, as below
+                    zero_v_tail<D, TOK>(stages + (j % S) * G::STAGE_BYTES, ir.tok_end - (ir.tok_begin + j * TOK),
+                                        threadIdx.x - 64, 128);
+                    fence_proxy_async_shared();
+                    named_barrier(2, 128);
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&p_full[2 * t + (j % NSB)]));
+                continue;
+            }
             float sv[TOK];
             {
                 float a[32];
