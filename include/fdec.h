@@ -334,11 +334,14 @@ fdec_status fdec_read_device_errors(fdec_plan_t plan, void* workspace, uint32_t*
  *   - The plan needs no fdec_plan_upload: every call copies the plan's work
  *     lists (host memory) into the array with cudaMemcpyAsync on `stream`,
  *     which also clears the device error word, then launches the kernels.
+ *   - Not for CUDA graph capture: every call copies the work lists from the
+ *     plan's pageable host memory, which stream capture does not accept.  A
+ *     captured decode loop uses fdec_run with an uploaded workspace.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current and keeps it for the
- *     process; make that first call before any stream capture begins.  The
- *     address belongs to the device's primary context: do not call this entry
- *     point again on a device after cudaDeviceReset of that device.
+ *     process.  The address belongs to the device's primary context: do not
+ *     call this entry point again on a device after cudaDeviceReset of that
+ *     device.
  *   - All calls share the one array: calls that overlap on the GPU (other
  *     streams, other threads) race and corrupt each other's results.
  *   - Device error bits land in the array and are not reported; use fdec_run
