@@ -791,32 +791,30 @@ def _run_fdec(args):
     peak, peak_kind = _peaks()
     achieved = kv_bytes / (split_ms * 1e-3) / 1e9
 
-    # ---- end to end through the public API from pinned host buffers
-    h_q = w.q.cpu().pin_memory()
-    h_table = torch.as_tensor(w.page_table).pin_memory()
-    h_lens = torch.as_tensor(w.seq_lens).pin_memory()
-    h_out = torch.empty(out.shape, dtype=torch.float32).pin_memory()
-    h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    d_q = torch.empty_like(w.q)
+    # ---- end to end through the public API from pinned host buffers: the step's
+    # inputs (q, page table, lengths) staged in one pinned buffer laid out like one
+    # device buffer (one host-to-device copy), out and lse in one device buffer (one
+    # device-to-host copy): each copy has a fixed cost whatever its size
+    st_in = _Staging(torch, dev, [w.q, torch.as_tensor(w.page_table), torch.as_tensor(w.seq_lens)])
+    st_res = _Staging(torch, dev, [out, lse])
+    d_q, d_table, d_lens = st_in.dev_views
+    d_out, d_lse = st_res.dev_views
     e2e_steps = max(10, min(args.steps, 2000))
     for i in range(args.warmup + e2e_steps):
         if i == args.warmup:
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-        d_q.copy_(h_q, non_blocking=True)
-        table.copy_(h_table, non_blocking=True)
-        lens.copy_(h_lens, non_blocking=True)
-        pd.run(d_q, w.k, w.v, table, lens, out, lse, scale=w.scale)
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        st_in.dev.copy_(st_in.host, non_blocking=True)
+        pd.run(d_q, w.k, w.v, d_table, d_lens, d_out, d_lse, scale=w.scale)
+        st_res.host.copy_(st_res.dev, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     e2e_py_s = (time.perf_counter() - t0) / e2e_steps
-    h2d = h_q.numel() * 2 + h_table.numel() * 4 + h_lens.numel() * 4
-    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+    h2d = st_in.host.numel()
+    d2h = st_res.host.numel()
     # The same steps from C (no Python or torch between the calls): the library's own
     # end-to-end cost, the headline e2e number.
-    e2e_s = _e2e_from_c(fd, pd, w, h_q, d_q, h_table, table, h_lens, lens, out, h_out, lse, h_lse, stream,
-                        args.warmup, e2e_steps)
+    e2e_s = _e2e_from_c(fd, pd, w, st_in, st_res, stream, args.warmup, e2e_steps)
+    assert torch.equal(st_res.host_views[0], out.cpu()) and torch.equal(st_res.host_views[1], lse.cpu())
 
     # ---- the long-context sweep: per-call time with an L2 flush before each call, and back to back
     # over rotating copies of the K/V pools (each call starting with its pages out of L2)
@@ -906,10 +904,10 @@ def _run_fdec(args):
             "e2e": {"value": round(kv_bytes / e2e_s / 1e9, 1), "unit": "GB/s", "us_per_call": round(e2e_s * 1e6, 2),
                     "python_us_per_call": round(e2e_py_s * 1e6, 2),
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                    "note": "per step: pinned H2D of q, page table and seq_lens (one cudaMemcpyAsync each), "
-                            "fdec_run, D2H of out and lse, stream sync; timed from C (value, us_per_call) and "
-                            "through the Python binding with torch copies (python_us_per_call); the K/V cache "
-                            "stays resident (decode state)"},
+                    "note": "per step: one pinned H2D copy of the staged q, page table and seq_lens, "
+                            "fdec_run, one D2H copy of out and lse (one device buffer), stream sync; timed from C "
+                            "(value, us_per_call) and through the Python binding with torch copies "
+                            "(python_us_per_call); the K/V cache stays resident (decode state)"},
             "gpu_launches": int(info["launches"]) * args.steps,
             "clocks": clocks.summary(),
             "cpu_baseline": cpu,
@@ -922,24 +920,47 @@ def _run_fdec(args):
         dist.destroy_process_group()
 
 
-def _e2e_from_c(fd, pd, w, h_q, d_q, h_table, d_table, h_lens, d_lens, out, h_out, lse, h_lse, stream, warmup,
-                iters) -> float:
+class _Staging:
+    """Tensors packed into one pinned host buffer and one device buffer of the same
+    layout (each tensor 16-byte aligned), with a view of each on both sides; the host
+    views start as copies of the given tensors."""
+
+    def __init__(self, torch, dev, tensors):
+        offs, at = [], 0
+        for t in tensors:
+            offs.append(at)
+            at = (at + t.numel() * t.element_size() + 15) // 16 * 16
+        self.host = torch.zeros(at, dtype=torch.uint8).pin_memory()
+        self.dev = torch.zeros(at, dtype=torch.uint8, device=dev)
+
+        def view(buf, t, off):
+            n = t.numel() * t.element_size()
+            return buf[off:off + n].view(t.dtype).view(t.shape)
+
+        self.host_views = [view(self.host, t, o) for t, o in zip(tensors, offs)]
+        self.dev_views = [view(self.dev, t, o) for t, o in zip(tensors, offs)]
+        for hv, t in zip(self.host_views, tensors):
+            hv.copy_(t.cpu())
+
+
+def _e2e_from_c(fd, pd, w, st_in, st_res, stream, warmup, iters) -> float:
     """Seconds per end-to-end step timed by the C loop in libfdec_e2e.so (e2e/e2e_loop.cu)."""
     import ctypes
 
     lib = ctypes.CDLL(os.path.join(ROOT, "paged_split_kv_gather_gb300", "libfdec_e2e.so"))
     P, I64, S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
     lib.fdec_e2e_loop.restype = ctypes.c_int
-    lib.fdec_e2e_loop.argtypes = [P, P, P, S, I64, I64, fd.KVDesc, fd.KVDesc, P, P, S, I64, P, P, S, ctypes.c_float,
-                                  P, P, S, P, P, S, P, P, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
+    lib.fdec_e2e_loop.argtypes = [P, P, P, S, P, I64, I64, fd.KVDesc, fd.KVDesc, P, I64, P, ctypes.c_float, P, P,
+                                  P, P, S, P, P, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
     from paged_split_kv_gather_gb300.workloads import q_token_stride
 
+    d_q, d_table, d_lens = st_in.dev_views
+    d_out, d_lse = st_res.dev_views
     secs = ctypes.c_double()
-    rc = lib.fdec_e2e_loop(pd.plan.handle, h_q.data_ptr(), d_q.data_ptr(), h_q.numel() * h_q.element_size(),
-                           q_token_stride(d_q), d_q.stride(2), fd.kv_desc(w.k), fd.kv_desc(w.v), h_table.data_ptr(),
-                           d_table.data_ptr(), h_table.numel() * 4, d_table.stride(0), h_lens.data_ptr(),
-                           d_lens.data_ptr(), h_lens.numel() * 4, w.scale, out.data_ptr(), h_out.data_ptr(),
-                           out.numel() * 4, lse.data_ptr(), h_lse.data_ptr(), lse.numel() * 4,
+    rc = lib.fdec_e2e_loop(pd.plan.handle, st_in.host.data_ptr(), st_in.dev.data_ptr(), st_in.host.numel(),
+                           d_q.data_ptr(), q_token_stride(d_q), d_q.stride(2), fd.kv_desc(w.k), fd.kv_desc(w.v),
+                           d_table.data_ptr(), d_table.stride(0), d_lens.data_ptr(), w.scale, d_out.data_ptr(),
+                           d_lse.data_ptr(), st_res.dev.data_ptr(), st_res.host.data_ptr(), st_res.host.numel(),
                            pd.workspace.data_ptr(), stream.cuda_stream, warmup, iters, ctypes.byref(secs))
     if rc != 0:
         raise RuntimeError(f"fdec_e2e_loop failed ({rc}): {fd.fdec_last_error()}")
