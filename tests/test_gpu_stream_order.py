@@ -83,3 +83,37 @@ def test_inputs_written_just_before_the_call_are_read(case):
     pd.run(q, w.k, w.v, table0, torch.as_tensor(caps, device="cuda"), out2, lse2, scale=w.scale, **sc)
     torch.cuda.synchronize()
     assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def _packed(tensors, device):
+    """One uint8 buffer holding every tensor at a 16-byte-aligned offset, and a view of each."""
+    offs, at = [], 0
+    for t in tensors:
+        offs.append(at)
+        at = (at + t.numel() * t.element_size() + 15) // 16 * 16
+    buf = torch.zeros(at, dtype=torch.uint8, device=device)
+    views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(tensors, offs)]
+    for v, t in zip(views, tensors):
+        v.copy_(t)
+    return buf, views
+
+
+@pytest.mark.parametrize("case", ["long_context_page64", "spec_decode_q8_tcgen05"])
+def test_inputs_and_outputs_packed_in_one_buffer(case):
+    # q, the page table and the lengths as views of one device buffer (one host-to-device
+    # copy per step), out and lse as views of another (one copy back): the same result,
+    # bitwise, as separate tensors
+    w = _cases()[case]()
+    pd = fd.PagedDecode(w.seq_lens, w.q_len, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
+                        w.causal, device="cuda")
+    table = torch.as_tensor(w.page_table, device="cuda")
+    lens = torch.as_tensor(w.seq_lens, device="cuda")
+    out = torch.empty((w.batch, w.q_len, w.num_qo_heads, w.head_dim), device="cuda")
+    lse = torch.empty((w.batch, w.q_len, w.num_qo_heads), device="cuda")
+    pd.run(w.q, w.k, w.v, table, lens, out, lse, scale=w.scale)
+    _, (q_p, table_p, lens_p) = _packed([w.q, table, lens], "cuda")
+    _, (out_p, lse_p) = _packed([torch.full_like(out, float("nan")), torch.full_like(lse, float("nan"))], "cuda")
+    pd.run(q_p, w.k, w.v, table_p, lens_p, out_p, lse_p, scale=w.scale)
+    torch.cuda.synchronize()
+    assert pd.device_errors() == 0
+    assert torch.equal(out_p, out) and torch.equal(lse_p, lse)
