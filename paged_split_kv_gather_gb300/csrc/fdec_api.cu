@@ -321,6 +321,22 @@ void log_plan(const fdec_plan_s* p) {
 // and from 64 at 256.
 static int tc_min_rows(int head_dim) { return head_dim >= 256 ? 32 : kMmaRows; }
 
+// A tiny decode: one query token, at most 4 query rows per KV head, head_dim up to
+// 128, every sequence within 5 blocks of 64 tokens and at most one (sequence, KV
+// head) pair per SM.  Measured on GB300 (f16, page 16; graph-replayed µs per call
+// after an L2 eviction, the SIMT kernel against the tensor-core one): 4.3-8.8
+// against 6.4-9.9 at head_dim 64 and 6.6-10.6 against 7.8-12.0 at head_dim 128
+// over 64 and 300 tokens, batches 1 and 4, 1 and 8 KV heads; at 1000 tokens and
+// more, or 8 rows, the tensor-core kernel wins or ties.
+static bool tiny_decode(const int32_t* seq_lens_host, int batch, int q_len, int rows, int num_kv_heads,
+                        int head_dim, int num_sms) {
+    if (q_len != 1 || rows > 4 || head_dim > 128 || static_cast<long long>(batch) * num_kv_heads > num_sms)
+        return false;
+    for (int b = 0; b < batch; ++b)
+        if (seq_lens_host[b] > 5 * kBlockTokens) return false;
+    return true;
+}
+
 extern "C" {
 
 const char* fdec_last_error(void) { return g_last_error.c_str(); }
@@ -398,12 +414,17 @@ fdec_status fdec_plan(const int32_t* seq_lens_host, int batch, int q_len, int pa
     // The warp-level tensor-core kernel by default (every head_dim; see
     // split_mma_kernel.cuh for why tensor cores pay off even when bandwidth-bound);
     // the tcgen05 kernel once the rows need more than one 16-row group (the 16-row
-    // kernel would stream K/V once per group); E4M3 caches always on the former;
-    // the fp32 SIMT kernel only on request.
+    // kernel would stream K/V once per group); E4M3 and q8_0 caches always on the
+    // former.  The fp32 SIMT kernel on request, and for tiny decodes (see
+    // tiny_decode): its shorter prologue (no tensor maps, stage barriers or unit
+    // counter) wins while a call is one short pass over a few pages.
     if (kv8)
         p->path = FDEC_PATH_MMA;
     else if (o.path == FDEC_PATH_AUTO)
-        p->path = (tc_ok && p->rows > tc_min_rows(head_dim)) ? FDEC_PATH_TC : (mma_ok ? FDEC_PATH_MMA : FDEC_PATH_SIMT);
+        p->path = tiny_decode(seq_lens_host, batch, q_len, static_cast<int>(rows_ll), num_kv_heads, head_dim, num_sms)
+                      ? FDEC_PATH_SIMT
+                      : (tc_ok && p->rows > tc_min_rows(head_dim)) ? FDEC_PATH_TC
+                                                                    : (mma_ok ? FDEC_PATH_MMA : FDEC_PATH_SIMT);
     else
         p->path = o.path;
     p->persistent = p->path == FDEC_PATH_MMA && !kv8 && split_mma_persist_supported(head_dim);

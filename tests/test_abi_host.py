@@ -102,8 +102,8 @@ def test_auto_plan_balances_ragged_batches():
 
 def test_path_selection():
     assert fd.fdec_plan_get_info(_plan([100], path=fd.FDEC_PATH_SIMT))["path"] == fd.FDEC_PATH_SIMT
-    for d in (64, 128, 192, 256, 512):
-        assert fd.fdec_plan_get_info(_plan([100], head_dim=d))["path"] == fd.FDEC_PATH_MMA
+    for d in (64, 128, 192, 256, 512):  # (1000 tokens: past the tiny-decode bound)
+        assert fd.fdec_plan_get_info(_plan([1000], head_dim=d))["path"] == fd.FDEC_PATH_MMA
         assert fd.fdec_plan_get_info(_plan([100], head_dim=d, path=fd.FDEC_PATH_SIMT))["path"] == fd.FDEC_PATH_SIMT
     for d in (64, 128, 192, 256):
         assert fd.fdec_plan_get_info(_plan([100], head_dim=d, path=fd.FDEC_PATH_TC))["path"] == fd.FDEC_PATH_TC
@@ -337,6 +337,24 @@ def test_binding_refuses_k_v_of_the_wrong_element_size():
                     out, None, torch.zeros(256, dtype=torch.uint8))
 
 
+def test_tiny_decodes_plan_on_the_simt_kernel():
+    # one token, <= 4 rows per KV head, head_dim <= 128, every sequence within 5 blocks, <= one
+    # (sequence, KV head) pair per SM: the SIMT kernel; one step past any bound: the tensor-core one
+    info = fd.fdec_plan_get_info(_plan([300], num_qo_heads=4, num_kv_heads=1, head_dim=64))
+    assert info["path"] == fd.FDEC_PATH_SIMT and info["launches"] == 1
+    assert fd.fdec_plan_get_info(_plan([320] * 4, num_qo_heads=32, num_kv_heads=8, head_dim=128))["path"] == \
+        fd.FDEC_PATH_SIMT
+    for kw in (dict(lens=[321]), dict(num_qo_heads=8), dict(head_dim=192), dict(q_len=2),
+               dict(lens=[64] * 153)):
+        args = dict(lens=[300], num_qo_heads=4, num_kv_heads=1, head_dim=64)
+        args.update(kw)
+        lens = args.pop("lens")
+        assert fd.fdec_plan_get_info(_plan(lens, **args))["path"] == fd.FDEC_PATH_MMA, kw
+    # quantised caches stay on the tensor-core kernel
+    assert fd.fdec_plan_get_info(_plan([300], num_qo_heads=4, num_kv_heads=1, head_dim=128, kv_dtype="fp8"))[
+        "path"] == fd.FDEC_PATH_MMA
+
+
 def test_plan_invariants_hold_for_random_batches():
     """Property check of the planner over random batches: split counts follow the
     chosen blocks per split, items and CTAs cover every (split, KV head, row group),
@@ -362,7 +380,10 @@ def test_plan_invariants_hold_for_random_batches():
             assert C == bps
         nb = np.maximum(1, -(-np.asarray(lens, dtype=np.int64) // 64))
         rows = q_len * group
-        want_path = (fd.FDEC_PATH_TC if (not kv8 and d in (64, 128, 192, 256) and rows > (32 if d == 256 else 16))
+        tiny = (not kv8 and q_len == 1 and rows <= 4 and d <= 128 and len(lens) * hk <= 152
+                and max(lens) <= 5 * 64)
+        want_path = (fd.FDEC_PATH_SIMT if tiny else
+                     fd.FDEC_PATH_TC if (not kv8 and d in (64, 128, 192, 256) and rows > (32 if d == 256 else 16))
                      else fd.FDEC_PATH_MMA)
         assert info["path"] == want_path
         # the persistent kernel (16-bit caches on the 16-row path; one CTA per SM at head_dim 512)

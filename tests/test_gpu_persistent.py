@@ -67,7 +67,7 @@ CASES = {
 def test_persistent_and_grid_kernels_agree_bitwise(case):
     w = CASES[case]()
     pd = fd.PagedDecode(w.seq_lens, w.q_len, w.page_size, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.dtype,
-                        w.causal, device="cuda")
+                        w.causal, device="cuda", path=fd.FDEC_PATH_MMA)  # (a tiny decode would plan on SIMT)
     table = torch.as_tensor(w.page_table, device="cuda")
     lens = torch.as_tensor(w.seq_lens, device="cuda")
     assert w.q.data_ptr() % 16 == 0
